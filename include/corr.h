@@ -1,0 +1,113 @@
+/*
+ * corr.h -- C ABI of libcorr.so, GB300 (sm_103a) sliding-window 2D
+ * correlation in two forms.
+ *
+ * Plain C types only.  Every buffer pointer is a DEVICE pointer (memory the
+ * caller allocated on the current CUDA device, e.g. a torch tensor's
+ * data_ptr()); the library never frees, keeps or reallocates a caller
+ * buffer.  Calls are asynchronous on the calling thread's stream (see
+ * corr_set_stream) and run on the calling thread's current CUDA device.
+ * Every argument is checked before anything is launched: a call that returns
+ * an error has written nothing.
+ *
+ * Return codes: CORR_OK or one of the negative CORR_E* codes below;
+ * corr_strerror() names them.  After CORR_ECUDA, corr_last_cuda_error()
+ * returns the cudaError_t value that caused it.
+ */
+#ifndef CORR_H_
+#define CORR_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CORR_OK 0
+#define CORR_EINVAL (-1)        /* null pointer, size <= 0, template larger than image */
+#define CORR_EUNSUPPORTED (-2)  /* a size the kernels do not handle (see each call) */
+#define CORR_ECUDA (-3)         /* CUDA runtime error (no device, launch failure, ...) */
+
+/* Largest template (pixels) whose SumISq = sum of 255^2 still fits the
+ * unsigned 32-bit accumulators: 66052 * 65025 < 2^32. */
+#define CORR_NCC_MAX_TEMPLATE_PIXELS 66052
+
+/*
+ * corr_ncc_u8 -- 8-bit normalized cross-correlation (template matching).
+ *
+ * Defined by The CUDA Handbook, ch. 15 "Image Processing: Normalized
+ * Correlation", section 15.5 "Instruction-Level Parallelism and DP4A": for
+ * every valid offset (x, y), 0 <= x <= w-wt, 0 <= y <= h-ht, the exact
+ * unsigned 32-bit sums over the template window
+ *     SumI   = sum_{j<ht,i<wt} I[y+j][x+i]
+ *     SumISq = sum I[y+j][x+i]^2
+ *     SumIT  = sum I[y+j][x+i] * T[j][i]
+ * and the normalized coefficient (N = wt*ht, SumT / SumTSq the template's
+ * sum and sum of squares)
+ *     coef = (N*SumIT - SumI*SumT) / sqrt((N*SumISq - SumI^2)(N*SumTSq - SumT^2)),
+ * with coef = 0 where either variance term is zero (flat window or flat
+ * template).  Numerator and variance terms are exact 64-bit integers; the
+ * final ratio is single precision (within 1e-5 absolute of the exact value).
+ *
+ *   image     device, w*h bytes, row-major, row pitch w bytes (any alignment;
+ *             8-byte aligned image with w % 8 == 0 takes the fast path).
+ *   w, h      image width and height in pixels, > 0.
+ *   tmpl      device, wt*ht bytes, row-major, pitch wt.
+ *   wt, ht    template size, 0 < wt <= w, 0 < ht <= h; wt must be a
+ *             multiple of 4 (the template packs into whole 32-bit words) and
+ *             wt*ht <= CORR_NCC_MAX_TEMPLATE_PIXELS, else CORR_EUNSUPPORTED.
+ *   sums_out  device, 3 planes [3][oh][ow] of uint32 (SumI, SumISq, SumIT),
+ *             ow = w-wt+1, oh = h-ht+1, dense, y-major; or NULL to skip.
+ *   coef_out  device, [oh][ow] float32, dense; or NULL to skip.
+ *             At least one of sums_out / coef_out must be non-NULL.
+ */
+int corr_ncc_u8(const uint8_t *image, int w, int h, const uint8_t *tmpl,
+                int wt, int ht, uint32_t *sums_out, float *coef_out);
+
+/*
+ * corr_xcorr_f32 -- float32 full 2D cross-correlation, all overlaps.
+ *
+ * Defined by the "Efficient GPU-accelerated Parallel Cross-correlation"
+ * artifact README (kernel overview: each output is one overlap of a left and
+ * a right matrix; all overlaps are computed; one-to-one, one-to-many and
+ * n-to-m batches).  For every pair (li, ri) and shift (dy, dx) with
+ * |dy| < H, |dx| < W:
+ *     out[li][ri][dy+H-1][dx+W-1] = sum_{y,x} L_li[y][x] * R_ri[y-dy][x-dx]
+ * over the (y, x) where both matrices are indexed inside their bounds (the
+ * same convention as scipy.signal.correlate2d(L, R, mode="full")).  Sums are
+ * accumulated in float32; each output is within 1e-5 * sum |L*R| (over the
+ * same overlap) of the exact value.
+ *
+ *   left      device, nl matrices [nl][H][W] float32, contiguous, 4-byte aligned.
+ *   nl        number of left matrices, > 0 (1 for one-to-one and one-to-many).
+ *   right     device, [nr][H][W] float32, contiguous, 4-byte aligned.
+ *   nr        number of right matrices, > 0.
+ *   H, W      matrix height and width, > 0.
+ *   out       device, [nl][nr][2H-1][2W-1] float32, dense; pair li*nr+ri.
+ *
+ * May allocate and free temporary device memory on the current stream
+ * (stream-ordered) for shapes it splits across blocks; returns CORR_ECUDA if
+ * that allocation fails.
+ */
+int corr_xcorr_f32(const float *left, int nl, const float *right, int nr,
+                   int H, int W, float *out);
+
+/* Stream for this thread's following calls (a cudaStream_t; NULL = the
+ * legacy default stream).  Thread-local; never fails. */
+int corr_set_stream(void *stream);
+void *corr_get_stream(void);
+
+/* Human-readable name of a return code (static string). */
+const char *corr_strerror(int code);
+
+/* cudaError_t behind this thread's most recent CORR_ECUDA (0 if none). */
+int corr_last_cuda_error(void);
+
+/* Library ABI version (major*100 + minor). */
+int corr_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CORR_H_ */

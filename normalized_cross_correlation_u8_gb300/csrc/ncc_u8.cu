@@ -1,0 +1,363 @@
+// ncc_u8.cu -- 8-bit normalized cross-correlation on sm_103a.
+//
+// Method (The CUDA Handbook, ch. 15 "Image Processing: Normalized
+// Correlation", section 15.5 "Instruction-Level Parallelism and DP4A"):
+// four pixels are packed into one 32-bit word and each of the three sums
+// advances by one *unsigned* __dp4a per word (SumI against 0x01010101,
+// SumISq against the word itself, SumIT against the packed template word).
+// Consecutive output columns slide the window by one byte, so a thread's
+// window words are cut out of two aligned image words with __funnelshift_r;
+// the template, whose width is a multiple of four, packs directly.  Several
+// independent output columns (and rows) per thread keep many accumulation
+// chains in flight (the section's instruction-level parallelism).
+//
+// GB300 layout of the work:
+//   * one warp owns a unit of 256 output columns x R output rows; each lane
+//     owns 8 adjacent columns (x0 = 8*lane, so its words start 8-byte
+//     aligned) and the same R rows;
+//   * the warp walks the image rows k = y0 .. y0+R+ht-2 once; every image
+//     row is loaded (8-byte vector loads through L1) and cut into windows
+//     once, then paired with template row k-r for each of its R output rows,
+//     so loads and funnel shifts are shared by R rows;
+//   * the template lives in shared memory (read as warp-uniform 16-byte
+//     broadcasts); each CTA also reduces SumT / SumTSq from it;
+//   * the epilogue forms N*SumIT - SumI*SumT and N*SumISq - SumI^2 exactly in
+//     64-bit integers before the single-precision ratio.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "internal.cuh"
+
+namespace corr {
+namespace {
+
+constexpr int kCols = 8;                   // output columns per lane
+constexpr int kUnitCols = 32 * kCols;      // output columns per warp unit
+constexpr int kWarpsPerCta = 4;
+constexpr int kThreads = 32 * kWarpsPerCta;
+constexpr uint32_t kOnes = 0x01010101u;
+
+struct NccArgs {
+  const uint8_t *image;
+  const uint8_t *tmpl;
+  uint32_t *sums;
+  float *coef;
+  size_t plane;      // ow * oh
+  int w, h, wt, ht;
+  int wtw;           // template words per row (wt / 4)
+  int wtp;           // shared-memory template row stride in words (multiple of 4)
+  int ow, oh;
+  int tiles_x;       // units across a row of outputs
+  int units;         // tiles_x * ceil(oh / R)
+};
+
+__device__ __forceinline__ uint32_t fshr(uint32_t lo, uint32_t hi, int bytes) {
+  return __funnelshift_r(lo, hi, 8 * bytes);
+}
+
+// Four bytes of image row `row` starting at byte `off`; bytes at or past w
+// read as zero (they only ever feed columns past the last valid offset).
+__device__ __forceinline__ uint32_t load_word_bytes(const uint8_t *row, int off,
+                                                    int w) {
+  uint32_t v = 0;
+#pragma unroll
+  for (int b = 0; b < 4; ++b)
+    if (off + b < w) v |= uint32_t(__ldg(row + off + b)) << (8 * b);
+  return v;
+}
+
+// Stage the template into shared memory as 32-bit words (row stride wtp,
+// zero padded) and reduce SumT, SumTSq over the CTA.
+__device__ __forceinline__ void stage_template(const NccArgs &a, uint32_t *tmpl_s,
+                                               uint32_t *red, uint32_t &sum_t,
+                                               uint32_t &sum_t_sq) {
+  if (threadIdx.x < 2) red[threadIdx.x] = 0;
+  __syncthreads();
+  const bool aligned4 = (reinterpret_cast<uintptr_t>(a.tmpl) & 3) == 0;
+  uint32_t s = 0, q = 0;
+  const int total = a.ht * a.wtp;
+  for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
+    const int j = idx / a.wtp, i = idx - j * a.wtp;
+    uint32_t v = 0;
+    if (i < a.wtw) {
+      const int byte = j * a.wt + 4 * i;
+      if (aligned4) {
+        v = __ldg(reinterpret_cast<const uint32_t *>(a.tmpl + byte));
+      } else {
+#pragma unroll
+        for (int b = 0; b < 4; ++b) v |= uint32_t(__ldg(a.tmpl + byte + b)) << (8 * b);
+      }
+    }
+    tmpl_s[idx] = v;
+    s = __dp4a(v, kOnes, s);
+    q = __dp4a(v, v, q);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    s += __shfl_xor_sync(0xffffffffu, s, o);
+    q += __shfl_xor_sync(0xffffffffu, q, o);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    atomicAdd(&red[0], s);
+    atomicAdd(&red[1], q);
+  }
+  __syncthreads();
+  sum_t = red[0];
+  sum_t_sq = red[1];
+}
+
+// Three unsigned dp4a per window: the section's inner step.
+template <int R>
+__device__ __forceinline__ void accum_window(uint32_t (&sI)[R][kCols],
+                                             uint32_t (&sQ)[R][kCols],
+                                             uint32_t (&sT)[R][kCols], int r,
+                                             int c, uint32_t win, uint32_t tw) {
+  sI[r][c] = __dp4a(win, kOnes, sI[r][c]);
+  sQ[r][c] = __dp4a(win, win, sQ[r][c]);
+  sT[r][c] = __dp4a(win, tw, sT[r][c]);
+}
+
+// Write the sums and the coefficient of one lane's R x 8 block.
+template <int R>
+__device__ __forceinline__ void epilogue(const NccArgs &a, int x0, int y0,
+                                         const uint32_t (&sI)[R][kCols],
+                                         const uint32_t (&sQ)[R][kCols],
+                                         const uint32_t (&sT)[R][kCols],
+                                         uint32_t sum_t, uint32_t sum_t_sq) {
+  const int64_t n = int64_t(a.wt) * a.ht;
+  const int64_t d_t = n * int64_t(sum_t_sq) - int64_t(sum_t) * int64_t(sum_t);
+  const float d_tf = float(d_t);
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int y = y0 + r;
+    if (y >= a.oh) break;
+#pragma unroll
+    for (int c = 0; c < kCols; ++c) {
+      const int x = x0 + c;
+      if (x >= a.ow) break;
+      const size_t o = size_t(y) * a.ow + x;
+      if (a.sums) {
+        a.sums[o] = sI[r][c];
+        a.sums[a.plane + o] = sQ[r][c];
+        a.sums[2 * a.plane + o] = sT[r][c];
+      }
+      if (a.coef) {
+        const int64_t si = sI[r][c];
+        const int64_t num = n * int64_t(sT[r][c]) - si * int64_t(sum_t);
+        const int64_t d_i = n * int64_t(sQ[r][c]) - si * si;
+        float cf = 0.f;
+        if (d_i > 0 && d_t > 0) cf = float(num) / sqrtf(float(d_i) * d_tf);
+        a.coef[o] = cf;
+      }
+    }
+  }
+}
+
+// One image row (tile-relative index rel = k - y0) against template rows
+// rel - r for the R output rows r of the unit; `mask` selects the rows r for
+// which 0 <= rel - r < ht (all of them when FULL).
+template <int R, int WT, bool FULL>
+__device__ __forceinline__ void row_fixed(const uint32_t (&wv)[WT + 2],
+                                          const uint32_t *tmpl_s, int rel,
+                                          unsigned mask, uint32_t (&sI)[R][kCols],
+                                          uint32_t (&sQ)[R][kCols],
+                                          uint32_t (&sT)[R][kCols]) {
+  constexpr int WTP = (WT + 3) & ~3;
+#pragma unroll
+  for (int ib = 0; ib < WT; ib += 4) {
+    uint4 tq[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+      if (FULL || ((mask >> r) & 1u))
+        tq[r] = *reinterpret_cast<const uint4 *>(tmpl_s + (rel - r) * WTP + ib);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int i = ib + m;
+      if (i >= WT) break;
+      uint32_t win[kCols];
+#pragma unroll
+      for (int c = 0; c < kCols; ++c) {
+        const int k = i + (c >> 2), s = c & 3;
+        win[c] = s == 0 ? wv[k] : fshr(wv[k], wv[k + 1], s);
+      }
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        if (!(FULL || ((mask >> r) & 1u))) continue;
+        const uint32_t tw = m == 0 ? tq[r].x : m == 1 ? tq[r].y : m == 2 ? tq[r].z : tq[r].w;
+#pragma unroll
+        for (int c = 0; c < kCols; ++c) accum_window<R>(sI, sQ, sT, r, c, win[c], tw);
+      }
+    }
+  }
+}
+
+// Fast path: template width WT words known at compile time, image pointer
+// and width 8-byte aligned, so every lane reads its WT+2 words as (WT+2)/2
+// aligned 8-byte loads (a pair never straddles the row end since w % 8 == 0).
+template <int R, int WT>
+__global__ void __launch_bounds__(kThreads)
+    ncc_u8_fixed_kernel(const NccArgs a) {
+  extern __shared__ uint4 smem_u4[];
+  uint32_t *tmpl_s = reinterpret_cast<uint32_t *>(smem_u4);
+  __shared__ uint32_t red[2];
+  uint32_t sum_t, sum_t_sq;
+  stage_template(a, tmpl_s, red, sum_t, sum_t_sq);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int unit = blockIdx.x * kWarpsPerCta + warp;
+  if (unit >= a.units) return;
+  const int tx = unit % a.tiles_x, rb = unit / a.tiles_x;
+  const int x0 = tx * kUnitCols + lane * kCols;
+  const int y0 = rb * R;
+
+  uint32_t sI[R][kCols], sQ[R][kCols], sT[R][kCols];
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+#pragma unroll
+    for (int c = 0; c < kCols; ++c) sI[r][c] = sQ[r][c] = sT[r][c] = 0;
+
+  const int nrows = min(R + a.ht - 1, a.h - y0);
+  constexpr int NP = (WT + 2) / 2;  // 8-byte pairs per row (WT even)
+  static_assert(WT % 2 == 0, "fixed path expects an even word count");
+  uint32_t wv[WT + 2], nx[WT + 2];
+
+  auto load_row = [&](int rel, uint32_t (&dst)[WT + 2]) {
+    const uint8_t *row = a.image + size_t(y0 + rel) * a.w;
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+      const int off = x0 + 8 * p;
+      uint2 v = make_uint2(0u, 0u);
+      if (off < a.w) v = __ldg(reinterpret_cast<const uint2 *>(row + off));
+      dst[2 * p] = v.x;
+      dst[2 * p + 1] = v.y;
+    }
+  };
+
+  load_row(0, nx);
+  for (int rel = 0; rel < nrows; ++rel) {
+#pragma unroll
+    for (int k = 0; k < WT + 2; ++k) wv[k] = nx[k];
+    if (rel + 1 < nrows) load_row(rel + 1, nx);
+    if (rel >= R - 1 && rel <= a.ht - 1) {
+      row_fixed<R, WT, true>(wv, tmpl_s, rel, 0u, sI, sQ, sT);
+    } else {
+      unsigned mask = 0;
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+        if (rel - r >= 0 && rel - r < a.ht) mask |= 1u << r;
+      row_fixed<R, WT, false>(wv, tmpl_s, rel, mask, sI, sQ, sT);
+    }
+  }
+  epilogue<R>(a, x0, y0, sI, sQ, sT, sum_t, sum_t_sq);
+}
+
+// General path: any template width (multiple of 4) and any image alignment.
+// Same decomposition; words are assembled from bytes and the template row is
+// walked one word at a time.
+template <int R>
+__global__ void __launch_bounds__(kThreads)
+    ncc_u8_general_kernel(const NccArgs a) {
+  extern __shared__ uint4 smem_u4[];
+  uint32_t *tmpl_s = reinterpret_cast<uint32_t *>(smem_u4);
+  __shared__ uint32_t red[2];
+  uint32_t sum_t, sum_t_sq;
+  stage_template(a, tmpl_s, red, sum_t, sum_t_sq);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int unit = blockIdx.x * kWarpsPerCta + warp;
+  if (unit >= a.units) return;
+  const int tx = unit % a.tiles_x, rb = unit / a.tiles_x;
+  const int x0 = tx * kUnitCols + lane * kCols;
+  const int y0 = rb * R;
+
+  uint32_t sI[R][kCols], sQ[R][kCols], sT[R][kCols];
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+#pragma unroll
+    for (int c = 0; c < kCols; ++c) sI[r][c] = sQ[r][c] = sT[r][c] = 0;
+
+  const int nrows = min(R + a.ht - 1, a.h - y0);
+  for (int rel = 0; rel < nrows; ++rel) {
+    const uint8_t *row = a.image + size_t(y0 + rel) * a.w;
+    unsigned mask = 0;
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+      if (rel - r >= 0 && rel - r < a.ht) mask |= 1u << r;
+    uint32_t w0 = load_word_bytes(row, x0, a.w);
+    uint32_t w1 = load_word_bytes(row, x0 + 4, a.w);
+    for (int i = 0; i < a.wtw; ++i) {
+      const uint32_t w2 = load_word_bytes(row, x0 + 4 * (i + 2), a.w);
+      uint32_t win[kCols];
+      win[0] = w0;
+      win[1] = fshr(w0, w1, 1);
+      win[2] = fshr(w0, w1, 2);
+      win[3] = fshr(w0, w1, 3);
+      win[4] = w1;
+      win[5] = fshr(w1, w2, 1);
+      win[6] = fshr(w1, w2, 2);
+      win[7] = fshr(w1, w2, 3);
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        if (!((mask >> r) & 1u)) continue;
+        const uint32_t tw = tmpl_s[(rel - r) * a.wtp + i];
+#pragma unroll
+        for (int c = 0; c < kCols; ++c) accum_window<R>(sI, sQ, sT, r, c, win[c], tw);
+      }
+      w0 = w1;
+      w1 = w2;
+    }
+  }
+  epilogue<R>(a, x0, y0, sI, sQ, sT, sum_t, sum_t_sq);
+}
+
+template <typename Kernel>
+cudaError_t launch(Kernel kernel, const NccArgs &a, size_t smem,
+                   cudaStream_t stream) {
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(
+        kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+  }
+  const int blocks = (a.units + kWarpsPerCta - 1) / kWarpsPerCta;
+  kernel<<<blocks, kThreads, smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t ncc_u8_launch(const uint8_t *image, int w, int h,
+                          const uint8_t *tmpl, int wt, int ht,
+                          uint32_t *sums_out, float *coef_out,
+                          cudaStream_t stream) {
+  constexpr int R = 2;
+  NccArgs a;
+  a.image = image;
+  a.tmpl = tmpl;
+  a.sums = sums_out;
+  a.coef = coef_out;
+  a.w = w;
+  a.h = h;
+  a.wt = wt;
+  a.ht = ht;
+  a.wtw = wt / 4;
+  a.wtp = (a.wtw + 3) & ~3;
+  a.ow = w - wt + 1;
+  a.oh = h - ht + 1;
+  a.plane = size_t(a.ow) * a.oh;
+  a.tiles_x = (a.ow + kUnitCols - 1) / kUnitCols;
+  a.units = a.tiles_x * ((a.oh + R - 1) / R);
+  const size_t smem = size_t(ht) * a.wtp * 4;
+
+  const bool aligned8 = (reinterpret_cast<uintptr_t>(image) & 7) == 0 && (w & 7) == 0;
+  if (aligned8) {
+    switch (a.wtw) {
+      case 4: return launch(ncc_u8_fixed_kernel<R, 4>, a, smem, stream);
+      case 8: return launch(ncc_u8_fixed_kernel<R, 8>, a, smem, stream);
+      case 16: return launch(ncc_u8_fixed_kernel<R, 16>, a, smem, stream);
+      default: break;
+    }
+  }
+  return launch(ncc_u8_general_kernel<R>, a, smem, stream);
+}
+
+}  // namespace corr

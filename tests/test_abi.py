@@ -1,0 +1,88 @@
+"""The C-ABI library builds, loads and exports every declared entry point;
+argument errors come back as codes before anything reaches the GPU (these
+tests make no compute call and need no GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import normalized_cross_correlation_u8_gb300 as corr
+from normalized_cross_correlation_u8_gb300 import _binding
+
+INCLUDE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+FAKE = ctypes.c_void_p(0x100000)    # never dereferenced: every call below fails validation
+
+
+def declared_functions():
+    names = set()
+    for fn in sorted(os.listdir(INCLUDE)):
+        if fn.endswith(".h"):
+            src = open(os.path.join(INCLUDE, fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(corr_\w+)\s*\(", src))
+    return sorted(names)
+
+
+def test_headers_declare_functions():
+    names = declared_functions()
+    assert "corr_ncc_u8" in names and "corr_xcorr_f32" in names
+    assert set(names) == set(_binding.EXPORTS), "binding and headers disagree"
+
+
+@pytest.mark.parametrize("name", declared_functions())
+def test_library_exports_declared_symbol(name):
+    lib = corr.load()
+    assert hasattr(lib, name), f"libcorr.so does not export {name}"
+
+
+def test_version_and_strerror():
+    lib = corr.load()
+    assert lib.corr_version() >= 100
+    for code in (0, -1, -2, -3):
+        assert lib.corr_strerror(code)
+    assert lib.corr_strerror(-99) == b"unknown error code"
+    assert lib.corr_last_cuda_error() == 0
+
+
+def test_stream_is_thread_local_setting():
+    lib = corr.load()
+    lib.corr_set_stream(ctypes.c_void_p(0x1234))
+    assert lib.corr_get_stream() == 0x1234
+    lib.corr_set_stream(None)
+    assert lib.corr_get_stream() is None
+
+
+@pytest.mark.parametrize("args,code", [
+    ((None, 16, 16, FAKE, 4, 4, FAKE, FAKE), -1),            # null image
+    ((FAKE, 16, 16, None, 4, 4, FAKE, FAKE), -1),            # null template
+    ((FAKE, 16, 16, FAKE, 4, 4, None, None), -1),            # no output at all
+    ((FAKE, 0, 16, FAKE, 4, 4, FAKE, FAKE), -1),             # empty image
+    ((FAKE, 16, 16, FAKE, 20, 4, FAKE, FAKE), -1),           # template wider
+    ((FAKE, 16, 16, FAKE, 4, 17, FAKE, FAKE), -1),           # template taller
+    ((FAKE, 16, 16, FAKE, 6, 4, FAKE, FAKE), -2),            # wt % 4 != 0
+    ((FAKE, 1000, 1000, FAKE, 260, 260, FAKE, FAKE), -2),    # > 66052 pixels
+    ((FAKE, 16, 16, FAKE, -4, 4, FAKE, FAKE), -1),
+])
+def test_ncc_argument_errors(args, code):
+    assert corr.load().corr_ncc_u8(*args) == code
+
+
+@pytest.mark.parametrize("args,code", [
+    ((None, 1, FAKE, 1, 4, 4, FAKE), -1),
+    ((FAKE, 1, FAKE, 1, 4, 4, None), -1),
+    ((FAKE, 0, FAKE, 1, 4, 4, FAKE), -1),
+    ((FAKE, 1, FAKE, 1, 0, 4, FAKE), -1),
+    ((ctypes.c_void_p(0x100002), 1, FAKE, 1, 4, 4, FAKE), -1),   # misaligned float*
+    ((FAKE, 70000, FAKE, 70000, 4, 4, FAKE), -2),               # pair count > int
+])
+def test_xcorr_argument_errors(args, code):
+    assert corr.load().corr_xcorr_f32(*args) == code
+
+
+def test_no_gpu_means_loud_failure():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(RuntimeError):
+        corr.ncc_u8(torch.zeros(8, 8, dtype=torch.uint8), torch.zeros(4, 4, dtype=torch.uint8))

@@ -1,0 +1,225 @@
+"""GPU parity of corr_ncc_u8 against the CPU oracle.
+
+Bar (The CUDA Handbook ch. 15, section 15.5 sums; normalized coefficient):
+SumI, SumISq, SumIT bit-exact; coefficient within 1e-5 absolute of the
+oracle's double-precision value from the exact sums.  Inputs always contain
+pixels above 127 and asymmetric templates (where signed-dp4a and byte-order
+slips show).  All calls go through the C ABI via the ctypes binding.
+"""
+import glob
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import normalized_cross_correlation_u8_gb300 as corr
+import oracle
+from normalized_cross_correlation_u8_gb300 import workloads as wl
+from tests.golden.make_golden import read_fixture
+
+pytestmark = pytest.mark.gpu
+COEF_TOL = 1e-5
+NT = max(1, os.cpu_count() or 1)
+RNG = np.random.default_rng(424242)
+
+
+def run_gpu(image, tmpl, sums=True, coef=True):
+    dev = torch.device("cuda", 0)
+    s, c = corr.ncc_u8(torch.from_numpy(image).to(dev), torch.from_numpy(tmpl).to(dev),
+                       sums=sums, coef=coef)
+    torch.cuda.synchronize()
+    s = s.cpu().numpy().view(np.uint32) if s is not None else None
+    c = c.cpu().numpy() if c is not None else None
+    return s, c
+
+
+def assert_parity(image, tmpl, s, c, ref=None):
+    if ref is None:
+        ref = oracle.ncc_u8(image, tmpl, nthreads=NT)
+    rs, rc64, _ = ref
+    if s is not None:
+        assert s.shape == rs.shape
+        bad = np.argwhere(s != rs)
+        assert bad.size == 0, f"{len(bad)} sum mismatches, first {bad[:5].tolist()}"
+    if c is not None:
+        assert c.shape == rc64.shape
+        err = np.abs(c.astype(np.float64) - rc64)
+        assert err.max() <= COEF_TOL, f"coef max err {err.max()} at {np.unravel_index(err.argmax(), err.shape)}"
+
+
+def rand_u8(h, w, lo=0, hi=256):
+    return RNG.integers(lo, hi, size=(h, w), dtype=np.uint8)
+
+
+@pytest.mark.parametrize("path", sorted(glob.glob(os.path.join(
+    os.path.dirname(__file__), "golden", "ncc_u8_*.txt"))))
+def test_fixture(path):
+    fx = read_fixture(path)
+    image, tmpl = fx["image"].astype(np.uint8), fx["tmpl"].astype(np.uint8)
+    s, c = run_gpu(image, tmpl)
+    np.testing.assert_array_equal(s, fx["sums"])
+    assert np.abs(c - fx["coef"]).max() <= COEF_TOL
+
+
+# fast path (wt in 16/32/64, w % 8 == 0) and general path shapes; ragged
+# tails in both directions (ow not a multiple of 256, oh odd)
+SHAPES = [
+    (40, 64, 16, 16), (97, 296, 16, 16), (77, 520, 32, 32), (130, 264, 64, 64),
+    (33, 1000, 32, 7), (50, 600, 64, 3), (21, 256, 16, 21),
+    (45, 300, 4, 3), (39, 100, 12, 5), (61, 333, 20, 9), (70, 515, 36, 11),
+    (16, 16, 16, 16), (9, 4, 4, 1), (5, 260, 128, 5), (300, 20, 8, 200),
+    (1, 1024, 64, 1), (200, 8, 8, 64),
+]
+
+
+@pytest.mark.parametrize("h,w,wt,ht", SHAPES)
+def test_random_shapes(h, w, wt, ht):
+    image, tmpl = rand_u8(h, w), rand_u8(ht, wt)
+    tmpl[0, :] = 255
+    tmpl[-1, -1] = 0
+    s, c = run_gpu(image, tmpl)
+    assert_parity(image, tmpl, s, c)
+
+
+def test_byte_order_single_hot_byte():
+    """Hot byte at each position of a 2-row, 16-wide template in turn."""
+    image = rand_u8(40, 264, 128, 256)
+    for j in range(2):
+        for i in range(16):
+            tmpl = np.zeros((2, 16), np.uint8)
+            tmpl[j, i] = 200
+            s, c = run_gpu(image, tmpl)
+            assert_parity(image, tmpl, s, c)
+
+
+def test_unaligned_image_pointer_and_width():
+    """Image viewed at a 1-byte offset (general path) and w % 8 != 0."""
+    base = rand_u8(1, 64 * 301 + 1).ravel()
+    dev = torch.device("cuda", 0)
+    tb = torch.from_numpy(base).to(dev)
+    img_t = tb[1:].view(64, 301)
+    tmpl = rand_u8(8, 32)
+    s, c = corr.ncc_u8(img_t, torch.from_numpy(tmpl).to(dev))
+    torch.cuda.synchronize()
+    assert_parity(base[1:].reshape(64, 301), tmpl, s.cpu().numpy().view(np.uint32), c.cpu().numpy())
+
+
+def test_single_offset_and_thin_shapes():
+    for (h, w, wt, ht) in [(16, 16, 16, 16), (7, 8, 8, 7), (1, 4, 4, 1), (3, 4, 4, 1), (1, 9, 4, 1)]:
+        image, tmpl = rand_u8(h, w), rand_u8(ht, wt)
+        s, c = run_gpu(image, tmpl)
+        assert_parity(image, tmpl, s, c)
+
+
+def test_largest_template():
+    """wt*ht = 66048 <= 66052: SumISq close to the uint32 limit."""
+    image, tmpl = rand_u8(260, 264, 200, 256), rand_u8(258, 256, 200, 256)
+    s, c = run_gpu(image, tmpl)
+    assert_parity(image, tmpl, s, c)
+    assert s[1].max() > 2 ** 31   # the top bit of SumISq is in use
+
+
+def test_flat_window_and_flat_template_give_zero():
+    image = rand_u8(40, 300)
+    image[10:30, 100:200] = 77
+    tmpl = rand_u8(8, 16)
+    s, c = run_gpu(image, tmpl)
+    assert_parity(image, tmpl, s, c)
+    assert (c[10:23, 100:185] == 0).all()
+    s, c = run_gpu(image, np.full((8, 16), 9, np.uint8))
+    assert (c == 0).all()
+    assert_parity(image, np.full((8, 16), 9, np.uint8), s, c)
+
+
+def test_sums_only_and_coef_only():
+    image, tmpl = rand_u8(70, 270), rand_u8(16, 16)
+    ref = oracle.ncc_u8(image, tmpl, nthreads=NT)
+    s, _ = run_gpu(image, tmpl, sums=True, coef=False)
+    assert_parity(image, tmpl, s, None, ref)
+    _, c = run_gpu(image, tmpl, sums=False, coef=True)
+    assert_parity(image, tmpl, None, c, ref)
+
+
+def test_guard_bands_untouched():
+    """Outputs written into the middle of larger buffers: the canaries on
+    both sides must survive."""
+    image, tmpl = rand_u8(57, 333), rand_u8(9, 20)
+    oh, ow = 57 - 9 + 1, 333 - 20 + 1
+    dev = torch.device("cuda", 0)
+    pad = 4096
+    sb = torch.full((3 * oh * ow + 2 * pad,), -559038737, dtype=torch.int32, device=dev)
+    cb = torch.full((oh * ow + 2 * pad,), 12345.0, dtype=torch.float32, device=dev)
+    s = sb[pad:pad + 3 * oh * ow].view(3, oh, ow)
+    c = cb[pad:pad + oh * ow].view(oh, ow)
+    corr.ncc_u8_into(torch.from_numpy(image).to(dev), torch.from_numpy(tmpl).to(dev), s, c)
+    torch.cuda.synchronize()
+    assert (sb[:pad] == -559038737).all() and (sb[-pad:] == -559038737).all()
+    assert (cb[:pad] == 12345.0).all() and (cb[-pad:] == 12345.0).all()
+    assert_parity(image, tmpl, s.cpu().numpy().view(np.uint32), c.cpu().numpy())
+
+
+def test_argument_errors_raise():
+    dev = torch.device("cuda", 0)
+    img = torch.zeros(32, 32, dtype=torch.uint8, device=dev)
+    with pytest.raises(corr.CorrError) as e:
+        corr.ncc_u8(img, torch.zeros(4, 6, dtype=torch.uint8, device=dev))
+    assert e.value.code == -2
+
+
+def test_host_tensors_round_trip():
+    image, tmpl = rand_u8(50, 200), rand_u8(8, 12)
+    s, c = corr.ncc_u8(torch.from_numpy(image).pin_memory(), torch.from_numpy(tmpl))
+    assert not s.is_cuda and not c.is_cuda
+    assert_parity(image, tmpl, s.numpy().view(np.uint32), c.numpy())
+
+
+def test_nondefault_stream():
+    image, tmpl = rand_u8(90, 400), rand_u8(32, 32)
+    dev = torch.device("cuda", 0)
+    st = torch.cuda.Stream(dev)
+    ti, tt = torch.from_numpy(image).to(dev), torch.from_numpy(tmpl).to(dev)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(st):
+        s, c = corr.ncc_u8(ti, tt)
+    st.synchronize()
+    assert_parity(image, tmpl, s.cpu().numpy().view(np.uint32), c.cpu().numpy())
+
+
+# ---- the named workloads ------------------------------------------------
+
+def test_workload_256_full():
+    w = wl.ncc_256()
+    s, c = run_gpu(w.image, w.tmpl)
+    assert_parity(w.image, w.tmpl, s, c)
+    x, y = w.offset
+    assert c[y, x] == pytest.approx(1.0, abs=1e-6)
+
+
+def test_workload_1080p_full():
+    w = wl.ncc_1080p()
+    s, c = run_gpu(w.image, w.tmpl)
+    assert_parity(w.image, w.tmpl, s, c)
+    x, y = w.offset
+    assert np.unravel_index(np.argmax(c), c.shape) == (y, x)   # soft: expected peak
+
+
+def test_workload_4k_sampled():
+    """Full 4033x4033 launch, compared on sampled offsets (rows at both
+    edges, the template's own offset, random interior points)."""
+    w = wl.ncc_4k()
+    s, c = run_gpu(w.image, w.tmpl)
+    oh, ow = c.shape
+    x0, y0 = w.offset
+    ys = np.concatenate([RNG.integers(0, oh, 400), [0, 0, oh - 1, oh - 1, y0]])
+    xs = np.concatenate([RNG.integers(0, ow, 400), [0, ow - 1, 0, ow - 1, x0]])
+    rs, rc = oracle.ncc_u8_at(w.image, w.tmpl, xs, ys)
+    np.testing.assert_array_equal(s[:, ys, xs], rs)
+    assert np.abs(c[ys, xs] - rc).max() <= COEF_TOL
+    assert c[y0, x0] == pytest.approx(1.0, abs=1e-6)
+    assert np.abs(c).max() <= 1.0 + 1e-6
+    # a full band of rows at the bottom edge, all columns
+    band = w.image[oh - 3:, :]
+    rb, rcb, _ = oracle.ncc_u8(band, w.tmpl, nthreads=NT)
+    np.testing.assert_array_equal(s[:, oh - 3:, :], rb)
+    assert np.abs(c[oh - 3:, :] - rcb).max() <= COEF_TOL
