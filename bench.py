@@ -1,0 +1,463 @@
+"""Benchmark of the sliding-window correlation path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one corr_ncc_u8 call over the 1920x1080 uint8 image with a 32x32
+template (every valid offset: SumI, SumISq, SumIT and the coefficient), i.e.
+template prep, tile loads, window packing, dp4a accumulation and the
+epilogue, all in one launch.  Inputs are resident in HBM when the timed
+region starts; a 256 MB buffer is written between steps so every step starts
+with a cold L2 (the workload's inputs and outputs would otherwise fit in the
+129 MB L2).  Prints one JSON line.
+
+The line also carries, per workload, the kernel-only throughput and its
+roofline fraction for the other five workloads (u8 256x256 / 4096x4096 and
+the three f32 cross-correlation batches), an end-to-end number through host
+buffers, and the CPU oracle's throughput on a bounded sample.
+
+--impl reference times the CPU oracle (the only reference implementation:
+the pages ship no code) on the same workload and metric.
+
+Multi-GPU (torchrun): every rank runs an independent replica of the step on
+its own GPU (the workload has no exchange step); value = all ranks' offsets /
+the slowest rank's time.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "NCC offsets/s (u8) and xcorr GFLOP/s (f32) on 1 GB300; % of roofline"
+UNIT = "offsets/s"
+HEADLINE = "ncc_1080p"
+SM_MAX_MHZ_NOMINAL = 2070.0
+DP4A_PER_SM_CLK = 64     # unsigned dp4a issue per SM per clock (probe: 63.7)
+FFMA_PER_SM_CLK = 128    # FP32 FMA per SM per clock (probe: 124 at live clock)
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--extras", type=int, default=1,
+                   help="1: also measure the other workloads, e2e and CPU baseline")
+    return p.parse_args()
+
+
+# --------------------------------------------------------------------------
+# distributed plumbing (host side only; no data-path collective)
+# --------------------------------------------------------------------------
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, value):
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(world, value):
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------
+# clocks sampled during the timed region
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, flags in rows for i, fl in enumerate(flags)
+                          if fl.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------
+# timing helpers
+# --------------------------------------------------------------------------
+
+def make_flush(torch, dev):
+    buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    return lambda: buf.fill_(1)
+
+
+def event_time_steps(torch, fn, steps, flush):
+    """Per-step CUDA-event durations (ms) on the current stream, with an L2
+    flush between steps (outside the events)."""
+    stream = torch.cuda.current_stream()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush()
+        starts[i].record(stream)
+        fn()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def source_hash(*paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel_key, src_paths):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the kernel source as it is now; else None."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            table = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = table.get(kernel_key)
+    if not e or e.get("source_sha256_16") != source_hash(*src_paths):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# --------------------------------------------------------------------------
+# our arm
+# --------------------------------------------------------------------------
+
+def ncc_buffers(torch, corr, w, dev):
+    img = torch.from_numpy(w.image).to(dev)
+    tm = torch.from_numpy(w.tmpl).to(dev)
+    h, ww = w.image.shape
+    ht, wt = w.tmpl.shape
+    s = torch.empty((3, h - ht + 1, ww - wt + 1), dtype=torch.int32, device=dev)
+    c = torch.empty((h - ht + 1, ww - wt + 1), dtype=torch.float32, device=dev)
+    return img, tm, s, c, (lambda: corr.ncc_u8_into(img, tm, s, c))
+
+
+def xcorr_buffers(torch, corr, w, dev):
+    L = torch.from_numpy(w.left).to(dev)
+    R = torch.from_numpy(w.right).to(dev)
+    nl, H, W = w.left.shape
+    nr = w.right.shape[0]
+    out = torch.empty((nl, nr, 2 * H - 1, 2 * W - 1), dtype=torch.float32, device=dev)
+    return L, R, out, (lambda: corr.xcorr_f32_into(L, R, out))
+
+
+def dp4a_per_offset(w):
+    ht, wt = w.tmpl.shape
+    return 3 * (wt * ht) // 4
+
+
+def run_ours(args, world, rank, local):
+    import numpy as np
+    import torch
+
+    import normalized_cross_correlation_u8_gb300 as corr
+    from normalized_cross_correlation_u8_gb300 import workloads as wl
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    corr.load()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    flush = make_flush(torch, dev)
+
+    # measured issue rates (same process, same clock regime)
+    dp4a_probe, _ = corr.peak_dp4a(0)
+    ffma_probe, _ = corr.peak_ffma()
+
+    w = wl.NCC_WORKLOADS[HEADLINE]()
+    img, tm, s, c, step = ncc_buffers(torch, corr, w, dev)
+    for _ in range(max(3, args.warmup)):
+        flush()
+        step()
+    torch.cuda.synchronize()
+
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0 = time.perf_counter()
+        times = event_time_steps(torch, step, args.steps, flush)
+        wall = time.perf_counter() - t0
+    torch.cuda.synchronize()
+    barrier(world)
+    total_ms = max_over_ranks(world, sum(times))
+    offsets_all = sum_over_ranks(world, float(w.offsets) * args.steps)
+    value = offsets_all / (total_ms * 1e-3)
+    ms_per_step = total_ms / args.steps
+    clocks = clk.summary()
+
+    avg_launch_s = (sum(times) / args.steps) * 1e-3
+    sm_mhz = clocks["sm_mhz"] if clocks else SM_MAX_MHZ_NOMINAL
+    dp4a_peak = sms * DP4A_PER_SM_CLK * SM_MAX_MHZ_NOMINAL * 1e6
+    achieved = w.offsets * dp4a_per_offset(w) / avg_launch_s
+    ncc_src = [os.path.join(ROOT, "normalized_cross_correlation_u8_gb300", "csrc", "ncc_u8.cu")]
+    roofline = {
+        "bound": "alu", "kernel": "ncc_u8_fixed_kernel (unsigned dp4a issue)",
+        "achieved": achieved / 1e12, "peak": dp4a_peak / 1e12, "unit": "Tdp4a/s",
+        "frac": achieved / dp4a_peak,
+        "peak_basis": f"{sms} SMs x {DP4A_PER_SM_CLK} dp4a/clk x {SM_MAX_MHZ_NOMINAL:.0f} MHz max clock",
+        "frac_at_live_clock": achieved / (sms * DP4A_PER_SM_CLK * sm_mhz * 1e6),
+        "probe_dp4a_per_s": dp4a_probe / 1e12,
+        "algorithmic_per_unit": f"{dp4a_per_offset(w)} dp4a per offset (3 per 4 template pixels)",
+        "traffic": traffic_for("ncc_u8_1080p", ncc_src),
+        "hbm_bytes_algorithmic": int(w.image.size + w.tmpl.size + 16 * w.offsets),
+    }
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "u8", "data": "synthetic",
+        "config": {"workload": w.name, "image": "1920x1080 uint8 (blurred noise, 30% > 127)",
+                   "template": "32x32 uint8 (patch + U[-8,8])", "offsets": w.offsets,
+                   "outputs": "SumI/SumISq/SumIT uint32 planes + coef f32",
+                   "l2": "flushed between steps (256 MB write)",
+                   "parallelism": f"replicas x{world}"},
+        "gpu_launches": args.steps,
+        "wall_s_timed_region": wall,
+        "clocks": clocks, "roofline": roofline,
+    }
+
+    if args.extras and rank == 0:
+        line["per_workload"] = extras_workloads(torch, corr, wl, dev, flush, sms,
+                                                dp4a_probe, ffma_probe)
+        line["e2e"] = e2e_headline(torch, corr, w, dev, args)
+        line["cpu_baseline"] = cpu_baseline_ncc(w)
+    elif args.extras:
+        line["e2e"] = None
+    return line
+
+
+def extras_workloads(torch, corr, wl, dev, flush, sms, dp4a_probe, ffma_probe):
+    out = {}
+    dp4a_peak = sms * DP4A_PER_SM_CLK * SM_MAX_MHZ_NOMINAL * 1e6
+    ffma_peak = sms * FFMA_PER_SM_CLK * SM_MAX_MHZ_NOMINAL * 1e6
+    for key, make in wl.NCC_WORKLOADS.items():
+        w = make()
+        *_, fn = ncc_buffers(torch, corr, w, dev)
+        reps = 30 if w.offsets > 1e7 else 200
+        for _ in range(3):
+            fn()
+        t = event_time_steps(torch, fn, reps, flush)
+        ms = statistics.median(t)
+        rate = w.offsets * dp4a_per_offset(w) / (ms * 1e-3)
+        out[key] = {"workload": w.name, "offsets_per_s": w.offsets / (ms * 1e-3),
+                    "us_per_launch": ms * 1e3,
+                    "roofline": {"bound": "alu", "achieved": rate / 1e12,
+                                 "peak": dp4a_peak / 1e12, "unit": "Tdp4a/s",
+                                 "frac": rate / dp4a_peak}}
+    for key, make in wl.XCORR_WORKLOADS.items():
+        w = make()
+        *_, fn = xcorr_buffers(torch, corr, w, dev)
+        for _ in range(3):
+            fn()
+        t = event_time_steps(torch, fn, 50, flush)
+        ms = statistics.median(t)
+        flops = w.flops / (ms * 1e-3)
+        out[key] = {"workload": w.name, "gflops": flops / 1e9, "us_per_launch": ms * 1e3,
+                    "roofline": {"bound": "alu", "achieved": flops / 1e12,
+                                 "peak": 2 * ffma_peak / 1e12, "unit": "TFLOP/s",
+                                 "frac": flops / (2 * ffma_peak)}}
+    out["probes"] = {"dp4a_per_s": dp4a_probe, "ffma_per_s": ffma_probe}
+    return out
+
+
+def e2e_headline(torch, corr, w, dev, args):
+    """Public API with host buffers: pinned H2D of the step's image and
+    template, the library call, D2H of all four output planes."""
+    h_img = torch.from_numpy(w.image).pin_memory()
+    h_tm = torch.from_numpy(w.tmpl).pin_memory()
+    img, tm, s, c, _ = ncc_buffers(torch, corr, w, dev)
+    h_s = torch.empty(tuple(s.shape), dtype=torch.int32).pin_memory()
+    h_c = torch.empty(tuple(c.shape), dtype=torch.float32).pin_memory()
+
+    def step():
+        img.copy_(h_img, non_blocking=True)
+        tm.copy_(h_tm, non_blocking=True)
+        corr.ncc_u8_into(img, tm, s, c)
+        h_s.copy_(s, non_blocking=True)
+        h_c.copy_(c, non_blocking=True)
+
+    for _ in range(5):
+        step()
+    torch.cuda.synchronize()
+    steps = max(50, min(args.steps // 10, 1000))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return {"value": w.offsets / (ms * 1e-3), "unit": UNIT,
+            "h2d_bytes_per_step": int(w.image.nbytes + w.tmpl.nbytes),
+            "d2h_bytes_per_step": int(s.numel() * 4 + c.numel() * 4),
+            "ms_per_step": ms, "steps": steps}
+
+
+# --------------------------------------------------------------------------
+# CPU oracle timings (baseline leg and reference arm)
+# --------------------------------------------------------------------------
+
+def oracle_band_rate(w, target_s, threads):
+    """Oracle offsets/s on a band of output rows of the workload, the band
+    grown until one timed call takes about target_s seconds."""
+    import numpy as np
+
+    import oracle
+    ht, wt = w.tmpl.shape
+    h = w.image.shape[0]
+    oh = h - ht + 1
+    ow = w.image.shape[1] - wt + 1
+    rows = max(1, threads)
+    while True:
+        band = np.ascontiguousarray(w.image[:rows + ht - 1])
+        t0 = time.perf_counter()
+        oracle.ncc_u8(band, w.tmpl, nthreads=threads)
+        dt = time.perf_counter() - t0
+        if dt >= target_s or rows >= oh:
+            return rows * ow / dt, rows, dt
+        rows = min(oh, max(rows + 1, int(rows * min(8.0, 1.2 * target_s / max(dt, 1e-3)))))
+
+
+def cpu_baseline_ncc(w):
+    threads = os.cpu_count() or 1
+    rate, rows, dt = oracle_band_rate(w, 10.0, threads)
+    return {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"first {rows} output rows x {w.image.shape[1] - w.tmpl.shape[1] + 1} "
+                      f"columns of {w.name} ({dt:.1f} s, OpenMP over rows)"}
+
+
+def run_reference(args, world, rank):
+    from normalized_cross_correlation_u8_gb300 import workloads as wl
+    if rank != 0:
+        return None
+    w = wl.NCC_WORKLOADS[HEADLINE]()
+    threads = os.cpu_count() or 1
+    # size one step's sample so the whole run stays within a few minutes
+    per_step_s = min(10.0, 120.0 / max(1, args.steps + args.warmup))
+    rate, rows, _ = oracle_band_rate(w, per_step_s, threads)
+    import numpy as np
+
+    import oracle
+    ht = w.tmpl.shape[0]
+    band = np.ascontiguousarray(w.image[:rows + ht - 1])
+    for _ in range(args.warmup):
+        oracle.ncc_u8(band, w.tmpl, nthreads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.ncc_u8(band, w.tmpl, nthreads=threads)
+    dt = time.perf_counter() - t0
+    ow = w.image.shape[1] - w.tmpl.shape[1] + 1
+    value = rows * ow * args.steps / dt
+    sample = f"first {rows} output rows x {ow} columns of {w.name} per step"
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+            "config": {"workload": w.name, "parallelism": "CPU oracle, rank 0 only"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "kind": "oracle",
+                             "cores": threads, "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+    else:
+        line = run_ours(args, world, rank, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -11,18 +11,24 @@
 // independent output columns (and rows) per thread keep many accumulation
 // chains in flight (the section's instruction-level parallelism).
 //
-// GB300 layout of the work:
-//   * one warp owns a unit of 256 output columns x R output rows; each lane
-//     owns 8 adjacent columns (x0 = 8*lane, so its words start 8-byte
-//     aligned) and the same R rows;
-//   * the warp walks the image rows k = y0 .. y0+R+ht-2 once; every image
-//     row is loaded (8-byte vector loads through L1) and cut into windows
-//     once, then paired with template row k-r for each of its R output rows,
-//     so loads and funnel shifts are shared by R rows;
-//   * the template lives in shared memory (read as warp-uniform 16-byte
-//     broadcasts); each CTA also reduces SumT / SumTSq from it;
+// GB300 layout of the work (fast path: wt in {16, 32, 64}, image and width
+// 8-byte aligned; every other shape takes the general path below):
+//   * a CTA owns 128 output columns x TY output rows; it copies the image
+//     tile plus its halo (TY+ht-1 rows x 128+wt+8 bytes) into shared memory
+//     with independent 16-byte vector loads (one memory latency per tile,
+//     out-of-image bytes zero), and stages the template as packed words;
+//   * each half-warp owns R output rows, each lane 8 adjacent columns whose
+//     words start 8-byte aligned; the half-warp walks its R+ht-1 tile rows
+//     once, cutting each row into the lane's 8 windows with funnel shifts
+//     (windows of columns 4..7 at word i equal those of columns 0..3 at word
+//     i+1, so 3 shifts per word serve 8 columns) and pairing it with
+//     template row k-r for each of its R output rows;
+//   * the template row is read as warp-uniform 16-byte shared broadcasts;
+//     each CTA also reduces SumT / SumTSq from it;
 //   * the epilogue forms N*SumIT - SumI*SumT and N*SumISq - SumI^2 exactly in
 //     64-bit integers before the single-precision ratio.
+// Measured on GB300 (R = 1, 2-warp CTAs): the unsigned dp4a pipe (64 per SM
+// per clock) is 73-91 % busy with dp4a depending on image and template size.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -32,8 +38,19 @@ namespace corr {
 namespace {
 
 constexpr int kCols = 8;                   // output columns per lane
-constexpr int kUnitCols = 32 * kCols;      // output columns per warp unit
-constexpr int kWarpsPerCta = 4;
+constexpr int kUnitCols = 32 * kCols;      // output columns per warp unit (general path)
+constexpr int kHalfUnitCols = 16 * kCols;  // output columns per warp unit (fast path)
+// Warps per CTA and output rows per half-warp (compile-time tuning knobs).
+#ifndef CORR_NCC_WARPS
+#define CORR_NCC_WARPS 2
+#endif
+#ifndef CORR_NCC_ROWS
+#define CORR_NCC_ROWS 1
+#endif
+#ifndef CORR_NCC_MINB
+#define CORR_NCC_MINB 1
+#endif
+constexpr int kWarpsPerCta = CORR_NCC_WARPS;
 constexpr int kThreads = 32 * kWarpsPerCta;
 constexpr uint32_t kOnes = 0x01010101u;
 
@@ -48,7 +65,7 @@ struct NccArgs {
   int wtp;           // shared-memory template row stride in words (multiple of 4)
   int ow, oh;
   int tiles_x;       // units across a row of outputs
-  int units;         // tiles_x * ceil(oh / R)
+  int units;         // warp units (fast path: 128 cols x 2R rows)
 };
 
 __device__ __forceinline__ uint32_t fshr(uint32_t lo, uint32_t hi, int bytes) {
@@ -117,16 +134,17 @@ __device__ __forceinline__ void accum_window(uint32_t (&sI)[R][kCols],
   sT[r][c] = __dp4a(win, tw, sT[r][c]);
 }
 
-// Write the sums and the coefficient of one lane's R x 8 block.
+// Write the sums and the coefficient of one lane's R x 8 block.  The
+// numerator and the window variance term are exact 64-bit integers; the
+// ratio is num * rsqrt(dI) * rsqrt(dT) in single precision (a few ulp of
+// |coef| <= 1, far inside the 1e-5 bound).  rs_t = rsqrt(dT) is per template.
 template <int R>
 __device__ __forceinline__ void epilogue(const NccArgs &a, int x0, int y0,
                                          const uint32_t (&sI)[R][kCols],
                                          const uint32_t (&sQ)[R][kCols],
                                          const uint32_t (&sT)[R][kCols],
-                                         uint32_t sum_t, uint32_t sum_t_sq) {
+                                         uint32_t sum_t, float rs_t) {
   const int64_t n = int64_t(a.wt) * a.ht;
-  const int64_t d_t = n * int64_t(sum_t_sq) - int64_t(sum_t) * int64_t(sum_t);
-  const float d_tf = float(d_t);
 #pragma unroll
   for (int r = 0; r < R; ++r) {
     const int y = y0 + r;
@@ -145,12 +163,19 @@ __device__ __forceinline__ void epilogue(const NccArgs &a, int x0, int y0,
         const int64_t si = sI[r][c];
         const int64_t num = n * int64_t(sT[r][c]) - si * int64_t(sum_t);
         const int64_t d_i = n * int64_t(sQ[r][c]) - si * si;
-        float cf = 0.f;
-        if (d_i > 0 && d_t > 0) cf = float(num) / sqrtf(float(d_i) * d_tf);
-        a.coef[o] = cf;
+        a.coef[o] = d_i > 0 ? float(num) * rsqrtf(float(d_i)) * rs_t : 0.f;
       }
     }
   }
+}
+
+// rsqrt of the template variance term N*SumTSq - SumT^2, or 0 for a flat
+// template (which makes every coefficient 0).
+__device__ __forceinline__ float template_rsqrt(const NccArgs &a, uint32_t sum_t,
+                                                uint32_t sum_t_sq) {
+  const int64_t n = int64_t(a.wt) * a.ht;
+  const int64_t d_t = n * int64_t(sum_t_sq) - int64_t(sum_t) * int64_t(sum_t);
+  return d_t > 0 ? rsqrtf(float(d_t)) : 0.f;
 }
 
 // One image row (tile-relative index rel = k - y0) against template rows
@@ -192,23 +217,65 @@ __device__ __forceinline__ void row_fixed(const uint32_t (&wv)[WT + 2],
 }
 
 // Fast path: template width WT words known at compile time, image pointer
-// and width 8-byte aligned, so every lane reads its WT+2 words as (WT+2)/2
-// aligned 8-byte loads (a pair never straddles the row end since w % 8 == 0).
-template <int R, int WT>
-__global__ void __launch_bounds__(kThreads)
+// and width 8-byte aligned.
+//
+// A CTA owns a tile of 128 output columns x TY = 2*R*kWarpsPerCta output
+// rows.  It first copies the image tile plus halo -- TY+ht-1 rows of
+// 128+4*WT+8 bytes (rounded to 16) -- into shared memory with 16-byte (or
+// 8-byte) vector loads that are all independent, so the tile costs one
+// memory latency instead of one per image row.  Then half-warp h of warp w
+// takes output rows w*2R + h*R .. +R-1 (each lane 8 adjacent columns) and
+// walks its R+ht-1 tile rows from shared memory; each row is cut into
+// windows once and paired with template row k-r for each of its R rows.
+// Words of the next tile row are read while the current one is consumed.
+template <int WT>
+struct TileGeom {
+  static constexpr int kRowBytes = (kHalfUnitCols + 4 * WT + 8 + 15) & ~15;
+};
+
+template <int R, int WT, bool V16>
+__global__ void __launch_bounds__(kThreads, CORR_NCC_MINB)
     ncc_u8_fixed_kernel(const NccArgs a) {
+  constexpr int WTP = (WT + 3) & ~3;
+  constexpr int RB = TileGeom<WT>::kRowBytes;
+  constexpr int TY = 2 * R * kWarpsPerCta;
   extern __shared__ uint4 smem_u4[];
   uint32_t *tmpl_s = reinterpret_cast<uint32_t *>(smem_u4);
+  uint8_t *tile = reinterpret_cast<uint8_t *>(smem_u4) + size_t(a.ht) * WTP * 4;
   __shared__ uint32_t red[2];
+
+  const int tx = blockIdx.x % a.tiles_x, ty = blockIdx.x / a.tiles_x;
+  const int xt = tx * kHalfUnitCols, yt = ty * TY;
+  const int trows = min(TY + a.ht - 1, a.h - yt);   // tile rows inside the image
+
+  // ---- tile + halo -> shared memory (out-of-image bytes become zero) ----
+  if (V16) {
+    constexpr int C = RB / 16;
+    for (int i = threadIdx.x; i < trows * C; i += kThreads) {
+      const int r = i / C, c = i - r * C;
+      const int x = xt + 16 * c;                    // w % 16 == 0: chunk in or out
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (x < a.w) v = __ldg(reinterpret_cast<const uint4 *>(a.image + size_t(yt + r) * a.w + x));
+      *reinterpret_cast<uint4 *>(tile + r * RB + 16 * c) = v;
+    }
+  } else {
+    constexpr int C = RB / 8;
+    for (int i = threadIdx.x; i < trows * C; i += kThreads) {
+      const int r = i / C, c = i - r * C;
+      const int x = xt + 8 * c;                     // w % 8 == 0: pair in or out
+      uint2 v = make_uint2(0u, 0u);
+      if (x < a.w) v = __ldg(reinterpret_cast<const uint2 *>(a.image + size_t(yt + r) * a.w + x));
+      *reinterpret_cast<uint2 *>(tile + r * RB + 8 * c) = v;
+    }
+  }
   uint32_t sum_t, sum_t_sq;
-  stage_template(a, tmpl_s, red, sum_t, sum_t_sq);
+  stage_template(a, tmpl_s, red, sum_t, sum_t_sq);   // ends with __syncthreads
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int unit = blockIdx.x * kWarpsPerCta + warp;
-  if (unit >= a.units) return;
-  const int tx = unit % a.tiles_x, rb = unit / a.tiles_x;
-  const int x0 = tx * kUnitCols + lane * kCols;
-  const int y0 = rb * R;
+  const int half = lane >> 4, hl = lane & 15;
+  const int yr0 = warp * 2 * R + half * R;           // tile-relative first row
+  const int x0 = xt + hl * kCols;
+  const int y0 = yt + yr0;
 
   uint32_t sI[R][kCols], sQ[R][kCols], sT[R][kCols];
 #pragma unroll
@@ -216,28 +283,22 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
     for (int c = 0; c < kCols; ++c) sI[r][c] = sQ[r][c] = sT[r][c] = 0;
 
-  const int nrows = min(R + a.ht - 1, a.h - y0);
-  constexpr int NP = (WT + 2) / 2;  // 8-byte pairs per row (WT even)
-  static_assert(WT % 2 == 0, "fixed path expects an even word count");
-  uint32_t wv[WT + 2], nx[WT + 2];
-
+  // Warp-uniform row count: rows of the lower half past the tile's rows in
+  // the image read the last staged row (their outputs are past oh and are
+  // never stored).
+  const int nrows = max(0, min(R + a.ht - 1, trows - warp * 2 * R));
+  const uint8_t *lane_base = tile + hl * kCols;
   auto load_row = [&](int rel, uint32_t (&dst)[WT + 2]) {
-    const uint8_t *row = a.image + size_t(y0 + rel) * a.w;
+    const int r = min(yr0 + rel, trows - 1);
+    const uint8_t *row = lane_base + r * RB;
 #pragma unroll
-    for (int p = 0; p < NP; ++p) {
-      const int off = x0 + 8 * p;
-      uint2 v = make_uint2(0u, 0u);
-      if (off < a.w) v = __ldg(reinterpret_cast<const uint2 *>(row + off));
+    for (int p = 0; p < (WT + 2) / 2; ++p) {
+      const uint2 v = *reinterpret_cast<const uint2 *>(row + 8 * p);
       dst[2 * p] = v.x;
       dst[2 * p + 1] = v.y;
     }
   };
-
-  load_row(0, nx);
-  for (int rel = 0; rel < nrows; ++rel) {
-#pragma unroll
-    for (int k = 0; k < WT + 2; ++k) wv[k] = nx[k];
-    if (rel + 1 < nrows) load_row(rel + 1, nx);
+  auto process = [&](const uint32_t (&wv)[WT + 2], int rel) {
     if (rel >= R - 1 && rel <= a.ht - 1) {
       row_fixed<R, WT, true>(wv, tmpl_s, rel, 0u, sI, sQ, sT);
     } else {
@@ -247,8 +308,18 @@ __global__ void __launch_bounds__(kThreads)
         if (rel - r >= 0 && rel - r < a.ht) mask |= 1u << r;
       row_fixed<R, WT, false>(wv, tmpl_s, rel, mask, sI, sQ, sT);
     }
+  };
+  static_assert(WT % 2 == 0, "fixed path expects an even word count");
+  uint32_t wa[WT + 2], wb[WT + 2];
+  if (nrows > 0) load_row(0, wa);
+  for (int rel = 0; rel < nrows; rel += 2) {
+    if (rel + 1 < nrows) load_row(rel + 1, wb);
+    process(wa, rel);
+    if (rel + 1 >= nrows) break;
+    if (rel + 2 < nrows) load_row(rel + 2, wa);
+    process(wb, rel + 1);
   }
-  epilogue<R>(a, x0, y0, sI, sQ, sT, sum_t, sum_t_sq);
+  epilogue<R>(a, x0, y0, sI, sQ, sT, sum_t, template_rsqrt(a, sum_t, sum_t_sq));
 }
 
 // General path: any template width (multiple of 4) and any image alignment.
@@ -307,19 +378,34 @@ __global__ void __launch_bounds__(kThreads)
       w1 = w2;
     }
   }
-  epilogue<R>(a, x0, y0, sI, sQ, sT, sum_t, sum_t_sq);
+  epilogue<R>(a, x0, y0, sI, sQ, sT, sum_t, template_rsqrt(a, sum_t, sum_t_sq));
+}
+
+template <typename Kernel>
+cudaError_t set_smem(Kernel kernel, size_t smem) {
+  if (smem > 48 * 1024)
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                int(smem));
+  return cudaSuccess;
 }
 
 template <typename Kernel>
 cudaError_t launch(Kernel kernel, const NccArgs &a, size_t smem,
                    cudaStream_t stream) {
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(
-        kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (e != cudaSuccess) return e;
-  }
+  cudaError_t e = set_smem(kernel, smem);
+  if (e != cudaSuccess) return e;
   const int blocks = (a.units + kWarpsPerCta - 1) / kWarpsPerCta;
   kernel<<<blocks, kThreads, smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+// One CTA per tile.
+template <typename Kernel>
+cudaError_t launch_tiles(Kernel kernel, const NccArgs &a, size_t smem,
+                         cudaStream_t stream) {
+  cudaError_t e = set_smem(kernel, smem);
+  if (e != cudaSuccess) return e;
+  kernel<<<a.units, kThreads, smem, stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -329,7 +415,7 @@ cudaError_t ncc_u8_launch(const uint8_t *image, int w, int h,
                           const uint8_t *tmpl, int wt, int ht,
                           uint32_t *sums_out, float *coef_out,
                           cudaStream_t stream) {
-  constexpr int R = 2;
+  constexpr int R = CORR_NCC_ROWS;
   NccArgs a;
   a.image = image;
   a.tmpl = tmpl;
@@ -344,19 +430,36 @@ cudaError_t ncc_u8_launch(const uint8_t *image, int w, int h,
   a.ow = w - wt + 1;
   a.oh = h - ht + 1;
   a.plane = size_t(a.ow) * a.oh;
-  a.tiles_x = (a.ow + kUnitCols - 1) / kUnitCols;
-  a.units = a.tiles_x * ((a.oh + R - 1) / R);
   const size_t smem = size_t(ht) * a.wtp * 4;
 
   const bool aligned8 = (reinterpret_cast<uintptr_t>(image) & 7) == 0 && (w & 7) == 0;
-  if (aligned8) {
+  const bool aligned16 = (reinterpret_cast<uintptr_t>(image) & 15) == 0 && (w & 15) == 0;
+  if (aligned8 && (a.wtw == 4 || a.wtw == 8 || a.wtw == 16)) {
+    constexpr int TY = 2 * R * kWarpsPerCta;
+    a.tiles_x = (a.ow + kHalfUnitCols - 1) / kHalfUnitCols;
+    const long long tiles = (long long)a.tiles_x * ((a.oh + TY - 1) / TY);
+    if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    a.units = int(tiles);
+    auto tile_smem = [&](int wtw) {
+      const size_t rb = (kHalfUnitCols + 4 * wtw + 8 + 15) & ~15;
+      return smem + size_t(TY + ht - 1) * rb;
+    };
+    const size_t ts = tile_smem(a.wtw);
+    if (ts > 200 * 1024) goto general;   // very tall template: general path
     switch (a.wtw) {
-      case 4: return launch(ncc_u8_fixed_kernel<R, 4>, a, smem, stream);
-      case 8: return launch(ncc_u8_fixed_kernel<R, 8>, a, smem, stream);
-      case 16: return launch(ncc_u8_fixed_kernel<R, 16>, a, smem, stream);
-      default: break;
+      case 4: return aligned16 ? launch_tiles(ncc_u8_fixed_kernel<R, 4, true>, a, ts, stream)
+                               : launch_tiles(ncc_u8_fixed_kernel<R, 4, false>, a, ts, stream);
+      case 8: return aligned16 ? launch_tiles(ncc_u8_fixed_kernel<R, 8, true>, a, ts, stream)
+                               : launch_tiles(ncc_u8_fixed_kernel<R, 8, false>, a, ts, stream);
+      default: return aligned16 ? launch_tiles(ncc_u8_fixed_kernel<R, 16, true>, a, ts, stream)
+                                : launch_tiles(ncc_u8_fixed_kernel<R, 16, false>, a, ts, stream);
     }
   }
+general:
+  a.tiles_x = (a.ow + kUnitCols - 1) / kUnitCols;
+  const long long units = (long long)a.tiles_x * ((a.oh + R - 1) / R);
+  if (units > 0x7fffffffLL - kWarpsPerCta) return cudaErrorInvalidConfiguration;
+  a.units = int(units);
   return launch(ncc_u8_general_kernel<R>, a, smem, stream);
 }
 
