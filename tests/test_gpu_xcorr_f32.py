@@ -65,6 +65,8 @@ def test_fixture(path):
     (1, 1, 16, 16), (1, 1, 17, 33), (1, 1, 40, 9), (1, 1, 100, 130),
     (1, 5, 31, 29), (1, 37, 64, 64), (3, 4, 7, 11), (5, 9, 16, 16),
     (2, 3, 50, 8), (33, 3, 5, 5), (1, 1, 1, 300), (1, 1, 300, 1),
+    # row-band split (three bands, W % 4 != 0, two pairs)
+    (1, 2, 130, 257), (2, 1, 200, 64),
     # too wide to stage: the bounds-checked fallback kernel
     (1, 1, 5, 400), (2, 2, 3, 700), (1, 6, 4, 520),
 ])
