@@ -92,6 +92,36 @@ int corr_ncc_u8(const uint8_t *image, int w, int h, const uint8_t *tmpl,
 int corr_xcorr_f32(const float *left, int nl, const float *right, int nr,
                    int H, int W, float *out);
 
+/*
+ * corr_xcorr_f32_noalloc -- corr_xcorr_f32 for callers that cannot allocate.
+ *
+ * No counterpart on the pages: this is a deployment variant of
+ * corr_xcorr_f32 with the same arguments, layouts, results and error codes.
+ * corr_xcorr_f32 takes temporary device memory for the partial sums of large
+ * matrices from a stream-ordered pool that may call the driver's allocator.
+ * Some callers cannot allow that -- an application that reserves all device
+ * memory up front for its own allocator, a plug-in whose host framework
+ * forbids driver allocations during its calls, a real-time loop that must
+ * never wait on an allocator.  This call allocates nothing: its scratch is a
+ * fixed array of CORR_XCORR_NOALLOC_SCRATCH_BYTES inside the library image,
+ * which every GPU that loads the library's device code holds until the
+ * process exits.
+ *
+ *   * Shapes whose partial sums need more than that return
+ *     CORR_EUNSUPPORTED before anything is launched.  Only matrices of 64 or
+ *     more rows on the large-matrix kernel use scratch: one 256x256 pair
+ *     needs 4 MiB, so up to four such pairs fit and five are rejected.
+ *   * The first call on a device that needs scratch looks the array's device
+ *     address up on that device; make that first call before any stream
+ *     capture begins on it.
+ *   * Every call, on every stream and thread, shares the one array: calls
+ *     that overlap on the GPU race and corrupt each other's results, so
+ *     order them (one stream, or events between streams).
+ */
+#define CORR_XCORR_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+int corr_xcorr_f32_noalloc(const float *left, int nl, const float *right, int nr,
+                           int H, int W, float *out);
+
 /* Stream for this thread's following calls (a cudaStream_t; NULL = the
  * legacy default stream).  Thread-local; never fails. */
 int corr_set_stream(void *stream);

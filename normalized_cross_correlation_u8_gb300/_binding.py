@@ -24,7 +24,7 @@ CORR_EUNSUPPORTED = -2
 CORR_ECUDA = -3
 NCC_MAX_TEMPLATE_PIXELS = 66052
 
-EXPORTS = ["corr_ncc_u8", "corr_xcorr_f32", "corr_set_stream",
+EXPORTS = ["corr_ncc_u8", "corr_xcorr_f32", "corr_xcorr_f32_noalloc", "corr_set_stream",
            "corr_get_stream", "corr_strerror", "corr_last_cuda_error",
            "corr_version", "corr_peak_dp4a", "corr_peak_ffma"]
 
@@ -65,6 +65,7 @@ def load(build_if_missing=True):
         c_int, vp, c_dbl_p = ctypes.c_int, ctypes.c_void_p, ctypes.POINTER(ctypes.c_double)
         lib.corr_ncc_u8.argtypes = [vp, c_int, c_int, vp, c_int, c_int, vp, vp]
         lib.corr_xcorr_f32.argtypes = [vp, c_int, vp, c_int, c_int, c_int, vp]
+        lib.corr_xcorr_f32_noalloc.argtypes = [vp, c_int, vp, c_int, c_int, c_int, vp]
         lib.corr_set_stream.argtypes = [vp]
         lib.corr_get_stream.argtypes = []
         lib.corr_get_stream.restype = vp
@@ -74,7 +75,8 @@ def load(build_if_missing=True):
         lib.corr_version.argtypes = []
         lib.corr_peak_dp4a.argtypes = [c_int, c_dbl_p, c_dbl_p]
         lib.corr_peak_ffma.argtypes = [c_dbl_p, c_dbl_p]
-        for f in (lib.corr_ncc_u8, lib.corr_xcorr_f32, lib.corr_set_stream,
+        for f in (lib.corr_ncc_u8, lib.corr_xcorr_f32, lib.corr_xcorr_f32_noalloc,
+                  lib.corr_set_stream,
                   lib.corr_last_cuda_error, lib.corr_version,
                   lib.corr_peak_dp4a, lib.corr_peak_ffma):
             f.restype = c_int
@@ -192,6 +194,32 @@ def xcorr_f32_into(left, right, out):
         _check(lib.corr_xcorr_f32(ctypes.c_void_p(left.data_ptr()), nl,
                                   ctypes.c_void_p(right.data_ptr()), nr, H, W,
                                   ctypes.c_void_p(out.data_ptr())))
+    return out
+
+
+def xcorr_f32_noalloc_into(left, right, out):
+    """As xcorr_f32_into, through corr_xcorr_f32_noalloc: the library allocates
+    no device memory (its scratch is a fixed 16 MiB array shared by all calls,
+    so calls that overlap on the GPU must be ordered by the caller).  Raises
+    CorrError (unsupported size) for shapes that need more scratch."""
+    for t in (left, right, out):
+        if t.dtype != torch.float32:
+            raise TypeError("xcorr operates on float32")
+    if left.dim() != 3 or right.dim() != 3 or left.shape[1:] != right.shape[1:]:
+        raise ValueError("left [nl,H,W] and right [nr,H,W] must share H, W")
+    dev = left.device
+    if not left.is_cuda or right.device != dev or out.device != dev:
+        raise ValueError("all tensors must be on the same CUDA device")
+    nl, H, W = left.shape
+    nr = right.shape[0]
+    if tuple(out.shape) != (nl, nr, 2 * H - 1, 2 * W - 1) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [nl, nr, 2H-1, 2W-1] tensor")
+    left, right = left.contiguous(), right.contiguous()
+    with torch.cuda.device(dev):
+        lib = _bind_stream(dev)
+        _check(lib.corr_xcorr_f32_noalloc(ctypes.c_void_p(left.data_ptr()), nl,
+                                          ctypes.c_void_p(right.data_ptr()), nr, H, W,
+                                          ctypes.c_void_p(out.data_ptr())))
     return out
 
 

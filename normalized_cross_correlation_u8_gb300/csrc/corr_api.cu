@@ -48,6 +48,23 @@ int corr_xcorr_f32(const float *left, int nl, const float *right, int nr,
       corr::xcorr_f32_launch(left, nl, right, nr, H, W, out, tls_stream));
 }
 
+int corr_xcorr_f32_noalloc(const float *left, int nl, const float *right, int nr,
+                           int H, int W, float *out) {
+  if (!left || !right || !out) return CORR_EINVAL;
+  if (nl <= 0 || nr <= 0 || H <= 0 || W <= 0) return CORR_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(left) | reinterpret_cast<uintptr_t>(right) |
+       reinterpret_cast<uintptr_t>(out)) & 3)
+    return CORR_EINVAL;
+  if (int64_t(nl) * nr > 0x7fffffffLL) return CORR_EUNSUPPORTED;
+  if (int64_t(2) * H - 1 > 0x7fffffffLL || int64_t(2) * W - 1 > 0x7fffffffLL)
+    return CORR_EUNSUPPORTED;
+  if (corr::xcorr_f32_scratch_bytes(left, nl, right, nr, H, W) >
+      CORR_XCORR_NOALLOC_SCRATCH_BYTES)
+    return CORR_EUNSUPPORTED;
+  return cuda_status(
+      corr::xcorr_f32_noalloc_launch(left, nl, right, nr, H, W, out, tls_stream));
+}
+
 int corr_set_stream(void *stream) {
   tls_stream = static_cast<cudaStream_t>(stream);
   return CORR_OK;

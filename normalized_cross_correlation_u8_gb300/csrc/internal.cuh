@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
 
 namespace corr {
@@ -18,5 +19,24 @@ cudaError_t ncc_u8_launch(const uint8_t *image, int w, int h,
 cudaError_t xcorr_f32_launch(const float *left, int nl, const float *right,
                              int nr, int H, int W, float *out,
                              cudaStream_t stream);
+
+// Bytes of split-row scratch corr_xcorr_f32 would take for this shape (0
+// when the chosen kernel needs none).
+size_t xcorr_f32_scratch_bytes(const float *left, int nl, const float *right, int nr,
+                               int H, int W);
+
+// As xcorr_f32_launch, but split-row partial sums go to `scratch` (at least
+// xcorr_f32_scratch_bytes long; cudaErrorInvalidValue otherwise) instead of
+// the library's pool: nothing is allocated.
+cudaError_t xcorr_f32_launch_scratch(const float *left, int nl, const float *right,
+                                     int nr, int H, int W, float *out, float *scratch,
+                                     size_t scratch_bytes, cudaStream_t stream);
+
+// Entry of the no-allocation variant (xcorr_noalloc.cu): scratch from the
+// library's fixed device array.  Returns cudaErrorInvalidValue if the shape
+// needs more than that array holds.
+cudaError_t xcorr_f32_noalloc_launch(const float *left, int nl, const float *right,
+                                     int nr, int H, int W, float *out,
+                                     cudaStream_t stream);
 
 }  // namespace corr

@@ -814,14 +814,27 @@ cudaError_t scratch_alloc(float **ptr, size_t bytes, cudaStream_t stream) {
 // Largest shared staging area of the rows / pair kernels (two CTAs per SM).
 constexpr size_t kMaxStageSmem = 110 * 1024;
 
-cudaError_t xcorr_f32_launch(const float *left, int nl, const float *right,
-                             int nr, int H, int W, float *out,
-                             cudaStream_t stream) {
-  const long long pairs = (long long)nl * nr;
-  if (H * W <= 256 && pairs >= 64)
-    return launch_tiny(left, nl, right, nr, H, W, out, stream);
+namespace {
 
+// Which kernel a shape takes, its arguments and the split-row scratch it needs.
+enum class XKind { Tiny, Pair, Rows, Direct };
+
+struct XPlan {
+  XKind kind;
   XArgs a;
+  size_t smem;           // dynamic shared memory of the pair / rows kernel
+  long long blocks;      // grid of the pair / rows kernel
+  size_t part_bytes;     // rows kernel with several bands: scratch bytes
+};
+
+XPlan make_plan(const float *left, int nl, const float *right, int nr, int H, int W,
+                float *out) {
+  XPlan pl;
+  pl.smem = 0;
+  pl.blocks = 0;
+  pl.part_bytes = 0;
+  const long long pairs = (long long)nl * nr;
+  XArgs &a = pl.a;
   a.left = left;
   a.right = right;
   a.out = out;
@@ -829,6 +842,10 @@ cudaError_t xcorr_f32_launch(const float *left, int nl, const float *right,
   a.nr = nr;
   a.H = H;
   a.W = W;
+  if (H * W <= 256 && pairs >= 64) {
+    pl.kind = XKind::Tiny;
+    return pl;
+  }
   const int need = kPadL + ((W + 3) & ~3) + kP + 8;
   a.S = ((need + 7) & ~7) + 4;
   a.dxbase = -(((W - 1) + 3) & ~3);
@@ -851,44 +868,88 @@ cudaError_t xcorr_f32_launch(const float *left, int nl, const float *right,
     if (parts > max_parts) parts = max_parts;
     if (parts < 1) parts = 1;
     a.parts = int(parts);
-    const long long blocks = pairs * a.parts;
-    if (blocks <= 0x7fffffffLL) {
-      cudaError_t e = cudaFuncSetAttribute(
-          xcorr_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(pair_smem));
-      if (e != cudaSuccess) return e;
-      xcorr_pair_kernel<<<unsigned(blocks), kThreads, pair_smem, stream>>>(a);
-      return cudaGetLastError();
+    if (pairs * a.parts <= 0x7fffffffLL) {
+      pl.kind = XKind::Pair;
+      pl.smem = pair_smem;
+      pl.blocks = pairs * a.parts;
+      return pl;
     }
   }
   const size_t rows_smem = size_t(2 * kChunkRows) * a.S * sizeof(float);
   a.nbands = (H + kBandRows - 1) / kBandRows;
   a.part_row = kP * a.ngroups;
   const long long blocks = pairs * a.ndyb * a.nsuper * a.nbands;
-  if (rows_smem > kMaxStageSmem || blocks > 0x7fffffffLL || H < 24)
-    return launch_direct(left, nl, right, nr, H, W, out, stream);
-  cudaError_t e = cudaFuncSetAttribute(
-      xcorr_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(rows_smem));
-  if (e != cudaSuccess) return e;
-  a.part = nullptr;
-  if (a.nbands > 1) {
-    const size_t part_bytes =
-        size_t(pairs) * a.ndyb * a.nbands * kQ * a.part_row * sizeof(float);
-    if ((e = scratch_alloc(&a.part, part_bytes, stream)) != cudaSuccess) return e;
+  if (rows_smem > kMaxStageSmem || blocks > 0x7fffffffLL || H < 24) {
+    pl.kind = XKind::Direct;
+    return pl;
   }
-  xcorr_rows_kernel<<<unsigned(blocks), kThreads, rows_smem, stream>>>(a);
+  pl.kind = XKind::Rows;
+  pl.smem = rows_smem;
+  pl.blocks = blocks;
+  if (a.nbands > 1)
+    pl.part_bytes = size_t(pairs) * a.ndyb * a.nbands * kQ * a.part_row * sizeof(float);
+  return pl;
+}
+
+// Launch a plan.  Split-row scratch comes from `fixed` (at least
+// pl.part_bytes long) when given, else from the library's pool.
+cudaError_t run_plan(XPlan &pl, float *fixed, cudaStream_t stream) {
+  XArgs &a = pl.a;
+  if (pl.kind == XKind::Tiny)
+    return launch_tiny(a.left, a.nl, a.right, a.nr, a.H, a.W, a.out, stream);
+  if (pl.kind == XKind::Direct)
+    return launch_direct(a.left, a.nl, a.right, a.nr, a.H, a.W, a.out, stream);
+  if (pl.kind == XKind::Pair) {
+    cudaError_t e = cudaFuncSetAttribute(
+        xcorr_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(pl.smem));
+    if (e != cudaSuccess) return e;
+    xcorr_pair_kernel<<<unsigned(pl.blocks), kThreads, pl.smem, stream>>>(a);
+    return cudaGetLastError();
+  }
+  cudaError_t e = cudaFuncSetAttribute(
+      xcorr_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(pl.smem));
+  if (e != cudaSuccess) return e;
+  const bool banded = a.nbands > 1;
+  const bool pooled = banded && fixed == nullptr;
+  a.part = banded ? fixed : nullptr;
+  if (pooled && (e = scratch_alloc(&a.part, pl.part_bytes, stream)) != cudaSuccess) return e;
+  xcorr_rows_kernel<<<unsigned(pl.blocks), kThreads, pl.smem, stream>>>(a);
   e = cudaGetLastError();
-  if (a.nbands > 1) {
-    if (e == cudaSuccess) {
-      const long long outs = pairs * (2LL * H - 1) * (2LL * W - 1);
-      const long long sum_blocks = (outs + 255) / 256;
-      xcorr_band_sum_kernel<<<unsigned(sum_blocks < 65535 * 16 ? sum_blocks : 65535 * 16), 256,
-                              0, stream>>>(a);
-      e = cudaGetLastError();
-    }
+  if (banded && e == cudaSuccess) {
+    const long long outs = (long long)a.nl * a.nr * (2LL * a.H - 1) * (2LL * a.W - 1);
+    const long long sum_blocks = (outs + 255) / 256;
+    xcorr_band_sum_kernel<<<unsigned(sum_blocks < 65535 * 16 ? sum_blocks : 65535 * 16), 256, 0,
+                            stream>>>(a);
+    e = cudaGetLastError();
+  }
+  if (pooled) {
     const cudaError_t f = cudaFreeAsync(a.part, stream);
     if (e == cudaSuccess) e = f;
   }
   return e;
+}
+
+}  // namespace
+
+cudaError_t xcorr_f32_launch(const float *left, int nl, const float *right,
+                             int nr, int H, int W, float *out,
+                             cudaStream_t stream) {
+  XPlan pl = make_plan(left, nl, right, nr, H, W, out);
+  return run_plan(pl, nullptr, stream);
+}
+
+size_t xcorr_f32_scratch_bytes(const float *left, int nl, const float *right, int nr,
+                               int H, int W) {
+  return make_plan(left, nl, right, nr, H, W, nullptr).part_bytes;
+}
+
+cudaError_t xcorr_f32_launch_scratch(const float *left, int nl, const float *right,
+                                     int nr, int H, int W, float *out, float *scratch,
+                                     size_t scratch_bytes, cudaStream_t stream) {
+  XPlan pl = make_plan(left, nl, right, nr, H, W, out);
+  if (pl.part_bytes > scratch_bytes || (pl.part_bytes > 0 && scratch == nullptr))
+    return cudaErrorInvalidValue;
+  return run_plan(pl, scratch, stream);
 }
 
 }  // namespace corr
