@@ -50,8 +50,16 @@ constexpr int kHalfUnitCols = 16 * kCols;  // output columns per warp unit (fast
 #ifndef CORR_NCC_MINB
 #define CORR_NCC_MINB 1
 #endif
+#ifndef CORR_NCC_KSPLIT
+#define CORR_NCC_KSPLIT 2
+#endif
 constexpr int kWarpsPerCta = CORR_NCC_WARPS;
 constexpr int kThreads = 32 * kWarpsPerCta;
+// Fast path: the template rows of a tile are split into kSplit ranges, one
+// per group of kWarpsPerCta warps; the groups' partial sums are added in
+// shared memory (integer sums: exact in any order).
+constexpr int kSplit = CORR_NCC_KSPLIT;
+constexpr int kFixedThreads = kThreads * kSplit;
 constexpr uint32_t kOnes = 0x01010101u;
 
 struct NccArgs {
@@ -234,7 +242,7 @@ struct TileGeom {
 };
 
 template <int R, int WT, bool V16>
-__global__ void __launch_bounds__(kThreads, CORR_NCC_MINB)
+__global__ void __launch_bounds__(kFixedThreads, CORR_NCC_MINB)
     ncc_u8_fixed_kernel(const NccArgs a) {
   constexpr int WTP = (WT + 3) & ~3;
   constexpr int RB = TileGeom<WT>::kRowBytes;
@@ -251,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, CORR_NCC_MINB)
   // ---- tile + halo -> shared memory (out-of-image bytes become zero) ----
   if (V16) {
     constexpr int C = RB / 16;
-    for (int i = threadIdx.x; i < trows * C; i += kThreads) {
+    for (int i = threadIdx.x; i < trows * C; i += kFixedThreads) {
       const int r = i / C, c = i - r * C;
       const int x = xt + 16 * c;                    // w % 16 == 0: chunk in or out
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
@@ -260,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, CORR_NCC_MINB)
     }
   } else {
     constexpr int C = RB / 8;
-    for (int i = threadIdx.x; i < trows * C; i += kThreads) {
+    for (int i = threadIdx.x; i < trows * C; i += kFixedThreads) {
       const int r = i / C, c = i - r * C;
       const int x = xt + 8 * c;                     // w % 8 == 0: pair in or out
       uint2 v = make_uint2(0u, 0u);
@@ -271,7 +279,10 @@ __global__ void __launch_bounds__(kThreads, CORR_NCC_MINB)
   uint32_t sum_t, sum_t_sq;
   stage_template(a, tmpl_s, red, sum_t, sum_t_sq);   // ends with __syncthreads
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp_id = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = warp_id % kWarpsPerCta;            // row group of the tile
+  const int ks = warp_id / kWarpsPerCta;              // template-row range
+  const int j_lo = ks * a.ht / kSplit, j_hi = (ks + 1) * a.ht / kSplit;
   const int half = lane >> 4, hl = lane & 15;
   const int yr0 = warp * 2 * R + half * R;           // tile-relative first row
   const int x0 = xt + hl * kCols;
@@ -298,26 +309,62 @@ __global__ void __launch_bounds__(kThreads, CORR_NCC_MINB)
       dst[2 * p + 1] = v.y;
     }
   };
+  // tile row yr0 + rel meets template row rel - r for output row r; this
+  // warp group takes template rows [j_lo, j_hi)
   auto process = [&](const uint32_t (&wv)[WT + 2], int rel) {
-    if (rel >= R - 1 && rel <= a.ht - 1) {
+    if (rel - (R - 1) >= j_lo && rel <= j_hi - 1) {
       row_fixed<R, WT, true>(wv, tmpl_s, rel, 0u, sI, sQ, sT);
     } else {
       unsigned mask = 0;
 #pragma unroll
       for (int r = 0; r < R; ++r)
-        if (rel - r >= 0 && rel - r < a.ht) mask |= 1u << r;
+        if (rel - r >= j_lo && rel - r < j_hi) mask |= 1u << r;
       row_fixed<R, WT, false>(wv, tmpl_s, rel, mask, sI, sQ, sT);
     }
   };
   static_assert(WT % 2 == 0, "fixed path expects an even word count");
+  const int rel_end = min(nrows, j_hi + R - 1);
   uint32_t wa[WT + 2], wb[WT + 2];
-  if (nrows > 0) load_row(0, wa);
-  for (int rel = 0; rel < nrows; rel += 2) {
-    if (rel + 1 < nrows) load_row(rel + 1, wb);
+  if (j_lo < rel_end) load_row(j_lo, wa);
+  for (int rel = j_lo; rel < rel_end; rel += 2) {
+    if (rel + 1 < rel_end) load_row(rel + 1, wb);
     process(wa, rel);
-    if (rel + 1 >= nrows) break;
-    if (rel + 2 < nrows) load_row(rel + 2, wa);
+    if (rel + 1 >= rel_end) break;
+    if (rel + 2 < rel_end) load_row(rel + 2, wa);
     process(wb, rel + 1);
+  }
+  if (kSplit > 1) {
+    // groups 1.. hand their partial sums to group 0 through shared memory
+    constexpr int E = 3 * R * kCols;
+    uint32_t *part = reinterpret_cast<uint32_t *>(tile + size_t(TY + a.ht - 1) * RB);
+    __syncthreads();                        // tile reads done; part may be written
+    if (ks > 0) {
+      uint32_t *dst = part + ((ks - 1) * kWarpsPerCta + warp) * E * 32 + lane;
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int c = 0; c < kCols; ++c) {
+          const int e = (r * kCols + c) * 3;
+          dst[(e + 0) * 32] = sI[r][c];
+          dst[(e + 1) * 32] = sQ[r][c];
+          dst[(e + 2) * 32] = sT[r][c];
+        }
+    }
+    __syncthreads();
+    if (ks > 0) return;
+#pragma unroll 1
+    for (int g = 1; g < kSplit; ++g) {
+      const uint32_t *src = part + ((g - 1) * kWarpsPerCta + warp) * E * 32 + lane;
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int c = 0; c < kCols; ++c) {
+          const int e = (r * kCols + c) * 3;
+          sI[r][c] += src[(e + 0) * 32];
+          sQ[r][c] += src[(e + 1) * 32];
+          sT[r][c] += src[(e + 2) * 32];
+        }
+    }
   }
   epilogue<R>(a, x0, y0, sI, sQ, sT, sum_t, template_rsqrt(a, sum_t, sum_t_sq));
 }
@@ -405,7 +452,7 @@ cudaError_t launch_tiles(Kernel kernel, const NccArgs &a, size_t smem,
                          cudaStream_t stream) {
   cudaError_t e = set_smem(kernel, smem);
   if (e != cudaSuccess) return e;
-  kernel<<<a.units, kThreads, smem, stream>>>(a);
+  kernel<<<a.units, kFixedThreads, smem, stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -442,7 +489,8 @@ cudaError_t ncc_u8_launch(const uint8_t *image, int w, int h,
     a.units = int(tiles);
     auto tile_smem = [&](int wtw) {
       const size_t rb = (kHalfUnitCols + 4 * wtw + 8 + 15) & ~15;
-      return smem + size_t(TY + ht - 1) * rb;
+      const size_t part = size_t(kSplit - 1) * kWarpsPerCta * 32 * 3 * R * kCols * 4;
+      return smem + size_t(TY + ht - 1) * rb + part;
     };
     const size_t ts = tile_smem(a.wtw);
     if (ts > 200 * 1024) goto general;   // very tall template: general path
