@@ -180,6 +180,29 @@ def event_time_steps(torch, fn, steps, flush):
     return [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
 
+def graph_time_per_call(torch, fn, calls=20):
+    """Device time per call from replaying a CUDA graph of `calls` calls
+    (host launch overhead excluded; L2 warm)."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(calls):
+                fn()
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    g.replay()
+    e1.record()
+    e1.synchronize()
+    return e0.elapsed_time(e1) / calls
+
+
 def source_hash(*paths):
     h = hashlib.sha256()
     for p in paths:
@@ -324,8 +347,9 @@ def extras_workloads(torch, corr, wl, dev, flush, sms, dp4a_probe, ffma_probe):
         t = event_time_steps(torch, fn, reps, flush)
         ms = statistics.median(t)
         rate = w.offsets * dp4a_per_offset(w) / (ms * 1e-3)
+        gms = graph_time_per_call(torch, fn)
         out[key] = {"workload": w.name, "offsets_per_s": w.offsets / (ms * 1e-3),
-                    "us_per_launch": ms * 1e3,
+                    "us_per_launch": ms * 1e3, "us_per_launch_graph_warm_l2": gms * 1e3,
                     "roofline": {"bound": "alu", "achieved": rate / 1e12,
                                  "peak": dp4a_peak / 1e12, "unit": "Tdp4a/s",
                                  "frac": rate / dp4a_peak}}
@@ -337,7 +361,9 @@ def extras_workloads(torch, corr, wl, dev, flush, sms, dp4a_probe, ffma_probe):
         t = event_time_steps(torch, fn, 50, flush)
         ms = statistics.median(t)
         flops = w.flops / (ms * 1e-3)
+        gms = graph_time_per_call(torch, fn)
         out[key] = {"workload": w.name, "gflops": flops / 1e9, "us_per_launch": ms * 1e3,
+                    "us_per_launch_graph_warm_l2": gms * 1e3,
                     "roofline": {"bound": "alu", "achieved": flops / 1e12,
                                  "peak": 2 * ffma_peak / 1e12, "unit": "TFLOP/s",
                                  "frac": flops / (2 * ffma_peak)}}

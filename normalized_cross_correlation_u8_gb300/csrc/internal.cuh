@@ -8,6 +8,14 @@
 
 namespace corr {
 
+// Number of SMs of the current device (queried once per device).
+int device_sm_count();
+
+// Let `kernel` use up to the device's opt-in shared memory (less its static
+// shared memory).  The attribute persists, so the driver is called once per
+// (device, kernel).
+cudaError_t allow_dynamic_smem(const void *kernel);
+
 // Launches the u8 normalized cross-correlation on `stream`.  Arguments are
 // already validated by the C ABI layer (corr_api.cu).
 cudaError_t ncc_u8_launch(const uint8_t *image, int w, int h,

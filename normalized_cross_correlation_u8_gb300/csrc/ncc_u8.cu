@@ -430,9 +430,7 @@ __global__ void __launch_bounds__(kThreads)
 
 template <typename Kernel>
 cudaError_t set_smem(Kernel kernel, size_t smem) {
-  if (smem > 48 * 1024)
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                int(smem));
+  if (smem > 48 * 1024) return allow_dynamic_smem(reinterpret_cast<const void *>(kernel));
   return cudaSuccess;
 }
 

@@ -80,17 +80,17 @@ __device__ __forceinline__ float4 lds128(uint32_t addr) {
   return v;
 }
 
-// Block J of a round: one float4 of L at la + 16 J, for each q a float4 of
-// R_q at ra[q] + 16 J into ring positions 4 (J mod 3) .. +3; shift p at step
-// s reads position (4 (J mod 3) + s - p) mod 12.
-template <int J>
-__device__ __forceinline__ void ring_block(float (&acc)[kQ][kP],
-                                           float (&ring)[kQ][kRing], uint32_t la,
-                                           const uint32_t (&ra)[kQ]) {
+// Block J of a round: one float4 of L at la + 16 J, for each of the NQ rows a
+// float4 of R_q at ra[q] + 16 J into ring positions 4 (J mod 3) .. +3; shift
+// p at step s reads position (4 (J mod 3) + s - p) mod 12.
+template <int J, int NQ>
+__device__ __forceinline__ void ring_block(float (&acc)[NQ][kP],
+                                           float (&ring)[NQ][kRing], uint32_t la,
+                                           const uint32_t (&ra)[NQ]) {
   constexpr int JR = J % 3;
   const float4 lv4 = lds128<16 * J>(la);
 #pragma unroll
-  for (int q = 0; q < kQ; ++q) {
+  for (int q = 0; q < NQ; ++q) {
     const float4 v = lds128<16 * J>(ra[q]);
     ring[q][4 * JR + 0] = v.x;
     ring[q][4 * JR + 1] = v.y;
@@ -103,7 +103,7 @@ __device__ __forceinline__ void ring_block(float (&acc)[kQ][kP],
 #pragma unroll
     for (int p = 0; p < kP; ++p)
 #pragma unroll
-      for (int q = 0; q < kQ; ++q)
+      for (int q = 0; q < NQ; ++q)
         acc[q][p] = fmaf(lv[s], ring[q][(4 * JR + s - p + 2 * kRing) % kRing], acc[q][p]);
 }
 
@@ -112,15 +112,16 @@ __device__ __forceinline__ void ring_block(float (&acc)[kQ][kP],
 //   r4[q]: float4 index of R_q[u0] (u0 = xlo - dx0) in shared memory
 // Block b covers x = xlo + 4b .. xlo + 4b + 3.  R_q[u0 + j] lives at ring
 // position (j - 4 b0) mod 12.
-__device__ __forceinline__ void lane_blocks(float (&acc)[kQ][kP], int l4,
-                                            const int (&r4)[kQ], int b0, int b1) {
+template <int NQ>
+__device__ __forceinline__ void lane_blocks(float (&acc)[NQ][kP], int l4,
+                                            const int (&r4)[NQ], int b0, int b1) {
   static_assert(kP == 8 && kRing == 12, "ring preload assumes P = 8");
   if (b0 >= b1) return;
   const uint32_t base = uint32_t(__cvta_generic_to_shared(g_smem4));
-  float ring[kQ][kRing];
-  uint32_t ra[kQ];
+  float ring[NQ][kRing];
+  uint32_t ra[NQ];
 #pragma unroll
-  for (int q = 0; q < kQ; ++q) {
+  for (int q = 0; q < NQ; ++q) {
     // R[u0 + 4 b0 - 8 .. u0 + 4 b0 - 1] -> positions 4..11
     ra[q] = base + 16u * uint32_t(r4[q] + b0);
     const float4 a = lds128<-32>(ra[q]);
@@ -132,23 +133,23 @@ __device__ __forceinline__ void lane_blocks(float (&acc)[kQ][kP], int l4,
   uint32_t la = base + 16u * uint32_t(l4 + b0);
   int b = b0;
   for (; b + 6 <= b1; b += 6) {
-    ring_block<0>(acc, ring, la, ra);
-    ring_block<1>(acc, ring, la, ra);
-    ring_block<2>(acc, ring, la, ra);
-    ring_block<3>(acc, ring, la, ra);
-    ring_block<4>(acc, ring, la, ra);
-    ring_block<5>(acc, ring, la, ra);
+    ring_block<0, NQ>(acc, ring, la, ra);
+    ring_block<1, NQ>(acc, ring, la, ra);
+    ring_block<2, NQ>(acc, ring, la, ra);
+    ring_block<3, NQ>(acc, ring, la, ra);
+    ring_block<4, NQ>(acc, ring, la, ra);
+    ring_block<5, NQ>(acc, ring, la, ra);
     la += 96;
 #pragma unroll
-    for (int q = 0; q < kQ; ++q) ra[q] += 96;
+    for (int q = 0; q < NQ; ++q) ra[q] += 96;
   }
   // 0..5 remaining blocks, positions continue (J mod 3)
   const int rem = b1 - b;
-  if (rem > 0) ring_block<0>(acc, ring, la, ra);
-  if (rem > 1) ring_block<1>(acc, ring, la, ra);
-  if (rem > 2) ring_block<2>(acc, ring, la, ra);
-  if (rem > 3) ring_block<3>(acc, ring, la, ra);
-  if (rem > 4) ring_block<4>(acc, ring, la, ra);
+  if (rem > 0) ring_block<0, NQ>(acc, ring, la, ra);
+  if (rem > 1) ring_block<1, NQ>(acc, ring, la, ra);
+  if (rem > 2) ring_block<2, NQ>(acc, ring, la, ra);
+  if (rem > 3) ring_block<3, NQ>(acc, ring, la, ra);
+  if (rem > 4) ring_block<4, NQ>(acc, ring, la, ra);
 }
 
 // Geometry of one output block of a warp: shifts dy0..dy0+3 x dx0..dx0+7.
@@ -175,21 +176,21 @@ __device__ __forceinline__ Block make_block(int H, int W, int dy0, int dx0) {
 // row / R row (before the kPadL zero columns).  With n == 32 lane ph takes
 // row y + ph; with fewer rows each row is split into k = 32 / n x sub-ranges
 // (lanes past n*k idle).
-template <typename LRow, typename RRow>
+template <int NPH, typename LRow, typename RRow>
 __device__ __forceinline__ void warp_pass(float (&acc)[kQ][kP], const Block &k,
-                                          int y, int n, int lane, LRow lrow,
+                                          int y, int n, int ph, LRow lrow,
                                           RRow rrow) {
   if (n <= 0 || k.nb == 0) return;
   int row, b0, b1;
-  if (n >= 32) {
-    row = y + lane;
+  if (n >= NPH) {
+    row = y + ph;
     b0 = 0;
     b1 = k.nb;
   } else {
-    const int parts = 32 / n;
-    const int part = lane / n;
+    const int parts = NPH / n;
+    const int part = ph / n;
     if (part >= parts) return;
-    row = y + (lane - part * n);
+    row = y + (ph - part * n);
     b0 = part * k.nb / parts;
     b1 = (part + 1) * k.nb / parts;
   }
@@ -198,7 +199,37 @@ __device__ __forceinline__ void warp_pass(float (&acc)[kQ][kP], const Block &k,
   int r4[kQ];
 #pragma unroll
   for (int q = 0; q < kQ; ++q) r4[q] = (rrow(row - k.dy0 - q) + kPadL + u0) >> 2;
-  lane_blocks(acc, l4, r4, b0, b1);
+  lane_blocks<kQ>(acc, l4, r4, b0, b1);
+}
+
+// Reduce-scatter over groups of NPH lanes (lanes of a group differ in their
+// low log2(NPH) bits): after log2(NPH) steps of halving, lane ph of a group
+// holds the group's full sums of outputs (32/NPH) * ph + i, i < 32/NPH, in
+// v[i].  Clears the accumulators.
+template <int NPH>
+__device__ __forceinline__ void reduce_scatter_group(float (&acc)[kQ][kP], int lane,
+                                                     float (&out)[32 / NPH]) {
+  float v[32];
+#pragma unroll
+  for (int q = 0; q < kQ; ++q)
+#pragma unroll
+    for (int p = 0; p < kP; ++p) v[q * kP + p] = acc[q][p];
+#pragma unroll
+  for (int o = NPH / 2, m = 16; o >= 1; o >>= 1, m >>= 1) {
+    const bool upper = (lane & o) != 0;   // keep v[m..2m) if set, else v[0..m)
+#pragma unroll
+    for (int i = 0; i < m; ++i) {
+      const float send = upper ? v[i] : v[i + m];
+      const float keep = upper ? v[i + m] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 32 / NPH; ++i) out[i] = v[i];
+#pragma unroll
+  for (int q = 0; q < kQ; ++q)
+#pragma unroll
+    for (int p = 0; p < kP; ++p) acc[q][p] = 0.f;
 }
 
 // Reduce-scatter over the 32 lanes: at each step a lane keeps one half of
@@ -280,6 +311,8 @@ struct XArgs {
   int nbands;     // rows kernel: row bands of kBandRows (split-row)
   int part_row;   // rows kernel: floats per partial-sum row (8 * ngroups)
   float *part;    // rows kernel: band partial sums (nbands > 1)
+  int nrblk;      // bcast kernel: blocks of 32 rights
+  int npairblk;   // bcast kernel: blocks of kWarps dx-group pairs
 };
 
 // ---------------------------------------------------------------------------
@@ -391,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 2) xcorr_rows_kernel(const XArgs a) 
     }
     const int yr_first = yc - k.dy0 - (kQ - 1);
     if (active)
-      warp_pass(acc, k, yc, min(kChunk, y_end - yc), lane,
+      warp_pass<32>(acc, k, yc, min(kChunk, y_end - yc), lane,
                 [&](int y) { return buf + (y - yc) * S; },
                 [&](int yr) { return buf + (kChunkL + yr - yr_first) * S; });
   }
@@ -431,44 +464,272 @@ __global__ void xcorr_band_sum_kernel(const XArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// pair kernel: the CTA stages one whole pair (R with kQ-1 zero rows above and
-// below), then its warps loop over output blocks of that pair.
+// pair kernel: the CTA stages NSLOT whole pairs (pairs NSLOT*pb + s; R with
+// kQ-1 zero rows above and below), then its warps pull output blocks
+// (4 dy x 8 dx) from a shared counter.  Lane (s, ph) of a warp works on block
+// b of pair slot s and takes overlap rows ph, ph + NPH, ... (NPH = 32/NSLOT),
+// so a lane sums NSLOT times more rows per block than with one slot, and the
+// reduce-scatter runs over NPH lanes.
 // ---------------------------------------------------------------------------
+template <int NSLOT>
 __global__ void __launch_bounds__(kThreads, 2) xcorr_pair_kernel(const XArgs a) {
+  constexpr int NPH = 32 / NSLOT;
   float *sm = reinterpret_cast<float *>(g_smem4);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ int next_item;
+  const int lane = threadIdx.x & 31;
   const int H = a.H, W = a.W, S = a.S;
-  const int pair = blockIdx.x / a.parts, part = blockIdx.x - pair * a.parts;
-  const int li = pair / a.nr, ri = pair - li * a.nr;
+  const int pb = blockIdx.x / a.parts, part = blockIdx.x - pb * a.parts;
+  const int npairs = a.nl * a.nr;
   const size_t mat = size_t(H) * W;
-  const float *L = a.left + li * mat;
-  const float *R = a.right + ri * mat;
   constexpr int kPadY = kQ - 1;
   const int rrows = H + 2 * kPadY;
-  zero_smem(sm, (H + rrows) * S);
+  const int slot_floats = (H + rrows) * S;
+  zero_smem(sm, NSLOT * slot_floats);
+  if (threadIdx.x == 0) next_item = 0;
   __syncthreads();
-  stage_rows(sm, 0, H, S, W, a.vec4, [&](int r) -> const float * { return L + size_t(r) * W; });
-  stage_rows(sm, H * S, rrows, S, W, a.vec4, [&](int r) -> const float * {
-    const int yr = r - kPadY;
-    return (yr >= 0 && yr < H) ? R + size_t(yr) * W : nullptr;
-  });
+#pragma unroll
+  for (int sl = 0; sl < NSLOT; ++sl) {
+    const int pair = NSLOT * pb + sl;
+    if (pair >= npairs) continue;
+    const int li = pair / a.nr, ri = pair - li * a.nr;
+    const float *L = a.left + li * mat;
+    const float *R = a.right + ri * mat;
+    stage_rows(sm, sl * slot_floats, H, S, W, a.vec4,
+               [&](int r) -> const float * { return L + size_t(r) * W; });
+    stage_rows(sm, sl * slot_floats + H * S, rrows, S, W, a.vec4, [&](int r) -> const float * {
+      const int yr = r - kPadY;
+      return (yr >= 0 && yr < H) ? R + size_t(yr) * W : nullptr;
+    });
+  }
   __syncthreads();
 
+  const int slot = lane / NPH, ph = lane - slot * NPH;
+  const int pair = NSLOT * pb + slot;
+  const bool pair_ok = pair < npairs;
+  const int base = slot * slot_floats;
   float acc[kQ][kP];
 #pragma unroll
   for (int q = 0; q < kQ; ++q)
 #pragma unroll
     for (int p = 0; p < kP; ++p) acc[q][p] = 0.f;
-  float *out_pair = a.out + size_t(pair) * (2 * H - 1) * (2 * W - 1);
+  float *out_pair = a.out + size_t(pair_ok ? pair : 0) * (2 * H - 1) * (2 * W - 1);
   const int nitems = a.ndyb * a.ngroups;
-  for (int it = part + a.parts * warp; it < nitems; it += a.parts * kWarps) {
+  const int mine = (nitems - part + a.parts - 1) / a.parts;   // items part + k*parts
+  for (;;) {
+    int u = 0;
+    if (lane == 0) u = atomicAdd(&next_item, 1);
+    u = __shfl_sync(0xffffffffu, u, 0);
+    if (u >= mine) break;
+    const int it = part + u * a.parts;                      // centre-first rank
     const int dyb = centered(it % a.ndyb, a.ndyb);
     const int g = centered(it / a.ndyb, a.ngroups);
     const Block k = make_block(H, W, dyb * kQ - (H - 1), a.dxbase + g * kP);
-    for (int y = k.ylo; y < k.yhi; y += 32)
-      warp_pass(acc, k, y, min(32, k.yhi - y), lane, [&](int yy) { return yy * S; },
-                [&](int yr) { return (H + kPadY + yr) * S; });
-    reduce_store(acc, k, lane, H, W, out_pair);
+    if (pair_ok)
+      for (int y = k.ylo; y < k.yhi; y += NPH)
+        warp_pass<NPH>(acc, k, y, min(NPH, k.yhi - y), ph,
+                       [&](int yy) { return base + yy * S; },
+                       [&](int yr) { return base + (H + kPadY + yr) * S; });
+    float v[32 / NPH];
+    reduce_scatter_group<NPH>(acc, lane, v);
+#pragma unroll
+    for (int i = 0; i < 32 / NPH; ++i) {
+      const int idx = (32 / NPH) * ph + i;
+      const int dy = k.dy0 + idx / kP, dx = k.dx0 + idx % kP;
+      if (pair_ok && dy > -H && dy < H && dx > -W && dx < W)
+        out_pair[size_t(dy + H - 1) * (2 * W - 1) + (dx + W - 1)] = v[i];
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// bcast kernel ("rights in lanes": one-to-many and n-to-m with >= 32 rights
+// per left).  A CTA owns one left, 32 rights (one per lane), one shift dy
+// and kWarps pairs of dx groups.  Lane r of every warp owns right r, so all
+// lanes of a warp share one left row (a broadcast load), one y range (the
+// exact overlap rows of dy) and one x range: control flow is uniform and
+// every lane sums all rows of its outputs itself -- no cross-lane reduction.
+// Warp w takes dx groups g = w and g + ceil(G/2), whose x ranges add up to
+// about W, so the warps of a CTA carry equal work between chunk barriers.  Overlap
+// rows are staged kBRows at a time (left rows, then per right a slab of
+// kBRows rows padded to an odd number of 16-byte units) with cp.async into
+// two buffers.
+// ---------------------------------------------------------------------------
+constexpr int kBRows = 4;
+constexpr int kBRights = 2;               // rights per lane
+constexpr int kBMats = 1 + 32 * kBRights; // matrices staged per chunk
+
+__device__ __forceinline__ int bcast_slab(int S) { return kBRows * S + 4; }
+__device__ __forceinline__ int bcast_buf(int S) {
+  return kBRows * S + 32 * kBRights * bcast_slab(S);
+}
+
+// Issue one chunk: left rows yc .. yc+kBRows-1 (zero past yhi) and, for each
+// of the CTA's 32*kBRights rights, rows yc-dy .. (zero past nr or past yhi).
+// The flattened (matrix, row, column) index advances by blockDim.x per step;
+// its three parts are carried instead of divided.
+__device__ __forceinline__ void issue_bchunk(const XArgs &a, uint32_t sbase, int buf,
+                                             const float *L, int r_first, int yc,
+                                             int yhi, int dy) {
+  const int W = a.W, S = a.S, H = a.H;
+  const bool vec4 = a.vec4;
+  const int step = vec4 ? 4 : 1, n = vec4 ? (W >> 2) : W;
+  const size_t mat = size_t(H) * W;
+  const int slab = bcast_slab(S);
+  const int per_mat = kBRows * n;
+  const int total = kBMats * per_mat;
+  const int stride = blockDim.x;
+  // stride = sm * per_mat + sr * n + sc
+  const int sm_ = stride / per_mat, srem = stride - sm_ * per_mat;
+  const int sr = srem / n, sc = srem - sr * n;
+  int m = threadIdx.x / per_mat;
+  int r = (threadIdx.x - m * per_mat) / n;
+  int c = threadIdx.x - m * per_mat - r * n;
+  for (int e = threadIdx.x; e < total; e += stride) {
+    const int y = yc + r;
+    bool ok = y < yhi;
+    const float *src;
+    int dst;
+    if (m == 0) {
+      src = L + (ok ? size_t(y) * W + c * step : 0);
+      dst = buf + r * S + kPadL + c * step;
+    } else {
+      const int ri = r_first + (m - 1);
+      ok = ok && ri < a.nr;
+      src = a.right + (ok ? size_t(ri) * mat + size_t(y - dy) * W + c * step : 0);
+      dst = buf + kBRows * S + (m - 1) * slab + r * S + kPadL + c * step;
+    }
+    cp_async(sbase + 4u * uint32_t(dst), src, ok, vec4);
+    c += sc;
+    r += sr;
+    m += sm_;
+    if (c >= n) { c -= n; ++r; }
+    if (r >= kBRows) { r -= kBRows; ++m; }
+  }
+}
+
+// x geometry of one dx group: first x (multiple of 4), u0 = xlo - dx0, and
+// number of 4-wide blocks of the union of its 8 shifts' overlaps.
+struct XGroup {
+  int dx0, xlo, u0, nb;
+};
+
+__device__ __forceinline__ XGroup make_xgroup(int W, int dx0) {
+  XGroup g;
+  g.dx0 = dx0;
+  g.xlo = max(0, dx0);
+  g.u0 = g.xlo - dx0;
+  const int xhi = min(W, W + dx0 + kP - 1);
+  g.nb = xhi > g.xlo ? (xhi - g.xlo + 3) >> 2 : 0;
+  return g;
+}
+
+constexpr int kBWarps = 2 * kWarps;     // two row halves x kWarps group pairs
+
+__global__ void __launch_bounds__(32 * kBWarps, 1) xcorr_bcast_kernel(const XArgs a) {
+  const uint32_t sbase = uint32_t(__cvta_generic_to_shared(g_smem4));
+  float *sm = reinterpret_cast<float *>(g_smem4);
+  const int warp_id = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = warp_id % kWarps;    // dx-group pair of this warp
+  const int rh = warp_id / kWarps;      // row half: rows 2*rh, 2*rh+1 of each chunk
+  const int H = a.H, W = a.W, S = a.S;
+  const int G = a.ngroups, ngp = (G + 1) / 2;
+  int item = blockIdx.x;
+  const int rb = item % a.nrblk;
+  item /= a.nrblk;
+  const int li = item % a.nl;
+  item /= a.nl;
+  const int pbk = item % a.npairblk;
+  item /= a.npairblk;
+  const int dy = centered(item, 2 * H - 1) - (H - 1);   // costly (central) dy first
+  const int ylo = max(0, dy), yhi = min(H, H + dy);
+  const float *L = a.left + size_t(li) * H * W;
+
+  // groups g and g + ngp: shifts dx and dx + 8*ngp (about dx + W), whose x
+  // ranges add up to about W, so every warp carries the same work
+  const int gp = pbk * kWarps + warp;
+  const bool gp_ok = gp < ngp;
+  const int gA = gp, gB = gp + ngp;
+  const bool has_b = gp_ok && gB < G;
+  const XGroup xa = make_xgroup(W, a.dxbase + gA * kP);
+  const XGroup xb = make_xgroup(W, a.dxbase + gB * kP);
+  const int r_first = rb * 32 * kBRights;   // lane owns rights r_first + lane + 32 j
+
+  const int bufn = bcast_buf(S), slab = bcast_slab(S);
+  zero_smem(sm, 2 * bufn);
+  __syncthreads();
+  float accA[kBRights][kP], accB[kBRights][kP];
+#pragma unroll
+  for (int j = 0; j < kBRights; ++j)
+#pragma unroll
+    for (int p = 0; p < kP; ++p) accA[j][p] = accB[j][p] = 0.f;
+
+  const int nchunks = (yhi - ylo + kBRows - 1) / kBRows;
+  if (nchunks > 0) issue_bchunk(a, sbase, 0, L, r_first, ylo, yhi, dy);
+  cp_async_commit();
+  for (int c = 0; c < nchunks; ++c) {
+    const int yc = ylo + c * kBRows;
+    const int buf = (c & 1) * bufn;
+    cp_async_wait_all();
+    __syncthreads();
+    if (c + 1 < nchunks) {
+      issue_bchunk(a, sbase, ((c + 1) & 1) * bufn, L, r_first, yc + kBRows, yhi, dy);
+      cp_async_commit();
+    }
+    if (!gp_ok) continue;
+    const int rows = min(kBRows, yhi - yc);
+    for (int k = 2 * rh; k < min(rows, 2 * rh + 2); ++k) {
+      const int lrow = buf + k * S + kPadL;
+      const int rrow = buf + kBRows * S + lane * slab + k * S + kPadL;
+      {
+        int r4[kBRights];
+#pragma unroll
+        for (int j = 0; j < kBRights; ++j) r4[j] = (rrow + 32 * j * slab + xa.u0) >> 2;
+        lane_blocks<kBRights>(accA, (lrow + xa.xlo) >> 2, r4, 0, xa.nb);
+      }
+      if (has_b) {
+        int r4[kBRights];
+#pragma unroll
+        for (int j = 0; j < kBRights; ++j) r4[j] = (rrow + 32 * j * slab + xb.u0) >> 2;
+        lane_blocks<kBRights>(accB, (lrow + xb.xlo) >> 2, r4, 0, xb.nb);
+      }
+    }
+  }
+  // row half 1 hands its partial sums to row half 0 (fixed order: exact
+  // same result on every run)
+  __syncthreads();                       // chunk buffers are free again
+  constexpr int kPart = 2 * kBRights * kP;   // partial sums per lane
+  float *part = sm + (warp * kPart) * 32 + lane;
+  if (rh == 1) {
+#pragma unroll
+    for (int j = 0; j < kBRights; ++j)
+#pragma unroll
+      for (int p = 0; p < kP; ++p) {
+        part[(j * kP + p) * 32] = accA[j][p];
+        part[((kBRights + j) * kP + p) * 32] = accB[j][p];
+      }
+  }
+  __syncthreads();
+  if (rh == 1 || !gp_ok) return;
+  const int OW = 2 * W - 1;
+#pragma unroll
+  for (int j = 0; j < kBRights; ++j) {
+    const int ri = r_first + lane + 32 * j;
+    if (ri >= a.nr) continue;
+    float *orow = a.out + (size_t(li) * a.nr + ri) * size_t(2 * H - 1) * OW +
+                  size_t(dy + H - 1) * OW;
+#pragma unroll
+    for (int p = 0; p < kP; ++p) {
+      const int dx = xa.dx0 + p;
+      if (dx > -W && dx < W) orow[dx + W - 1] = accA[j][p] + part[(j * kP + p) * 32];
+    }
+    if (has_b) {
+#pragma unroll
+      for (int p = 0; p < kP; ++p) {
+        const int dx = xb.dx0 + p;
+        if (dx > -W && dx < W)
+          orow[dx + W - 1] = accB[j][p] + part[((kBRights + j) * kP + p) * 32];
+      }
+    }
   }
 }
 
@@ -480,7 +741,7 @@ __global__ void __launch_bounds__(kThreads, 2) xcorr_pair_kernel(const XArgs a) 
 // of a block pair round-robin in a centre-first order and pulled by the
 // CTA's warps from a shared counter.
 // ---------------------------------------------------------------------------
-constexpr int kTinyL = 32, kTinyR = 16, kTinyWarps = 8;
+constexpr int kTinyL = 32, kTinyR = 16, kTinyWarps = 16;
 
 struct TinyArgs {
   const float *left;
@@ -503,49 +764,47 @@ __global__ void __launch_bounds__(32 * kTinyWarps) xcorr_tiny_kernel(const TinyA
   const int rbk = bid % a.rblocks, lbk = bid / a.rblocks;
   const int l_base = lbk * kTinyL, r_base = rbk * kTinyR;
 
-  // stage: thread (m, pos4) reads 16 bytes (positions 4 pos4 .. +3) of
-  // matrix m and scatters them to Ls[pos*32 + m] (lanes of a warp take 32
-  // consecutive m, so each shared store touches 32 distinct banks).  H*W is
-  // a multiple of 4 on this path when the rows are 16-byte aligned;
-  // otherwise element loads are used.
+  // stage: item (m, p4) = 16 bytes (positions 4 p4 .. +3) of matrix m,
+  // scattered to Xs[pos * NB + m]; lanes of a warp take consecutive m, so
+  // each shared store hits 32 distinct banks.  Four items' loads are issued
+  // before their stores so their latencies overlap.
   {
     const int hw4 = (HW + 3) >> 2;
-    for (int i = threadIdx.x; i < hw4 * kTinyL; i += blockDim.x) {
-      const int m = i % kTinyL, p4 = i / kTinyL;
-      const int l = l_base + m;
-      float e[4] = {0.f, 0.f, 0.f, 0.f};
-      if (l < a.nl) {
-        const float *src = a.left + size_t(l) * HW + 4 * p4;
-        if (a.vec4) {
-          const float4 v = __ldg(reinterpret_cast<const float4 *>(src));
-          e[0] = v.x; e[1] = v.y; e[2] = v.z; e[3] = v.w;
-        } else {
+    auto stage = [&](float *Xs, const float *src0, int base_m, int nmat, int NB) {
+      const int items = hw4 * NB;
+      for (int i0 = threadIdx.x; i0 < items; i0 += 4 * blockDim.x) {
+        float e[4][4];
 #pragma unroll
-          for (int t = 0; t < 4; ++t) e[t] = 4 * p4 + t < HW ? __ldg(src + t) : 0.f;
+        for (int k = 0; k < 4; ++k) {
+          const int i = i0 + k * blockDim.x;
+          const int m = i % NB, p4 = i / NB;
+          const int mm = base_m + m;
+#pragma unroll
+          for (int t = 0; t < 4; ++t) e[k][t] = 0.f;
+          if (i < items && mm < nmat) {
+            const float *src = src0 + size_t(mm) * HW + 4 * p4;
+            if (a.vec4) {
+              const float4 v = __ldg(reinterpret_cast<const float4 *>(src));
+              e[k][0] = v.x; e[k][1] = v.y; e[k][2] = v.z; e[k][3] = v.w;
+            } else {
+#pragma unroll
+              for (int t = 0; t < 4; ++t) e[k][t] = 4 * p4 + t < HW ? __ldg(src + t) : 0.f;
+            }
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int i = i0 + k * blockDim.x;
+          if (i >= items) break;
+          const int m = i % NB, p4 = i / NB;
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            if (4 * p4 + t < HW) Xs[(4 * p4 + t) * NB + m] = e[k][t];
         }
       }
-#pragma unroll
-      for (int t = 0; t < 4; ++t)
-        if (4 * p4 + t < HW) Ls[(4 * p4 + t) * kTinyL + m] = e[t];
-    }
-    for (int i = threadIdx.x; i < hw4 * kTinyR; i += blockDim.x) {
-      const int m = i % kTinyR, p4 = i / kTinyR;
-      const int r = r_base + m;
-      float e[4] = {0.f, 0.f, 0.f, 0.f};
-      if (r < a.nr) {
-        const float *src = a.right + size_t(r) * HW + 4 * p4;
-        if (a.vec4) {
-          const float4 v = __ldg(reinterpret_cast<const float4 *>(src));
-          e[0] = v.x; e[1] = v.y; e[2] = v.z; e[3] = v.w;
-        } else {
-#pragma unroll
-          for (int t = 0; t < 4; ++t) e[t] = 4 * p4 + t < HW ? __ldg(src + t) : 0.f;
-        }
-      }
-#pragma unroll
-      for (int t = 0; t < 4; ++t)
-        if (4 * p4 + t < HW) Rs[(4 * p4 + t) * kTinyR + m] = e[t];
-    }
+    };
+    stage(Ls, a.left, l_base, a.nl, kTinyL);
+    stage(Rs, a.right, r_base, a.nr, kTinyR);
   }
   if (threadIdx.x == 0) next_unit = 0;
   __syncthreads();
@@ -569,20 +828,26 @@ __global__ void __launch_bounds__(32 * kTinyWarps) xcorr_tiny_kernel(const TinyA
     for (int i = 0; i < 4; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    const int nx = xhi - xlo;
     for (int y = ylo; y < yhi; ++y) {
       const float4 *lp = reinterpret_cast<const float4 *>(Ls + (y * W + xlo) * kTinyL) + lb;
       const float4 *rp =
           reinterpret_cast<const float4 *>(Rs + ((y - dy) * W + (xlo - dx)) * kTinyR) + rb;
-#pragma unroll 4
-      for (int x = xlo; x < xhi; ++x) {
-        const float4 l = *lp, r = *rp;
+      // the next step's operands are loaded while this step's FMAs run
+      float4 l = lp[0], r = rp[0];
+      for (int t = 0; t < nx; ++t) {
+        float4 ln = l, rn = r;
+        if (t + 1 < nx) {
+          ln = lp[(t + 1) * (kTinyL / 4)];
+          rn = rp[(t + 1) * (kTinyR / 4)];
+        }
         const float lv[4] = {l.x, l.y, l.z, l.w}, rv[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
           for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(lv[i], rv[j], acc[i][j]);
-        lp += kTinyL / 4;
-        rp += kTinyR / 4;
+        l = ln;
+        r = rn;
       }
     }
     const size_t o = size_t(dy + H - 1) * ndx + (dx + W - 1);
@@ -728,12 +993,7 @@ cudaError_t launch_direct(const float *left, int nl, const float *right, int nr,
   return cudaGetLastError();
 }
 
-int sm_count() {
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 1;
-  return sms > 0 ? sms : 1;
-}
+int sm_count() { return device_sm_count(); }
 
 cudaError_t launch_tiny(const float *left, int nl, const float *right, int nr, int H,
                         int W, float *out, cudaStream_t stream) {
@@ -758,8 +1018,7 @@ cudaError_t launch_tiny(const float *left, int nl, const float *right, int nr, i
   const long long blocks = bp * a.nc;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   const size_t smem = size_t(H) * W * (kTinyL + kTinyR) * sizeof(float);
-  cudaError_t e = cudaFuncSetAttribute(xcorr_tiny_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void *>(xcorr_tiny_kernel));
   if (e != cudaSuccess) return e;
   xcorr_tiny_kernel<<<unsigned(blocks), 32 * kTinyWarps, smem, stream>>>(a);
   return cudaGetLastError();
@@ -811,13 +1070,15 @@ cudaError_t scratch_alloc(float **ptr, size_t bytes, cudaStream_t stream) {
 
 }  // namespace
 
-// Largest shared staging area of the rows / pair kernels (two CTAs per SM).
+// Largest shared staging area of the rows / pair kernels (two CTAs per SM),
+// and of the bcast kernel (one CTA per SM at worst).
 constexpr size_t kMaxStageSmem = 110 * 1024;
+constexpr size_t kMaxBcastSmem = 200 * 1024;
 
 namespace {
 
 // Which kernel a shape takes, its arguments and the split-row scratch it needs.
-enum class XKind { Tiny, Pair, Rows, Direct };
+enum class XKind { Tiny, Bcast, Pair, Rows, Direct };
 
 struct XPlan {
   XKind kind;
@@ -825,6 +1086,7 @@ struct XPlan {
   size_t smem;           // dynamic shared memory of the pair / rows kernel
   long long blocks;      // grid of the pair / rows kernel
   size_t part_bytes;     // rows kernel with several bands: scratch bytes
+  int nslot;             // pair kernel: pairs staged per CTA
 };
 
 XPlan make_plan(const float *left, int nl, const float *right, int nr, int H, int W,
@@ -833,6 +1095,7 @@ XPlan make_plan(const float *left, int nl, const float *right, int nr, int H, in
   pl.smem = 0;
   pl.blocks = 0;
   pl.part_bytes = 0;
+  pl.nslot = 1;
   const long long pairs = (long long)nl * nr;
   XArgs &a = pl.a;
   a.left = left;
@@ -858,20 +1121,42 @@ XPlan make_plan(const float *left, int nl, const float *right, int nr, int H, in
   a.nbands = 1;
   a.part_row = 0;
   a.part = nullptr;
+  a.nrblk = 0;
+  a.npairblk = 0;
 
-  // pair kernel: the whole pair fits, and there are enough rows per lane
-  const size_t pair_smem = size_t(H + H + 2 * (kQ - 1)) * a.S * sizeof(float);
-  if (pair_smem <= kMaxStageSmem && H >= 24) {
+  // bcast kernel: at least 32 rights per left, rows of 8+ floats, and two
+  // chunk buffers fit
+  {
+    const size_t buf_floats =
+        size_t(kBRows) * a.S + 32 * kBRights * (size_t(kBRows) * a.S + 4);
+    const size_t bsmem = 2 * buf_floats * sizeof(float);
+    const int ngp = (a.ngroups + 1) / 2;
+    a.nrblk = (nr + 32 * kBRights - 1) / (32 * kBRights);
+    a.npairblk = (ngp + kWarps - 1) / kWarps;
+    const long long bblocks = (long long)nl * a.nrblk * a.npairblk * (2LL * H - 1);
+    if (nr >= 32 && W >= 8 && bsmem <= kMaxBcastSmem && bblocks <= 0x7fffffffLL) {
+      pl.kind = XKind::Bcast;
+      pl.smem = bsmem;
+      pl.blocks = bblocks;
+      return pl;
+    }
+  }
+  // pair kernel: whole pairs fit (two per CTA when possible), and there are
+  // enough rows per lane
+  const size_t slot_smem = size_t(H + H + 2 * (kQ - 1)) * a.S * sizeof(float);
+  if (slot_smem <= kMaxStageSmem && H >= 24) {
+    pl.nslot = (pairs >= 2 && 2 * slot_smem <= kMaxStageSmem) ? 2 : 1;
+    const long long pblocks = (pairs + pl.nslot - 1) / pl.nslot;
     const int items = a.ndyb * a.ngroups;
-    long long parts = (4LL * sm_count() + pairs - 1) / pairs;
+    long long parts = (8LL * sm_count() + pblocks - 1) / pblocks;
     const long long max_parts = (items + kWarps - 1) / kWarps;
     if (parts > max_parts) parts = max_parts;
     if (parts < 1) parts = 1;
     a.parts = int(parts);
-    if (pairs * a.parts <= 0x7fffffffLL) {
+    if (pblocks * a.parts <= 0x7fffffffLL) {
       pl.kind = XKind::Pair;
-      pl.smem = pair_smem;
-      pl.blocks = pairs * a.parts;
+      pl.smem = pl.nslot * slot_smem;
+      pl.blocks = pblocks * a.parts;
       return pl;
     }
   }
@@ -899,15 +1184,20 @@ cudaError_t run_plan(XPlan &pl, float *fixed, cudaStream_t stream) {
     return launch_tiny(a.left, a.nl, a.right, a.nr, a.H, a.W, a.out, stream);
   if (pl.kind == XKind::Direct)
     return launch_direct(a.left, a.nl, a.right, a.nr, a.H, a.W, a.out, stream);
-  if (pl.kind == XKind::Pair) {
-    cudaError_t e = cudaFuncSetAttribute(
-        xcorr_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(pl.smem));
+  if (pl.kind == XKind::Bcast) {
+    cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void *>(xcorr_bcast_kernel));
     if (e != cudaSuccess) return e;
-    xcorr_pair_kernel<<<unsigned(pl.blocks), kThreads, pl.smem, stream>>>(a);
+    xcorr_bcast_kernel<<<unsigned(pl.blocks), 32 * kBWarps, pl.smem, stream>>>(a);
     return cudaGetLastError();
   }
-  cudaError_t e = cudaFuncSetAttribute(
-      xcorr_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(pl.smem));
+  if (pl.kind == XKind::Pair) {
+    auto kern = pl.nslot == 2 ? xcorr_pair_kernel<2> : xcorr_pair_kernel<1>;
+    cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void *>(kern));
+    if (e != cudaSuccess) return e;
+    kern<<<unsigned(pl.blocks), kThreads, pl.smem, stream>>>(a);
+    return cudaGetLastError();
+  }
+  cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void *>(xcorr_rows_kernel));
   if (e != cudaSuccess) return e;
   const bool banded = a.nbands > 1;
   const bool pooled = banded && fixed == nullptr;
@@ -950,6 +1240,58 @@ cudaError_t xcorr_f32_launch_scratch(const float *left, int nl, const float *rig
   if (pl.part_bytes > scratch_bytes || (pl.part_bytes > 0 && scratch == nullptr))
     return cudaErrorInvalidValue;
   return run_plan(pl, scratch, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Per-device cached launch attributes.
+// ---------------------------------------------------------------------------
+namespace {
+constexpr int kAttrDevices = 64;
+std::mutex g_attr_mu;
+int g_sms[kAttrDevices] = {};
+int g_smem_optin[kAttrDevices] = {};
+const void *g_smem_done[kAttrDevices][16] = {};
+}  // namespace
+
+int device_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kAttrDevices) return 1;
+  std::lock_guard<std::mutex> lock(g_attr_mu);
+  if (!g_sms[dev]) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms <= 0)
+      return 1;
+    g_sms[dev] = sms;
+  }
+  return g_sms[dev];
+}
+
+cudaError_t allow_dynamic_smem(const void *kernel) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kAttrDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_attr_mu);
+  int slot = 0;
+  for (; slot < 16 && g_smem_done[dev][slot]; ++slot)
+    if (g_smem_done[dev][slot] == kernel) return cudaSuccess;
+  if (!g_smem_optin[dev]) {
+    int v = 0;
+    if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
+        cudaSuccess)
+      return e;
+    g_smem_optin[dev] = v;
+  }
+  // dynamic + the kernel's static shared memory may not exceed the opt-in limit
+  cudaFuncAttributes fa;
+  if ((e = cudaFuncGetAttributes(&fa, kernel)) != cudaSuccess) return e;
+  const int dyn = g_smem_optin[dev] - int(fa.sharedSizeBytes);
+  if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn)) !=
+      cudaSuccess)
+    return e;
+  if (slot < 16) g_smem_done[dev][slot] = kernel;
+  return cudaSuccess;
 }
 
 }  // namespace corr
