@@ -108,9 +108,9 @@ int corr_xcorr_f32(const float *left, int nl, const float *right, int nr,
  * process exits.
  *
  *   * Shapes whose partial sums need more than that return
- *     CORR_EUNSUPPORTED before anything is launched.  Only matrices of 64 or
- *     more rows on the large-matrix kernel use scratch: one 256x256 pair
- *     needs 4 MiB, so up to four such pairs fit and five are rejected.
+ *     CORR_EUNSUPPORTED before anything is launched.  Only matrices of more
+ *     than 128 rows on the large-matrix kernel use scratch: one 256x256 pair
+ *     needs 2 MiB, so up to eight such pairs fit and nine are rejected.
  *   * The first call on a device that needs scratch looks the array's device
  *     address up on that device; make that first call before any stream
  *     capture begins on it.

@@ -38,18 +38,22 @@
 #include <stdint.h>
 
 #include <mutex>
+#include <utility>
 
 #include "internal.cuh"
 
 namespace corr {
 namespace {
 
-constexpr int kP = 8;                // neighbouring shifts dx per lane
-constexpr int kQ = 4;                // neighbouring shifts dy per lane
-constexpr int kRing = kP + 4;        // ring of R values (multiple of 4)
-constexpr int kPadL = kP;            // zero columns left of a staged row
+constexpr int kP = 8;                // pair / bcast kernels: shifts dx per lane
+constexpr int kQ = 4;                // pair kernel: shifts dy per lane
+constexpr int kPadL = kP;            // pair / bcast kernels: zero columns left of a row
 constexpr int kWarps = 8;            // rows / pair kernels
 constexpr int kThreads = 32 * kWarps;
+
+// rows kernel: shifts dx and dy per lane.
+constexpr int kRowsP = kP;
+constexpr int kRowsQ = kQ;
 
 // k-th block in order of distance from the middle of n blocks (costly
 // central blocks first).
@@ -60,11 +64,10 @@ __device__ __forceinline__ int centered(int k, int n) {
 }
 
 // ---------------------------------------------------------------------------
-// Per-lane ring walk over x blocks [b0, b1) of one overlap row.
-//   l4:    float4 index of L[xlo] in shared memory
-//   r4[q]: float4 index of R_q[u0] (u0 = xlo - dx0) in shared memory
-// Block b covers x = xlo + 4b .. xlo + 4b + 3.  R_q[u0 + j] lives at ring
-// position (j - 4 b0) mod 12.
+// Per-lane ring walk.  A lane owns P neighbouring shifts dx0 .. dx0+P-1 for
+// NQ right rows; for each 4-wide x block it loads one float4 of L and one
+// float4 of each right row into a register ring of P + 4 entries, so that
+// R[x - dx0 - p] for every shift p sits at a compile-time ring position.
 // ---------------------------------------------------------------------------
 extern __shared__ float4 g_smem4[];
 
@@ -80,14 +83,22 @@ __device__ __forceinline__ float4 lds128(uint32_t addr) {
   return v;
 }
 
+template <int P>
+struct RingGeom {
+  static constexpr int kSize = P + 4;                  // ring entries per row
+  static constexpr int kCycle = kSize / 4;             // blocks per ring turn
+  static constexpr int kRound = kCycle >= 4 ? kCycle : 2 * kCycle;   // unrolled blocks
+  static_assert(P % 4 == 0, "ring of whole float4 blocks");
+};
+
 // Block J of a round: one float4 of L at la + 16 J, for each of the NQ rows a
-// float4 of R_q at ra[q] + 16 J into ring positions 4 (J mod 3) .. +3; shift
-// p at step s reads position (4 (J mod 3) + s - p) mod 12.
-template <int J, int NQ>
-__device__ __forceinline__ void ring_block(float (&acc)[NQ][kP],
-                                           float (&ring)[NQ][kRing], uint32_t la,
+// float4 of R_q at ra[q] + 16 J into ring positions 4 (J mod cycle) .. +3;
+// shift p at step s reads position (4 (J mod cycle) + s - p) mod (P + 4).
+template <int P, int J, int NQ>
+__device__ __forceinline__ void ring_block(float (&acc)[NQ][P],
+                                           float (&ring)[NQ][P + 4], uint32_t la,
                                            const uint32_t (&ra)[NQ]) {
-  constexpr int JR = J % 3;
+  constexpr int RS = RingGeom<P>::kSize, JR = J % RingGeom<P>::kCycle;
   const float4 lv4 = lds128<16 * J>(la);
 #pragma unroll
   for (int q = 0; q < NQ; ++q) {
@@ -101,85 +112,107 @@ __device__ __forceinline__ void ring_block(float (&acc)[NQ][kP],
 #pragma unroll
   for (int s = 0; s < 4; ++s)
 #pragma unroll
-    for (int p = 0; p < kP; ++p)
+    for (int p = 0; p < P; ++p)
 #pragma unroll
       for (int q = 0; q < NQ; ++q)
-        acc[q][p] = fmaf(lv[s], ring[q][(4 * JR + s - p + 2 * kRing) % kRing], acc[q][p]);
+        acc[q][p] = fmaf(lv[s], ring[q][(4 * JR + s - p + 2 * RS) % RS], acc[q][p]);
+}
+
+template <int P, int NQ, int... Js>
+__device__ __forceinline__ void ring_round(float (&acc)[NQ][P], float (&ring)[NQ][P + 4],
+                                           uint32_t la, const uint32_t (&ra)[NQ],
+                                           std::integer_sequence<int, Js...>) {
+  (ring_block<P, Js, NQ>(acc, ring, la, ra), ...);
+}
+
+// The first rem (< one round) blocks of a round.
+template <int P, int NQ, int... Js>
+__device__ __forceinline__ void ring_tail(float (&acc)[NQ][P], float (&ring)[NQ][P + 4],
+                                          uint32_t la, const uint32_t (&ra)[NQ], int rem,
+                                          std::integer_sequence<int, Js...>) {
+  ((rem > Js ? ring_block<P, Js, NQ>(acc, ring, la, ra) : (void)0), ...);
+}
+
+// R_q[u0 + 4 b0 - P .. u0 + 4 b0 - 1] -> ring positions 4 .. P + 3.
+template <int P, int NQ, int K>
+__device__ __forceinline__ void ring_load(float (&ring)[NQ][P + 4], const uint32_t (&ra)[NQ]) {
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) {
+    const float4 v = lds128<-16 * (P / 4 - K)>(ra[q]);
+    ring[q][4 + 4 * K + 0] = v.x;
+    ring[q][4 + 4 * K + 1] = v.y;
+    ring[q][4 + 4 * K + 2] = v.z;
+    ring[q][4 + 4 * K + 3] = v.w;
+  }
+}
+template <int P, int NQ, int... Ks>
+__device__ __forceinline__ void ring_preload(float (&ring)[NQ][P + 4],
+                                             const uint32_t (&ra)[NQ],
+                                             std::integer_sequence<int, Ks...>) {
+  (ring_load<P, NQ, Ks>(ring, ra), ...);
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) ring[q][0] = ring[q][1] = ring[q][2] = ring[q][3] = 0.f;
 }
 
 // Per-lane ring walk over x blocks [b0, b1) of one overlap row.
 //   l4:    float4 index of L[xlo] in shared memory
-//   r4[q]: float4 index of R_q[u0] (u0 = xlo - dx0) in shared memory
+//   r4[q]: float4 index of R_q[u0] (u0 = xlo - dx0) in shared memory; at
+//          least P zero (or real) values precede it
 // Block b covers x = xlo + 4b .. xlo + 4b + 3.  R_q[u0 + j] lives at ring
-// position (j - 4 b0) mod 12.
-template <int NQ>
-__device__ __forceinline__ void lane_blocks(float (&acc)[NQ][kP], int l4,
+// position (j - 4 b0) mod (P + 4).
+template <int P, int NQ>
+__device__ __forceinline__ void lane_blocks(float (&acc)[NQ][P], int l4,
                                             const int (&r4)[NQ], int b0, int b1) {
-  static_assert(kP == 8 && kRing == 12, "ring preload assumes P = 8");
+  using G = RingGeom<P>;
   if (b0 >= b1) return;
   const uint32_t base = uint32_t(__cvta_generic_to_shared(g_smem4));
-  float ring[NQ][kRing];
+  float ring[NQ][G::kSize];
   uint32_t ra[NQ];
 #pragma unroll
-  for (int q = 0; q < NQ; ++q) {
-    // R[u0 + 4 b0 - 8 .. u0 + 4 b0 - 1] -> positions 4..11
-    ra[q] = base + 16u * uint32_t(r4[q] + b0);
-    const float4 a = lds128<-32>(ra[q]);
-    const float4 b = lds128<-16>(ra[q]);
-    ring[q][4] = a.x; ring[q][5] = a.y; ring[q][6] = a.z; ring[q][7] = a.w;
-    ring[q][8] = b.x; ring[q][9] = b.y; ring[q][10] = b.z; ring[q][11] = b.w;
-    ring[q][0] = ring[q][1] = ring[q][2] = ring[q][3] = 0.f;
-  }
+  for (int q = 0; q < NQ; ++q) ra[q] = base + 16u * uint32_t(r4[q] + b0);
+  ring_preload<P, NQ>(ring, ra, std::make_integer_sequence<int, P / 4>{});
   uint32_t la = base + 16u * uint32_t(l4 + b0);
   int b = b0;
-  for (; b + 6 <= b1; b += 6) {
-    ring_block<0, NQ>(acc, ring, la, ra);
-    ring_block<1, NQ>(acc, ring, la, ra);
-    ring_block<2, NQ>(acc, ring, la, ra);
-    ring_block<3, NQ>(acc, ring, la, ra);
-    ring_block<4, NQ>(acc, ring, la, ra);
-    ring_block<5, NQ>(acc, ring, la, ra);
-    la += 96;
+  for (; b + G::kRound <= b1; b += G::kRound) {
+    ring_round<P, NQ>(acc, ring, la, ra, std::make_integer_sequence<int, G::kRound>{});
+    la += 16 * G::kRound;
 #pragma unroll
-    for (int q = 0; q < NQ; ++q) ra[q] += 96;
+    for (int q = 0; q < NQ; ++q) ra[q] += 16 * G::kRound;
   }
-  // 0..5 remaining blocks, positions continue (J mod 3)
-  const int rem = b1 - b;
-  if (rem > 0) ring_block<0, NQ>(acc, ring, la, ra);
-  if (rem > 1) ring_block<1, NQ>(acc, ring, la, ra);
-  if (rem > 2) ring_block<2, NQ>(acc, ring, la, ra);
-  if (rem > 3) ring_block<3, NQ>(acc, ring, la, ra);
-  if (rem > 4) ring_block<4, NQ>(acc, ring, la, ra);
+  // 0 .. kRound-1 remaining blocks; ring positions continue (J mod cycle)
+  ring_tail<P, NQ>(acc, ring, la, ra, b1 - b,
+                   std::make_integer_sequence<int, G::kRound - 1>{});
 }
 
-// Geometry of one output block of a warp: shifts dy0..dy0+3 x dx0..dx0+7.
+// Geometry of one output block of a warp: shifts dy0..dy0+Q-1 x
+// dx0..dx0+P-1.
 struct Block {
   int dy0, dx0;
-  int ylo, yhi;   // union of the overlap rows of the 4 shifts dy
+  int ylo, yhi;   // union of the overlap rows of the Q shifts dy
   int xlo, nb;    // first x (multiple of 4) and number of 4-wide x blocks
 };
 
+template <int P, int Q>
 __device__ __forceinline__ Block make_block(int H, int W, int dy0, int dx0) {
   Block k;
   k.dy0 = dy0;
   k.dx0 = dx0;
   k.ylo = max(0, dy0);
-  k.yhi = min(H, H + dy0 + kQ - 1);
+  k.yhi = min(H, H + dy0 + Q - 1);
   k.xlo = max(0, dx0);
-  const int xhi = min(W, W + dx0 + kP - 1);
+  const int xhi = min(W, W + dx0 + P - 1);
   k.nb = xhi > k.xlo ? (xhi - k.xlo + 3) >> 2 : 0;
   return k;
 }
 
-// One pass of up to 32 overlap rows [y, y + n) of a block over the lanes of a
-// warp.  lrow(y) / rrow(yr) give the float index of column 0 of a staged L
-// row / R row (before the kPadL zero columns).  With n == 32 lane ph takes
-// row y + ph; with fewer rows each row is split into k = 32 / n x sub-ranges
-// (lanes past n*k idle).
-template <int NPH, typename LRow, typename RRow>
-__device__ __forceinline__ void warp_pass(float (&acc)[kQ][kP], const Block &k,
-                                          int y, int n, int ph, LRow lrow,
-                                          RRow rrow) {
+// One pass of up to NPH overlap rows [y, y + n) of a block over NPH lanes.
+// lrow(y) / rrow(yr) give the float index of column 0 of a staged L row / R
+// row (after its P zero columns).  With n >= NPH lane ph takes row y + ph;
+// with fewer rows each row is split into k = NPH / n x sub-ranges (lanes
+// past n*k idle).
+template <int P, int Q, int NPH, typename LRow, typename RRow>
+__device__ __forceinline__ void warp_pass(float (&acc)[Q][P], const Block &k, int y, int n,
+                                          int ph, LRow lrow, RRow rrow) {
   if (n <= 0 || k.nb == 0) return;
   int row, b0, b1;
   if (n >= NPH) {
@@ -195,25 +228,26 @@ __device__ __forceinline__ void warp_pass(float (&acc)[kQ][kP], const Block &k,
     b1 = (part + 1) * k.nb / parts;
   }
   const int u0 = k.xlo - k.dx0;
-  const int l4 = (lrow(row) + kPadL + k.xlo) >> 2;
-  int r4[kQ];
+  const int l4 = (lrow(row) + k.xlo) >> 2;
+  int r4[Q];
 #pragma unroll
-  for (int q = 0; q < kQ; ++q) r4[q] = (rrow(row - k.dy0 - q) + kPadL + u0) >> 2;
-  lane_blocks<kQ>(acc, l4, r4, b0, b1);
+  for (int q = 0; q < Q; ++q) r4[q] = (rrow(row - k.dy0 - q) + u0) >> 2;
+  lane_blocks<P, Q>(acc, l4, r4, b0, b1);
 }
 
 // Reduce-scatter over groups of NPH lanes (lanes of a group differ in their
 // low log2(NPH) bits): after log2(NPH) steps of halving, lane ph of a group
 // holds the group's full sums of outputs (32/NPH) * ph + i, i < 32/NPH, in
-// v[i].  Clears the accumulators.
-template <int NPH>
-__device__ __forceinline__ void reduce_scatter_group(float (&acc)[kQ][kP], int lane,
+// out[i] (output index q * P + p).  Clears the accumulators.
+template <int P, int Q, int NPH>
+__device__ __forceinline__ void reduce_scatter_group(float (&acc)[Q][P], int lane,
                                                      float (&out)[32 / NPH]) {
+  static_assert(P * Q == 32, "32 outputs per block");
   float v[32];
 #pragma unroll
-  for (int q = 0; q < kQ; ++q)
+  for (int q = 0; q < Q; ++q)
 #pragma unroll
-    for (int p = 0; p < kP; ++p) v[q * kP + p] = acc[q][p];
+    for (int p = 0; p < P; ++p) v[q * P + p] = acc[q][p];
 #pragma unroll
   for (int o = NPH / 2, m = 16; o >= 1; o >>= 1, m >>= 1) {
     const bool upper = (lane & o) != 0;   // keep v[m..2m) if set, else v[0..m)
@@ -227,44 +261,28 @@ __device__ __forceinline__ void reduce_scatter_group(float (&acc)[kQ][kP], int l
 #pragma unroll
   for (int i = 0; i < 32 / NPH; ++i) out[i] = v[i];
 #pragma unroll
-  for (int q = 0; q < kQ; ++q)
+  for (int q = 0; q < Q; ++q)
 #pragma unroll
-    for (int p = 0; p < kP; ++p) acc[q][p] = 0.f;
+    for (int p = 0; p < P; ++p) acc[q][p] = 0.f;
 }
 
 // Reduce-scatter over the 32 lanes: at each step a lane keeps one half of
 // its remaining partial sums and adds the partner's copy of that half, so
 // after 16 + 8 + 4 + 2 + 1 shuffles lane i holds the full sum of output
-// i = q * 8 + p.  Returns it and clears the accumulators.
-__device__ __forceinline__ float reduce_scatter(float (&acc)[kQ][kP], int lane) {
-  float v[32];
-#pragma unroll
-  for (int q = 0; q < kQ; ++q)
-#pragma unroll
-    for (int p = 0; p < kP; ++p) v[q * kP + p] = acc[q][p];
-#pragma unroll
-  for (int n = 16; n >= 1; n >>= 1) {
-    const bool upper = (lane & n) != 0;   // keep v[n..2n) if set, else v[0..n)
-#pragma unroll
-    for (int i = 0; i < n; ++i) {
-      const float send = upper ? v[i] : v[i + n];
-      const float keep = upper ? v[i + n] : v[i];
-      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, n);
-    }
-  }
-#pragma unroll
-  for (int q = 0; q < kQ; ++q)
-#pragma unroll
-    for (int p = 0; p < kP; ++p) acc[q][p] = 0.f;
+// i = q * P + p.  Returns it and clears the accumulators.
+template <int P, int Q>
+__device__ __forceinline__ float reduce_scatter(float (&acc)[Q][P], int lane) {
+  float v[1];
+  reduce_scatter_group<P, Q, 32>(acc, lane, v);
   return v[0];
 }
 
 // Reduce and store the block's outputs into out_pair ([2H-1][2W-1]).
-__device__ __forceinline__ void reduce_store(float (&acc)[kQ][kP], const Block &k,
-                                             int lane, int H, int W,
-                                             float *out_pair) {
-  const float v = reduce_scatter(acc, lane);
-  const int dy = k.dy0 + (lane >> 3), dx = k.dx0 + (lane & 7);
+template <int P, int Q>
+__device__ __forceinline__ void reduce_store(float (&acc)[Q][P], const Block &k, int lane,
+                                             int H, int W, float *out_pair) {
+  const float v = reduce_scatter<P, Q>(acc, lane);
+  const int dy = k.dy0 + lane / P, dx = k.dx0 + lane % P;
   if (dy > -H && dy < H && dx > -W && dx < W)
     out_pair[size_t(dy + H - 1) * (2 * W - 1) + (dx + W - 1)] = v;
 }
@@ -316,20 +334,26 @@ struct XArgs {
 };
 
 // ---------------------------------------------------------------------------
-// rows kernel: one CTA = one pair x 4 dy x 64 dx x one band of kBandRows
-// overlap rows (split-row: the bands of a block are summed afterwards in a
-// fixed order, so results do not depend on scheduling).  The band's rows
-// are staged kChunk at a time into two shared buffers with cp.async, so the
-// next chunk streams in while the current one is consumed (one barrier per
-// chunk).  A chunk of 16 rows is spread over the 32 lanes by splitting each
-// row's x range in two.  With a single band the CTA writes the outputs
+// rows kernel: one CTA = one pair x Q shifts dy x 8 warps' dx groups (P
+// shifts each) x one band of kBandRows overlap rows (split-row: the bands of
+// a block are summed afterwards in a fixed order, so results do not depend
+// on scheduling).  The band's rows are staged CH at a time (CH = 32, or 16
+// for wide rows) into one shared buffer with cp.async; lane i of every warp
+// takes overlap row i of the chunk and walks its group's whole x range, so a
+// walk is long and the per-chunk costs (staging, barrier, walk set-up) are
+// small beside it.  Two CTAs share an SM, so one computes while the other
+// waits for its chunk.  With a single band the CTA writes the outputs
 // directly; otherwise it writes its band's partial sums to
-//   part[((pair * ndyb + dyb) * nbands + band) * kQ + q][8 * group + p].
+//   part[((pair * ndyb + dyb) * nbands + band) * Q + q][P * group + p].
 // ---------------------------------------------------------------------------
-constexpr int kBandRows = 64;
-constexpr int kChunk = 16;
-constexpr int kChunkL = kChunk, kChunkR = kChunk + kQ - 1;
-constexpr int kChunkRows = kChunkL + kChunkR;
+constexpr int kBandRows = 128;
+
+template <int Q, int CH>
+struct ChunkGeom {
+  static_assert(CH == 16 || CH == 32, "a chunk's rows spread evenly over the lanes");
+  static_assert(kBandRows % CH == 0, "bands of whole chunks");
+  static constexpr int kL = CH, kR = CH + Q - 1, kRows = kL + kR;
+};
 
 __device__ __forceinline__ void cp_async(uint32_t dst, const float *src, bool valid,
                                          bool vec4) {
@@ -349,33 +373,37 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_group 0;\n" ::: "memory");
 }
 
-// Issue the copies of one chunk (L rows yc .. yc+kChunkL-1 below y_end, R
-// rows yr_first .. yr_first+kChunkR-1 inside [0, H); other rows zero-fill)
-// into the buffer starting at float `buf`.  One warp per row.
-__device__ __forceinline__ void issue_chunk(uint32_t sbase, int buf, int S, int W,
+// Issue the copies of one chunk (L rows yc .. yc+kL-1 below y_end, R rows
+// yr_first .. yr_first+kR-1 inside [0, H); other rows zero-fill) into the
+// buffer starting at float `buf`, data at column `pad`.  One warp per row.
+template <int Q, int CH>
+__device__ __forceinline__ void issue_chunk(uint32_t sbase, int buf, int S, int pad, int W,
                                             bool vec4, const float *L, const float *R,
                                             int yc, int y_end, int yr_first, int H) {
+  using C = ChunkGeom<Q, CH>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int step = vec4 ? 4 : 1, n = vec4 ? (W >> 2) : W;
-  for (int r = warp; r < kChunkRows; r += kWarps) {
+  for (int r = warp; r < C::kRows; r += kWarps) {
     const float *src;
     bool ok;
-    if (r < kChunkL) {
+    if (r < C::kL) {
       const int y = yc + r;
       ok = y < y_end;
       src = L + (ok ? size_t(y) * W : 0);
     } else {
-      const int yr = yr_first + (r - kChunkL);
+      const int yr = yr_first + (r - C::kL);
       ok = yr >= 0 && yr < H;
       src = R + (ok ? size_t(yr) * W : 0);
     }
-    const uint32_t d = sbase + 4u * uint32_t(buf + r * S + kPadL);
+    const uint32_t d = sbase + 4u * uint32_t(buf + r * S + pad);
     for (int c = lane; c < n; c += 32)
       cp_async(d + 4u * uint32_t(c * step), src + c * step, ok, vec4);
   }
 }
 
+template <int P, int Q, int CH>
 __global__ void __launch_bounds__(kThreads, 2) xcorr_rows_kernel(const XArgs a) {
+  using C = ChunkGeom<Q, CH>;
   float *sm = reinterpret_cast<float *>(g_smem4);
   const uint32_t sbase = uint32_t(__cvta_generic_to_shared(g_smem4));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -393,53 +421,48 @@ __global__ void __launch_bounds__(kThreads, 2) xcorr_rows_kernel(const XArgs a) 
   const float *R = a.right + ri * mat;
 
   const int group = dxs * kWarps + warp;
-  const Block k = make_block(H, W, dyb * kQ - (H - 1), a.dxbase + group * kP);
   const bool active = group < a.ngroups;
+  const int dy0 = dyb * Q - (H - 1);
+  const Block k = make_block<P, Q>(H, W, dy0, a.dxbase + group * P);
+  // every group of the CTA shares dy0, hence the overlap rows
   const int y_begin = max(k.ylo, band * kBandRows);
   const int y_end = min(k.yhi, (band + 1) * kBandRows);
   if (y_begin >= y_end) return;           // CTA-uniform: this band is empty
 
-  const int buf_floats = kChunkRows * S;
-  zero_smem(sm, 2 * buf_floats);          // padding columns stay zero
-  __syncthreads();
-  float acc[kQ][kP];
+  zero_smem(sm, C::kRows * S);            // padding columns stay zero
+  float acc[Q][P];
 #pragma unroll
-  for (int q = 0; q < kQ; ++q)
+  for (int q = 0; q < Q; ++q)
 #pragma unroll
-    for (int p = 0; p < kP; ++p) acc[q][p] = 0.f;
+    for (int p = 0; p < P; ++p) acc[q][p] = 0.f;
 
-  const int nchunks = (y_end - y_begin + kChunk - 1) / kChunk;
-  issue_chunk(sbase, 0, S, W, a.vec4, L, R, y_begin, y_end, y_begin - k.dy0 - (kQ - 1), H);
-  cp_async_commit();
+  const int nchunks = (y_end - y_begin + CH - 1) / CH;
   for (int c = 0; c < nchunks; ++c) {
-    const int yc = y_begin + c * kChunk;
-    const int buf = (c & 1) * buf_floats;
-    cp_async_wait_all();        // this thread's copies of chunk c have landed
-    __syncthreads();            // ... everyone's, and chunk c-1 is consumed
-    if (c + 1 < nchunks) {
-      const int yn = yc + kChunk;
-      issue_chunk(sbase, ((c + 1) & 1) * buf_floats, S, W, a.vec4, L, R, yn, y_end,
-                  yn - k.dy0 - (kQ - 1), H);
-      cp_async_commit();
-    }
-    const int yr_first = yc - k.dy0 - (kQ - 1);
+    const int yc = y_begin + c * CH;
+    const int yr_first = yc - dy0 - (Q - 1);
+    __syncthreads();            // the buffer is free (zeroed, or chunk c-1 consumed)
+    issue_chunk<Q, CH>(sbase, 0, S, P, W, a.vec4, L, R, yc, y_end, yr_first, H);
+    cp_async_commit();
+    cp_async_wait_all();        // this thread's copies have landed
+    __syncthreads();            // ... and everyone's
     if (active)
-      warp_pass<32>(acc, k, yc, min(kChunk, y_end - yc), lane,
-                [&](int y) { return buf + (y - yc) * S; },
-                [&](int yr) { return buf + (kChunkL + yr - yr_first) * S; });
+      warp_pass<P, Q, 32>(acc, k, yc, min(CH, y_end - yc), lane,
+                          [&](int y) { return (y - yc) * S + P; },
+                          [&](int yr) { return (C::kL + yr - yr_first) * S + P; });
   }
   if (!active) return;
   if (a.nbands == 1) {
-    reduce_store(acc, k, lane, H, W, a.out + size_t(pair) * (2 * H - 1) * (2 * W - 1));
+    reduce_store<P, Q>(acc, k, lane, H, W, a.out + size_t(pair) * (2 * H - 1) * (2 * W - 1));
   } else {
-    const float v = reduce_scatter(acc, lane);
+    const float v = reduce_scatter<P, Q>(acc, lane);
     const size_t slot = (size_t(pair) * a.ndyb + dyb) * a.nbands + band;
-    a.part[(slot * kQ + (lane >> 3)) * a.part_row + group * kP + (lane & 7)] = v;
+    a.part[(slot * Q + lane / P) * a.part_row + group * P + lane % P] = v;
   }
 }
 
 // Second pass of the rows kernel: out = sum over the non-empty bands of the
 // partial sums, in band order.
+template <int Q>
 __global__ void xcorr_band_sum_kernel(const XArgs a) {
   const int H = a.H, W = a.W, oh = 2 * H - 1, ow = 2 * W - 1;
   const long long total = (long long)a.nl * a.nr * oh * ow;
@@ -449,15 +472,15 @@ __global__ void xcorr_band_sum_kernel(const XArgs a) {
     const long long t = i / ow;
     const int oy = int(t % oh);
     const int pair = int(t / oh);
-    const int dyb = oy / kQ, q = oy - dyb * kQ;
-    const int dy0 = dyb * kQ - (H - 1);
-    const int ylo = max(0, dy0), yhi = min(H, H + dy0 + kQ - 1);
+    const int dyb = oy / Q, q = oy - dyb * Q;
+    const int dy0 = dyb * Q - (H - 1);
+    const int ylo = max(0, dy0), yhi = min(H, H + dy0 + Q - 1);
     const int col = (ox - (W - 1)) - a.dxbase;
     const size_t slot0 = (size_t(pair) * a.ndyb + dyb) * a.nbands;
     float sum = 0.f;
     for (int b = 0; b < a.nbands; ++b) {
       if (max(ylo, b * kBandRows) >= min(yhi, (b + 1) * kBandRows)) continue;
-      sum += a.part[((slot0 + b) * kQ + q) * a.part_row + col];
+      sum += a.part[((slot0 + b) * Q + q) * a.part_row + col];
     }
     a.out[i] = sum;
   }
@@ -523,14 +546,14 @@ __global__ void __launch_bounds__(kThreads, 2) xcorr_pair_kernel(const XArgs a) 
     const int it = part + u * a.parts;                      // centre-first rank
     const int dyb = centered(it % a.ndyb, a.ndyb);
     const int g = centered(it / a.ndyb, a.ngroups);
-    const Block k = make_block(H, W, dyb * kQ - (H - 1), a.dxbase + g * kP);
+    const Block k = make_block<kP, kQ>(H, W, dyb * kQ - (H - 1), a.dxbase + g * kP);
     if (pair_ok)
       for (int y = k.ylo; y < k.yhi; y += NPH)
-        warp_pass<NPH>(acc, k, y, min(NPH, k.yhi - y), ph,
-                       [&](int yy) { return base + yy * S; },
-                       [&](int yr) { return base + (H + kPadY + yr) * S; });
+        warp_pass<kP, kQ, NPH>(acc, k, y, min(NPH, k.yhi - y), ph,
+                               [&](int yy) { return base + yy * S + kPadL; },
+                               [&](int yr) { return base + (H + kPadY + yr) * S + kPadL; });
     float v[32 / NPH];
-    reduce_scatter_group<NPH>(acc, lane, v);
+    reduce_scatter_group<kP, kQ, NPH>(acc, lane, v);
 #pragma unroll
     for (int i = 0; i < 32 / NPH; ++i) {
       const int idx = (32 / NPH) * ph + i;
@@ -684,13 +707,13 @@ __global__ void __launch_bounds__(32 * kBWarps, 1) xcorr_bcast_kernel(const XArg
         int r4[kBRights];
 #pragma unroll
         for (int j = 0; j < kBRights; ++j) r4[j] = (rrow + 32 * j * slab + xa.u0) >> 2;
-        lane_blocks<kBRights>(accA, (lrow + xa.xlo) >> 2, r4, 0, xa.nb);
+        lane_blocks<kP, kBRights>(accA, (lrow + xa.xlo) >> 2, r4, 0, xa.nb);
       }
       if (has_b) {
         int r4[kBRights];
 #pragma unroll
         for (int j = 0; j < kBRights; ++j) r4[j] = (rrow + 32 * j * slab + xb.u0) >> 2;
-        lane_blocks<kBRights>(accB, (lrow + xb.xlo) >> 2, r4, 0, xb.nb);
+        lane_blocks<kP, kBRights>(accB, (lrow + xb.xlo) >> 2, r4, 0, xb.nb);
       }
     }
   }
@@ -1087,6 +1110,7 @@ struct XPlan {
   long long blocks;      // grid of the pair / rows kernel
   size_t part_bytes;     // rows kernel with several bands: scratch bytes
   int nslot;             // pair kernel: pairs staged per CTA
+  int chunk;             // rows kernel: rows per staged chunk (32 or 16)
 };
 
 XPlan make_plan(const float *left, int nl, const float *right, int nr, int H, int W,
@@ -1096,6 +1120,7 @@ XPlan make_plan(const float *left, int nl, const float *right, int nr, int H, in
   pl.blocks = 0;
   pl.part_bytes = 0;
   pl.nslot = 1;
+  pl.chunk = 32;
   const long long pairs = (long long)nl * nr;
   XArgs &a = pl.a;
   a.left = left;
@@ -1160,9 +1185,23 @@ XPlan make_plan(const float *left, int nl, const float *right, int nr, int H, in
       return pl;
     }
   }
-  const size_t rows_smem = size_t(2 * kChunkRows) * a.S * sizeof(float);
+  // rows kernel: its own shifts per lane (kRowsP x kRowsQ) and row padding
+  {
+    const int need = kRowsP + ((W + 3) & ~3) + kRowsP + 8;
+    a.S = ((need + 7) & ~7) + 4;
+    a.ngroups = ((W - 1) - a.dxbase) / kRowsP + 1;
+    a.ndyb = (2 * H - 1 + kRowsQ - 1) / kRowsQ;
+    a.nsuper = (a.ngroups + kWarps - 1) / kWarps;
+  }
+  // 32-row chunks where they fit two CTAs per SM, else 16-row chunks
+  size_t rows_smem = size_t(ChunkGeom<kRowsQ, 32>::kRows) * a.S * sizeof(float);
+  pl.chunk = 32;
+  if (rows_smem > kMaxStageSmem) {
+    rows_smem = size_t(ChunkGeom<kRowsQ, 16>::kRows) * a.S * sizeof(float);
+    pl.chunk = 16;
+  }
   a.nbands = (H + kBandRows - 1) / kBandRows;
-  a.part_row = kP * a.ngroups;
+  a.part_row = kRowsP * a.ngroups;
   const long long blocks = pairs * a.ndyb * a.nsuper * a.nbands;
   if (rows_smem > kMaxStageSmem || blocks > 0x7fffffffLL || H < 24) {
     pl.kind = XKind::Direct;
@@ -1172,7 +1211,7 @@ XPlan make_plan(const float *left, int nl, const float *right, int nr, int H, in
   pl.smem = rows_smem;
   pl.blocks = blocks;
   if (a.nbands > 1)
-    pl.part_bytes = size_t(pairs) * a.ndyb * a.nbands * kQ * a.part_row * sizeof(float);
+    pl.part_bytes = size_t(pairs) * a.ndyb * a.nbands * kRowsQ * a.part_row * sizeof(float);
   return pl;
 }
 
@@ -1197,18 +1236,20 @@ cudaError_t run_plan(XPlan &pl, float *fixed, cudaStream_t stream) {
     kern<<<unsigned(pl.blocks), kThreads, pl.smem, stream>>>(a);
     return cudaGetLastError();
   }
-  cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void *>(xcorr_rows_kernel));
+  auto rows_kernel = pl.chunk == 32 ? xcorr_rows_kernel<kRowsP, kRowsQ, 32>
+                                    : xcorr_rows_kernel<kRowsP, kRowsQ, 16>;
+  cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void *>(rows_kernel));
   if (e != cudaSuccess) return e;
   const bool banded = a.nbands > 1;
   const bool pooled = banded && fixed == nullptr;
   a.part = banded ? fixed : nullptr;
   if (pooled && (e = scratch_alloc(&a.part, pl.part_bytes, stream)) != cudaSuccess) return e;
-  xcorr_rows_kernel<<<unsigned(pl.blocks), kThreads, pl.smem, stream>>>(a);
+  rows_kernel<<<unsigned(pl.blocks), kThreads, pl.smem, stream>>>(a);
   e = cudaGetLastError();
   if (banded && e == cudaSuccess) {
     const long long outs = (long long)a.nl * a.nr * (2LL * a.H - 1) * (2LL * a.W - 1);
     const long long sum_blocks = (outs + 255) / 256;
-    xcorr_band_sum_kernel<<<unsigned(sum_blocks < 65535 * 16 ? sum_blocks : 65535 * 16), 256, 0,
+    xcorr_band_sum_kernel<kRowsQ><<<unsigned(sum_blocks < 65535 * 16 ? sum_blocks : 65535 * 16), 256, 0,
                             stream>>>(a);
     e = cudaGetLastError();
   }

@@ -67,10 +67,12 @@ def test_fixture(path):
     (2, 3, 50, 8), (33, 3, 5, 5), (1, 1, 1, 300), (1, 1, 300, 1),
     # rights in lanes: ragged right block, W % 4 != 0, short H, several lefts
     (2, 40, 20, 12), (1, 33, 30, 10), (3, 64, 9, 40), (1, 96, 33, 8),
-    # row-band split (three bands, W % 4 != 0, two pairs)
+    # row kernel, 32-row chunks: two row bands, a ragged last chunk, W % 4 != 0
     (1, 2, 130, 257), (2, 1, 200, 64),
-    # too wide to stage: the bounds-checked fallback kernel
-    (1, 1, 5, 400), (2, 2, 3, 700), (1, 6, 4, 520),
+    # row kernel, 16-row chunks (rows too wide for 32): one and two bands
+    (1, 1, 40, 520), (1, 1, 140, 420),
+    # too short or too wide to stage: the bounds-checked fallback kernel
+    (1, 1, 5, 400), (2, 2, 3, 700), (1, 6, 4, 520), (1, 1, 24, 800),
 ])
 def test_shapes(nl, nr, H, W):
     check(rand(nl, H, W), rand(nr, H, W, "normal"))
