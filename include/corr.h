@@ -108,9 +108,12 @@ int corr_xcorr_f32(const float *left, int nl, const float *right, int nr,
  * process exits.
  *
  *   * Shapes whose partial sums need more than that return
- *     CORR_EUNSUPPORTED before anything is launched.  Only matrices of more
- *     than 128 rows on the large-matrix kernel use scratch: one 256x256 pair
- *     needs 2 MiB, so up to eight such pairs fit and nine are rejected.
+ *     CORR_EUNSUPPORTED before anything is launched.  Only the large-matrix
+ *     kernels use scratch, when they split the overlap rows into bands
+ *     (more than 128 rows in a small batch: one 256x256 pair needs 2 MiB)
+ *     or the rows into x segments (rows wider than about 770 floats: about
+ *     48 bytes per matrix element, so one 1024x1024 pair needs 48 MiB and
+ *     is rejected).
  *   * The first call on a device that needs scratch looks the array's device
  *     address up on that device; make that first call before any stream
  *     capture begins on it.

@@ -326,45 +326,62 @@ struct XArgs {
   int nsuper;     // rows kernel: ceil(ngroups / kWarps)
   int parts;      // pair kernel: CTAs per pair
   int vec4;       // rows can be read as float4
-  int nbands;     // rows kernel: row bands of kBandRows (split-row)
-  int part_row;   // rows kernel: floats per partial-sum row (8 * ngroups)
-  float *part;    // rows kernel: band partial sums (nbands > 1)
+  int nbands;     // rows kernel: row bands (split-row)
+  int band_rows;  // rows kernel: overlap rows per band
+  int nxseg;      // rows kernel: x segments (split-row along x)
+  int xseg;       // rows kernel: columns per x segment (multiple of 4)
+  int SL, SR;     // rows kernel: shared L / R row strides in floats (% 8 == 4)
+  int part_row;   // rows kernel: floats per partial-sum row (P * ngroups)
+  float *part;    // rows kernel: partial sums (nbands * nxseg > 1)
   int nrblk;      // bcast kernel: blocks of 32 rights
   int npairblk;   // bcast kernel: blocks of kWarps dx-group pairs
 };
 
 // ---------------------------------------------------------------------------
 // rows kernel: one CTA = one pair x Q shifts dy x 8 warps' dx groups (P
-// shifts each) x one band of kBandRows overlap rows (split-row: the bands of
-// a block are summed afterwards in a fixed order, so results do not depend
-// on scheduling).  The band's rows are staged CH at a time (CH = 32, or 16
-// for wide rows) into one shared buffer with cp.async; lane i of every warp
-// takes overlap row i of the chunk and walks its group's whole x range, so a
-// walk is long and the per-chunk costs (staging, barrier, walk set-up) are
-// small beside it.  Two CTAs share an SM, so one computes while the other
-// waits for its chunk.  With a single band the CTA writes the outputs
-// directly; otherwise it writes its band's partial sums to
-//   part[((pair * ndyb + dyb) * nbands + band) * Q + q][P * group + p].
+// shifts each) x one band of overlap rows x one segment of x (split-row in
+// both directions: the partial sums of a block are added afterwards in a
+// fixed order, so results do not depend on scheduling).
+//
+// The CTA's groups cover shifts DX0 .. DX0 + 8P - 1; the L columns any of
+// them touches inside the segment form the window [xa, xb), and the R
+// columns they pair with form [xa - DX0 - 8P, xb - DX0 + 4).  Only these
+// windows are staged, 32 overlap rows at a time, with cp.async into one
+// shared buffer (columns outside the matrix, or past the segment for L,
+// arrive as zeros, so the inner loop has no bounds tests).  Lane i of every
+// warp takes overlap row i of the chunk and walks its group's whole x range
+// inside the window, so a walk is long beside the per-chunk costs (staging,
+// barrier, walk set-up).  Two CTAs share an SM, so one computes while the
+// other waits for its chunk.  With one band and one segment the CTA writes
+// the outputs directly; otherwise it writes its partial sums to
+//   part[(slot * Q + q) * part_row + P * group + p],
+//   slot = ((pair * ndyb + dyb) * nbands + band) * nxseg + xseg.
 // ---------------------------------------------------------------------------
-constexpr int kBandRows = 128;
+constexpr int kChunk = 32;
+constexpr int kBandRows = 128;       // band height when bands are needed
 
-template <int Q, int CH>
+template <int Q, int CH = kChunk>
 struct ChunkGeom {
   static_assert(CH == 16 || CH == 32, "a chunk's rows spread evenly over the lanes");
-  static_assert(kBandRows % CH == 0, "bands of whole chunks");
   static constexpr int kL = CH, kR = CH + Q - 1, kRows = kL + kR;
 };
 
+__device__ __forceinline__ void cp_async16(uint32_t dst, const float *src, int bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const float *src, bool valid) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src),
+               "r"(valid ? 4 : 0)
+               : "memory");
+}
 __device__ __forceinline__ void cp_async(uint32_t dst, const float *src, bool valid,
                                          bool vec4) {
   if (vec4)
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
-                 "r"(valid ? 16 : 0)
-                 : "memory");
+    cp_async16(dst, src, valid ? 16 : 0);
   else
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src),
-                 "r"(valid ? 4 : 0)
-                 : "memory");
+    cp_async4(dst, src, valid);
 }
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;\n" ::: "memory");
@@ -373,13 +390,49 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_group 0;\n" ::: "memory");
 }
 
-// Issue the copies of one chunk (L rows yc .. yc+kL-1 below y_end, R rows
-// yr_first .. yr_first+kR-1 inside [0, H); other rows zero-fill) into the
-// buffer starting at float `buf`, data at column `pad`.  One warp per row.
+// L window [xa, xb) of CTA column dxs in x segment xseg (empty if xa >= xb).
+// xa is a multiple of 4.
+__host__ __device__ inline void rows_window(int W, int dxbase, int P, int dxs, int xseg,
+                                            int seg, int &xa, int &xb) {
+  const int dx_first = dxbase + dxs * kWarps * P;
+  const int dx_last = dx_first + kWarps * P - 1;
+  const int xs0 = xseg * seg, xs1 = min(W, xs0 + seg);
+  xa = max(xs0, max(0, dx_first));
+  xb = min(xs1, W + dx_last);
+}
+
+// Copy one row window of n4 float4 slots starting at column c0 of global row
+// `row` to shared byte address d; columns outside [lo, hi), and every column
+// when !row_ok, arrive as zeros (their copies read nothing; `row` is still a
+// valid address).  One warp.
+__device__ __forceinline__ void stage_window(uint32_t d, const float *row, bool row_ok, int c0,
+                                             int n4, int lo, int hi, bool vec4, int lane) {
+  if (vec4) {
+    // c0, lo and the row start are 16-byte aligned, hi may not be (an L
+    // window ending at W + dx): a slot is whole, partial or empty
+    for (int c = lane; c < n4; c += 32) {
+      const int x = c0 + 4 * c;
+      int bytes = 0;
+      if (row_ok && x >= lo) bytes = 4 * max(0, min(4, hi - x));
+      cp_async16(d + 16u * uint32_t(c), row + (bytes ? x : 0), bytes);
+    }
+  } else {
+    for (int c = lane; c < 4 * n4; c += 32) {
+      const int x = c0 + c;
+      const bool ok = row_ok && x >= lo && x < hi;
+      cp_async4(d + 4u * uint32_t(c), row + (ok ? x : 0), ok);
+    }
+  }
+}
+
+// Full-row variant for rows narrow enough that CH whole rows of L and R fit:
+// rows are staged at column P of a zero-padded shared row of stride S (the
+// padding is zeroed once), and every warp reads the same rows.  No x
+// segments; partial sums (bands only) use the same slots with xseg = 0.
 template <int Q, int CH>
-__device__ __forceinline__ void issue_chunk(uint32_t sbase, int buf, int S, int pad, int W,
-                                            bool vec4, const float *L, const float *R,
-                                            int yc, int y_end, int yr_first, int H) {
+__device__ __forceinline__ void issue_rows(uint32_t sbase, int S, int pad, int W, bool vec4,
+                                           const float *L, const float *R, int yc, int y_end,
+                                           int yr_first, int H) {
   using C = ChunkGeom<Q, CH>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int step = vec4 ? 4 : 1, n = vec4 ? (W >> 2) : W;
@@ -395,7 +448,7 @@ __device__ __forceinline__ void issue_chunk(uint32_t sbase, int buf, int S, int 
       ok = yr >= 0 && yr < H;
       src = R + (ok ? size_t(yr) * W : 0);
     }
-    const uint32_t d = sbase + 4u * uint32_t(buf + r * S + pad);
+    const uint32_t d = sbase + 4u * uint32_t(r * S + pad);
     for (int c = lane; c < n; c += 32)
       cp_async(d + 4u * uint32_t(c * step), src + c * step, ok, vec4);
   }
@@ -425,8 +478,8 @@ __global__ void __launch_bounds__(kThreads, 2) xcorr_rows_kernel(const XArgs a) 
   const int dy0 = dyb * Q - (H - 1);
   const Block k = make_block<P, Q>(H, W, dy0, a.dxbase + group * P);
   // every group of the CTA shares dy0, hence the overlap rows
-  const int y_begin = max(k.ylo, band * kBandRows);
-  const int y_end = min(k.yhi, (band + 1) * kBandRows);
+  const int y_begin = max(k.ylo, band * a.band_rows);
+  const int y_end = min(k.yhi, (band + 1) * a.band_rows);
   if (y_begin >= y_end) return;           // CTA-uniform: this band is empty
 
   zero_smem(sm, C::kRows * S);            // padding columns stay zero
@@ -441,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 2) xcorr_rows_kernel(const XArgs a) 
     const int yc = y_begin + c * CH;
     const int yr_first = yc - dy0 - (Q - 1);
     __syncthreads();            // the buffer is free (zeroed, or chunk c-1 consumed)
-    issue_chunk<Q, CH>(sbase, 0, S, P, W, a.vec4, L, R, yc, y_end, yr_first, H);
+    issue_rows<Q, CH>(sbase, S, P, W, a.vec4, L, R, yc, y_end, yr_first, H);
     cp_async_commit();
     cp_async_wait_all();        // this thread's copies have landed
     __syncthreads();            // ... and everyone's
@@ -460,9 +513,96 @@ __global__ void __launch_bounds__(kThreads, 2) xcorr_rows_kernel(const XArgs a) 
   }
 }
 
-// Second pass of the rows kernel: out = sum over the non-empty bands of the
-// partial sums, in band order.
-template <int Q>
+// Windowed variant (any width).
+template <int P, int Q>
+__global__ void __launch_bounds__(kThreads, 2) xcorr_rows_win_kernel(const XArgs a) {
+  using C = ChunkGeom<Q>;
+  const uint32_t sbase = uint32_t(__cvta_generic_to_shared(g_smem4));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int H = a.H, W = a.W, SL = a.SL, SR = a.SR;
+  int item = blockIdx.x;
+  const int band = item % a.nbands;
+  item /= a.nbands;
+  const int xseg = item % a.nxseg;
+  item /= a.nxseg;
+  const int pair = item % (a.nl * a.nr);
+  item /= a.nl * a.nr;
+  const int dyb = centered(item % a.ndyb, a.ndyb);
+  const int dxs = centered(item / a.ndyb, a.nsuper);
+  const int li = pair / a.nr, ri = pair - li * a.nr;
+  const size_t mat = size_t(H) * W;
+  const float *L = a.left + li * mat;
+  const float *R = a.right + ri * mat;
+
+  const int dy0 = dyb * Q - (H - 1);
+  // every group of the CTA shares dy0, hence the overlap rows
+  const int y_begin = max(max(0, dy0), band * a.band_rows);
+  const int y_end = min(min(H, H + dy0 + Q - 1), (band + 1) * a.band_rows);
+  int xa, xb;
+  rows_window(W, a.dxbase, P, dxs, xseg, a.xseg, xa, xb);
+  if (y_begin >= y_end || xa >= xb) return;   // CTA-uniform: nothing to add here
+
+  const int DX0 = a.dxbase + dxs * kWarps * P;
+  const int nl4 = (xb - xa + 3) >> 2;         // L slots; block reads stay inside
+  const int nr4 = nl4 + 2 * P;                // R slots from ua = xa - DX0 - 8P
+  const int ua = xa - DX0 - kWarps * P;
+  const int r_base = C::kL * SL;              // float index of the first R row
+
+  const int group = dxs * kWarps + warp;
+  const bool active = group < a.ngroups;
+  Block k = make_block<P, Q>(H, W, dy0, a.dxbase + group * P);
+  {
+    // the group's x range clipped to the window
+    const int xhi = min(min(W, W + k.dx0 + P - 1), xb);
+    k.xlo = max(k.xlo, xa);
+    k.nb = xhi > k.xlo ? (xhi - k.xlo + 3) >> 2 : 0;
+  }
+  float acc[Q][P];
+#pragma unroll
+  for (int q = 0; q < Q; ++q)
+#pragma unroll
+    for (int p = 0; p < P; ++p) acc[q][p] = 0.f;
+
+  const bool vec4 = a.vec4;
+  const int nchunks = (y_end - y_begin + kChunk - 1) / kChunk;
+  for (int c = 0; c < nchunks; ++c) {
+    const int yc = y_begin + c * kChunk;
+    const int yr_first = yc - dy0 - (Q - 1);
+    if (c > 0) __syncthreads();     // chunk c-1 is consumed
+    for (int r = warp; r < C::kL + C::kR; r += kWarps) {
+      if (r < C::kL) {
+        const int y = yc + r;
+        const bool ok = y < y_end;
+        stage_window(sbase + 4u * uint32_t(r * SL), L + (ok ? size_t(y) * W : 0), ok, xa, nl4,
+                     xa, xb, vec4, lane);
+      } else {
+        const int yr = yr_first + (r - C::kL);
+        const bool ok = yr >= 0 && yr < H;
+        stage_window(sbase + 4u * uint32_t(r_base + (r - C::kL) * SR),
+                     R + (ok ? size_t(yr) * W : 0), ok, ua, nr4, 0, W, vec4, lane);
+      }
+    }
+    cp_async_commit();
+    cp_async_wait_all();            // this thread's copies have landed
+    __syncthreads();                // ... and everyone's
+    if (active)
+      warp_pass<P, Q, 32>(acc, k, yc, min(kChunk, y_end - yc), lane,
+                          [&](int y) { return (y - yc) * SL - xa; },
+                          [&](int yr) { return r_base + (yr - yr_first) * SR - ua; });
+  }
+  if (!active) return;
+  if (a.nbands * a.nxseg == 1) {
+    reduce_store<P, Q>(acc, k, lane, H, W, a.out + size_t(pair) * (2 * H - 1) * (2 * W - 1));
+  } else {
+    const float v = reduce_scatter<P, Q>(acc, lane);
+    const size_t slot = ((size_t(pair) * a.ndyb + dyb) * a.nbands + band) * a.nxseg + xseg;
+    a.part[(slot * Q + lane / P) * a.part_row + group * P + lane % P] = v;
+  }
+}
+
+// Second pass of the rows kernel: out = sum of the partial sums of the
+// (band, segment) CTAs that ran, in band-then-segment order.
+template <int P, int Q>
 __global__ void xcorr_band_sum_kernel(const XArgs a) {
   const int H = a.H, W = a.W, oh = 2 * H - 1, ow = 2 * W - 1;
   const long long total = (long long)a.nl * a.nr * oh * ow;
@@ -476,11 +616,17 @@ __global__ void xcorr_band_sum_kernel(const XArgs a) {
     const int dy0 = dyb * Q - (H - 1);
     const int ylo = max(0, dy0), yhi = min(H, H + dy0 + Q - 1);
     const int col = (ox - (W - 1)) - a.dxbase;
+    const int dxs = (col / P) / kWarps;
     const size_t slot0 = (size_t(pair) * a.ndyb + dyb) * a.nbands;
     float sum = 0.f;
     for (int b = 0; b < a.nbands; ++b) {
-      if (max(ylo, b * kBandRows) >= min(yhi, (b + 1) * kBandRows)) continue;
-      sum += a.part[((slot0 + b) * Q + q) * a.part_row + col];
+      if (max(ylo, b * a.band_rows) >= min(yhi, (b + 1) * a.band_rows)) continue;
+      for (int s = 0; s < a.nxseg; ++s) {
+        int xa, xb;
+        rows_window(W, a.dxbase, P, dxs, s, a.xseg, xa, xb);
+        if (xa >= xb) continue;
+        sum += a.part[(((slot0 + b) * a.nxseg + s) * Q + q) * a.part_row + col];
+      }
     }
     a.out[i] = sum;
   }
@@ -1110,7 +1256,7 @@ struct XPlan {
   long long blocks;      // grid of the pair / rows kernel
   size_t part_bytes;     // rows kernel with several bands: scratch bytes
   int nslot;             // pair kernel: pairs staged per CTA
-  int chunk;             // rows kernel: rows per staged chunk (32 or 16)
+  int chunk;             // rows kernel: 32 / 16 (whole rows) or 0 (windows)
 };
 
 XPlan make_plan(const float *left, int nl, const float *right, int nr, int H, int W,
@@ -1120,7 +1266,7 @@ XPlan make_plan(const float *left, int nl, const float *right, int nr, int H, in
   pl.blocks = 0;
   pl.part_bytes = 0;
   pl.nslot = 1;
-  pl.chunk = 32;
+  pl.chunk = 0;
   const long long pairs = (long long)nl * nr;
   XArgs &a = pl.a;
   a.left = left;
@@ -1144,6 +1290,10 @@ XPlan make_plan(const float *left, int nl, const float *right, int nr, int H, in
             (reinterpret_cast<uintptr_t>(right) & 15) == 0) ? 1 : 0;
   a.parts = 1;
   a.nbands = 1;
+  a.band_rows = H;
+  a.nxseg = 1;
+  a.xseg = 0;
+  a.SL = a.SR = 0;
   a.part_row = 0;
   a.part = nullptr;
   a.nrblk = 0;
@@ -1185,33 +1335,58 @@ XPlan make_plan(const float *left, int nl, const float *right, int nr, int H, in
       return pl;
     }
   }
-  // rows kernel: its own shifts per lane (kRowsP x kRowsQ) and row padding
+  // rows kernels (shifts per lane kRowsP x kRowsQ): whole zero-padded rows
+  // in 32-row chunks, else 16-row chunks, where a chunk leaves room for two
+  // CTAs per SM; else L / R windows of x segments narrow enough for that
+  a.ngroups = ((W - 1) - a.dxbase) / kRowsP + 1;
+  a.ndyb = (2 * H - 1 + kRowsQ - 1) / kRowsQ;
+  a.nsuper = (a.ngroups + kWarps - 1) / kWarps;
   {
     const int need = kRowsP + ((W + 3) & ~3) + kRowsP + 8;
     a.S = ((need + 7) & ~7) + 4;
-    a.ngroups = ((W - 1) - a.dxbase) / kRowsP + 1;
-    a.ndyb = (2 * H - 1 + kRowsQ - 1) / kRowsQ;
-    a.nsuper = (a.ngroups + kWarps - 1) / kWarps;
   }
-  // 32-row chunks where they fit two CTAs per SM, else 16-row chunks
-  size_t rows_smem = size_t(ChunkGeom<kRowsQ, 32>::kRows) * a.S * sizeof(float);
-  pl.chunk = 32;
-  if (rows_smem > kMaxStageSmem) {
-    rows_smem = size_t(ChunkGeom<kRowsQ, 16>::kRows) * a.S * sizeof(float);
+  a.nxseg = 1;
+  a.xseg = 4 * ((W + 3) / 4);
+  pl.chunk = 0;
+  if ((pl.smem = size_t(ChunkGeom<kRowsQ, 32>::kRows) * a.S * sizeof(float)) <= kMaxStageSmem) {
+    pl.chunk = 32;
+  } else if ((pl.smem = size_t(ChunkGeom<kRowsQ, 16>::kRows) * a.S * sizeof(float)) <=
+             kMaxStageSmem) {
     pl.chunk = 16;
+  } else {
+    auto win_smem = [&](int seg) {
+      const int l = 4 * ((seg + 3) / 4);
+      a.SL = l | 4;                        // stride % 8 == 4: conflict-free
+      a.SR = (l + 8 * kRowsP) | 4;         //   16-byte loads across rows
+      return (size_t(ChunkGeom<kRowsQ>::kL) * a.SL + size_t(ChunkGeom<kRowsQ>::kR) * a.SR) *
+             sizeof(float);
+    };
+    while (win_smem(a.xseg) > kMaxStageSmem && a.xseg > 4) {
+      ++a.nxseg;
+      a.xseg = 4 * (((W + a.nxseg - 1) / a.nxseg + 3) / 4);
+    }
+    pl.smem = win_smem(a.xseg);
   }
-  a.nbands = (H + kBandRows - 1) / kBandRows;
+  // row bands only where the grid would otherwise be short of CTAs
+  const long long unbanded = pairs * a.ndyb * a.nsuper * a.nxseg;
+  if (unbanded >= 16LL * sm_count() || H <= kBandRows) {
+    a.nbands = 1;
+    a.band_rows = H;
+  } else {
+    a.nbands = (H + kBandRows - 1) / kBandRows;
+    a.band_rows = kBandRows;
+  }
   a.part_row = kRowsP * a.ngroups;
-  const long long blocks = pairs * a.ndyb * a.nsuper * a.nbands;
-  if (rows_smem > kMaxStageSmem || blocks > 0x7fffffffLL || H < 24) {
+  const long long blocks = unbanded * a.nbands;
+  if (blocks > 0x7fffffffLL || H < 24) {
     pl.kind = XKind::Direct;
     return pl;
   }
   pl.kind = XKind::Rows;
-  pl.smem = rows_smem;
   pl.blocks = blocks;
-  if (a.nbands > 1)
-    pl.part_bytes = size_t(pairs) * a.ndyb * a.nbands * kRowsQ * a.part_row * sizeof(float);
+  if (a.nbands * a.nxseg > 1)
+    pl.part_bytes = size_t(pairs) * a.ndyb * a.nbands * a.nxseg * kRowsQ * a.part_row *
+                    sizeof(float);
   return pl;
 }
 
@@ -1236,11 +1411,12 @@ cudaError_t run_plan(XPlan &pl, float *fixed, cudaStream_t stream) {
     kern<<<unsigned(pl.blocks), kThreads, pl.smem, stream>>>(a);
     return cudaGetLastError();
   }
-  auto rows_kernel = pl.chunk == 32 ? xcorr_rows_kernel<kRowsP, kRowsQ, 32>
-                                    : xcorr_rows_kernel<kRowsP, kRowsQ, 16>;
+  auto rows_kernel = pl.chunk == 32   ? xcorr_rows_kernel<kRowsP, kRowsQ, 32>
+                     : pl.chunk == 16 ? xcorr_rows_kernel<kRowsP, kRowsQ, 16>
+                                      : xcorr_rows_win_kernel<kRowsP, kRowsQ>;
   cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void *>(rows_kernel));
   if (e != cudaSuccess) return e;
-  const bool banded = a.nbands > 1;
+  const bool banded = a.nbands * a.nxseg > 1;
   const bool pooled = banded && fixed == nullptr;
   a.part = banded ? fixed : nullptr;
   if (pooled && (e = scratch_alloc(&a.part, pl.part_bytes, stream)) != cudaSuccess) return e;
@@ -1249,8 +1425,8 @@ cudaError_t run_plan(XPlan &pl, float *fixed, cudaStream_t stream) {
   if (banded && e == cudaSuccess) {
     const long long outs = (long long)a.nl * a.nr * (2LL * a.H - 1) * (2LL * a.W - 1);
     const long long sum_blocks = (outs + 255) / 256;
-    xcorr_band_sum_kernel<kRowsQ><<<unsigned(sum_blocks < 65535 * 16 ? sum_blocks : 65535 * 16), 256, 0,
-                            stream>>>(a);
+    xcorr_band_sum_kernel<kRowsP, kRowsQ>
+        <<<unsigned(sum_blocks < 65535 * 16 ? sum_blocks : 65535 * 16), 256, 0, stream>>>(a);
     e = cudaGetLastError();
   }
   if (pooled) {

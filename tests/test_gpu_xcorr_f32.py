@@ -67,12 +67,16 @@ def test_fixture(path):
     (2, 3, 50, 8), (33, 3, 5, 5), (1, 1, 1, 300), (1, 1, 300, 1),
     # rights in lanes: ragged right block, W % 4 != 0, short H, several lefts
     (2, 40, 20, 12), (1, 33, 30, 10), (3, 64, 9, 40), (1, 96, 33, 8),
-    # row kernel, 32-row chunks: two row bands, a ragged last chunk, W % 4 != 0
+    # row kernel: two row bands, a ragged last chunk, W % 4 != 0
     (1, 2, 130, 257), (2, 1, 200, 64),
-    # row kernel, 16-row chunks (rows too wide for 32): one and two bands
-    (1, 1, 40, 520), (1, 1, 140, 420),
-    # too short or too wide to stage: the bounds-checked fallback kernel
-    (1, 1, 5, 400), (2, 2, 3, 700), (1, 6, 4, 520), (1, 1, 24, 800),
+    # row kernel, whole rows in 16-row chunks (too wide for 32): one and two
+    # bands, two pairs
+    (1, 1, 40, 520), (1, 1, 140, 420), (2, 1, 26, 450),
+    # row kernel, windows of three x segments (rows too wide to stage whole),
+    # also with W % 4 != 0 (element-wise staging)
+    (1, 1, 24, 800), (1, 1, 30, 799),
+    # too short to give lanes rows: the bounds-checked fallback kernel
+    (1, 1, 5, 400), (2, 2, 3, 700), (1, 6, 4, 520),
 ])
 def test_shapes(nl, nr, H, W):
     check(rand(nl, H, W), rand(nr, H, W, "normal"))

@@ -32,7 +32,7 @@ def call(fn, L, R, out):
               R.shape[0], H, W, ctypes.c_void_p(out.data_ptr()))
 
 
-@pytest.mark.parametrize("nl,nr,H,W", [(1, 1, 256, 256), (1, 2, 130, 257), (2, 3, 40, 40),
+@pytest.mark.parametrize("nl,nr,H,W", [(1, 1, 256, 256), (1, 2, 130, 257), (1, 1, 24, 800), (2, 3, 40, 40),
                                        (32, 64, 16, 16)])
 def test_noalloc_matches_allocating_entry_point(nl, nr, H, W):
     rng = np.random.default_rng(77 + H)
@@ -61,9 +61,10 @@ def test_noalloc_matches_allocating_entry_point(nl, nr, H, W):
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
     dev = torch.device("cuda", 0)
-    L = torch.zeros((1, 256, 256), dtype=torch.float32, device=dev)
-    R = torch.zeros((9, 256, 256), dtype=torch.float32, device=dev)   # 9 x 2 MiB > 16 MiB
-    out = torch.full((1, 9, 511, 511), 7.0, dtype=torch.float32, device=dev)
+    # one 1024x1024 pair: three x segments of partial sums, 48 MiB > 16 MiB
+    L = torch.zeros((1, 1024, 1024), dtype=torch.float32, device=dev)
+    R = torch.zeros((1, 1024, 1024), dtype=torch.float32, device=dev)
+    out = torch.full((1, 1, 2047, 2047), 7.0, dtype=torch.float32, device=dev)
     assert call(corr.load().corr_xcorr_f32_noalloc, L, R, out) == -2
     torch.cuda.synchronize()
     assert (out == 7.0).all()                  # nothing was launched
