@@ -723,9 +723,26 @@ __global__ void __launch_bounds__(kThreads, 2) xcorr_pair_kernel(const XArgs a) 
 // kBRows rows padded to an odd number of 16-byte units) with cp.async into
 // two buffers.
 // ---------------------------------------------------------------------------
-constexpr int kBRows = 4;
-constexpr int kBRights = 2;               // rights per lane
+#ifndef CORR_XC_BROWS
+#define CORR_XC_BROWS 4
+#endif
+#ifndef CORR_XC_BR
+#define CORR_XC_BR 2
+#endif
+#ifndef CORR_XC_BMINB
+#define CORR_XC_BMINB 1
+#endif
+constexpr int kBRows = CORR_XC_BROWS;     // overlap rows per chunk
+constexpr int kBRights = CORR_XC_BR;      // rights per lane
+static_assert(kBRows % 2 == 0, "two row halves");
 constexpr int kBMats = 1 + 32 * kBRights; // matrices staged per chunk
+#ifndef CORR_XC_BPAIRS
+#define CORR_XC_BPAIRS 8
+#endif
+constexpr int kBWarps = 2 * kWarps;              // row parts x group pairs
+constexpr int kBPairs = CORR_XC_BPAIRS;          // dx-group pairs per CTA
+constexpr int kBParts = kBWarps / kBPairs;       // row parts of a chunk
+static_assert(kBRows % kBParts == 0, "whole rows per row part");
 
 __device__ __forceinline__ int bcast_slab(int S) { return kBRows * S + 4; }
 __device__ __forceinline__ int bcast_buf(int S) {
@@ -734,8 +751,8 @@ __device__ __forceinline__ int bcast_buf(int S) {
 
 // Issue one chunk: left rows yc .. yc+kBRows-1 (zero past yhi) and, for each
 // of the CTA's 32*kBRights rights, rows yc-dy .. (zero past nr or past yhi).
-// The flattened (matrix, row, column) index advances by blockDim.x per step;
-// its three parts are carried instead of divided.
+// A row's addresses are formed once: a row of n copies goes to the smallest
+// of 4, 8, 16 or 32 lanes that covers it (lanes along the row).
 __device__ __forceinline__ void issue_bchunk(const XArgs &a, uint32_t sbase, int buf,
                                              const float *L, int r_first, int yc,
                                              int yhi, int dy) {
@@ -744,35 +761,28 @@ __device__ __forceinline__ void issue_bchunk(const XArgs &a, uint32_t sbase, int
   const int step = vec4 ? 4 : 1, n = vec4 ? (W >> 2) : W;
   const size_t mat = size_t(H) * W;
   const int slab = bcast_slab(S);
-  const int per_mat = kBRows * n;
-  const int total = kBMats * per_mat;
-  const int stride = blockDim.x;
-  // stride = sm * per_mat + sr * n + sc
-  const int sm_ = stride / per_mat, srem = stride - sm_ * per_mat;
-  const int sr = srem / n, sc = srem - sr * n;
-  int m = threadIdx.x / per_mat;
-  int r = (threadIdx.x - m * per_mat) / n;
-  int c = threadIdx.x - m * per_mat - r * n;
-  for (int e = threadIdx.x; e < total; e += stride) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int lpr = n <= 4 ? 4 : n <= 8 ? 8 : n <= 16 ? 16 : 32;   // lanes per row
+  const int rpw = 32 / lpr;                     // rows per warp step
+  const int sub = lane / lpr, col0 = lane % lpr;
+  for (int row = warp * rpw + sub; row < kBMats * kBRows; row += kBWarps * rpw) {
+    const int m = row / kBRows, r = row % kBRows;
     const int y = yc + r;
     bool ok = y < yhi;
     const float *src;
     int dst;
     if (m == 0) {
-      src = L + (ok ? size_t(y) * W + c * step : 0);
-      dst = buf + r * S + kPadL + c * step;
+      src = L + (ok ? size_t(y) * W : 0);
+      dst = buf + r * S + kPadL;
     } else {
       const int ri = r_first + (m - 1);
       ok = ok && ri < a.nr;
-      src = a.right + (ok ? size_t(ri) * mat + size_t(y - dy) * W + c * step : 0);
-      dst = buf + kBRows * S + (m - 1) * slab + r * S + kPadL + c * step;
+      src = a.right + (ok ? size_t(ri) * mat + size_t(y - dy) * W : 0);
+      dst = buf + kBRows * S + (m - 1) * slab + r * S + kPadL;
     }
-    cp_async(sbase + 4u * uint32_t(dst), src, ok, vec4);
-    c += sc;
-    r += sr;
-    m += sm_;
-    if (c >= n) { c -= n; ++r; }
-    if (r >= kBRows) { r -= kBRows; ++m; }
+    const uint32_t d = sbase + 4u * uint32_t(dst);
+    for (int c = col0; c < n; c += lpr)
+      cp_async(d + 4u * uint32_t(c * step), src + c * step, ok, vec4);
   }
 }
 
@@ -792,14 +802,13 @@ __device__ __forceinline__ XGroup make_xgroup(int W, int dx0) {
   return g;
 }
 
-constexpr int kBWarps = 2 * kWarps;     // two row halves x kWarps group pairs
 
-__global__ void __launch_bounds__(32 * kBWarps, 1) xcorr_bcast_kernel(const XArgs a) {
+__global__ void __launch_bounds__(32 * kBWarps, CORR_XC_BMINB) xcorr_bcast_kernel(const XArgs a) {
   const uint32_t sbase = uint32_t(__cvta_generic_to_shared(g_smem4));
   float *sm = reinterpret_cast<float *>(g_smem4);
   const int warp_id = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int warp = warp_id % kWarps;    // dx-group pair of this warp
-  const int rh = warp_id / kWarps;      // row half: rows 2*rh, 2*rh+1 of each chunk
+  const int warp = warp_id % kBPairs;   // dx-group pair of this warp
+  const int rh = warp_id / kBPairs;     // row part: rows rh * kBRows / kBParts .. of a chunk
   const int H = a.H, W = a.W, S = a.S;
   const int G = a.ngroups, ngp = (G + 1) / 2;
   int item = blockIdx.x;
@@ -815,7 +824,7 @@ __global__ void __launch_bounds__(32 * kBWarps, 1) xcorr_bcast_kernel(const XArg
 
   // groups g and g + ngp: shifts dx and dx + 8*ngp (about dx + W), whose x
   // ranges add up to about W, so every warp carries the same work
-  const int gp = pbk * kWarps + warp;
+  const int gp = pbk * kBPairs + warp;
   const bool gp_ok = gp < ngp;
   const int gA = gp, gB = gp + ngp;
   const bool has_b = gp_ok && gB < G;
@@ -846,7 +855,7 @@ __global__ void __launch_bounds__(32 * kBWarps, 1) xcorr_bcast_kernel(const XArg
     }
     if (!gp_ok) continue;
     const int rows = min(kBRows, yhi - yc);
-    for (int k = 2 * rh; k < min(rows, 2 * rh + 2); ++k) {
+    for (int k = rh * (kBRows / kBParts); k < min(rows, (rh + 1) * (kBRows / kBParts)); ++k) {
       const int lrow = buf + k * S + kPadL;
       const int rrow = buf + kBRows * S + lane * slab + k * S + kPadL;
       {
@@ -863,12 +872,12 @@ __global__ void __launch_bounds__(32 * kBWarps, 1) xcorr_bcast_kernel(const XArg
       }
     }
   }
-  // row half 1 hands its partial sums to row half 0 (fixed order: exact
-  // same result on every run)
+  // row parts 1.. hand their partial sums to row part 0, which adds them in
+  // part order (the same result on every run)
   __syncthreads();                       // chunk buffers are free again
   constexpr int kPart = 2 * kBRights * kP;   // partial sums per lane
-  float *part = sm + (warp * kPart) * 32 + lane;
-  if (rh == 1) {
+  if (rh > 0) {
+    float *part = sm + (((rh - 1) * kBPairs + warp) * kPart) * 32 + lane;
 #pragma unroll
     for (int j = 0; j < kBRights; ++j)
 #pragma unroll
@@ -878,7 +887,18 @@ __global__ void __launch_bounds__(32 * kBWarps, 1) xcorr_bcast_kernel(const XArg
       }
   }
   __syncthreads();
-  if (rh == 1 || !gp_ok) return;
+  if (rh > 0 || !gp_ok) return;
+#pragma unroll
+  for (int q = 1; q < kBParts; ++q) {
+    const float *part = sm + (((q - 1) * kBPairs + warp) * kPart) * 32 + lane;
+#pragma unroll
+    for (int j = 0; j < kBRights; ++j)
+#pragma unroll
+      for (int p = 0; p < kP; ++p) {
+        accA[j][p] += part[(j * kP + p) * 32];
+        accB[j][p] += part[((kBRights + j) * kP + p) * 32];
+      }
+  }
   const int OW = 2 * W - 1;
 #pragma unroll
   for (int j = 0; j < kBRights; ++j) {
@@ -889,14 +909,13 @@ __global__ void __launch_bounds__(32 * kBWarps, 1) xcorr_bcast_kernel(const XArg
 #pragma unroll
     for (int p = 0; p < kP; ++p) {
       const int dx = xa.dx0 + p;
-      if (dx > -W && dx < W) orow[dx + W - 1] = accA[j][p] + part[(j * kP + p) * 32];
+      if (dx > -W && dx < W) orow[dx + W - 1] = accA[j][p];
     }
     if (has_b) {
 #pragma unroll
       for (int p = 0; p < kP; ++p) {
         const int dx = xb.dx0 + p;
-        if (dx > -W && dx < W)
-          orow[dx + W - 1] = accB[j][p] + part[((kBRights + j) * kP + p) * 32];
+        if (dx > -W && dx < W) orow[dx + W - 1] = accB[j][p];
       }
     }
   }
@@ -1180,9 +1199,23 @@ cudaError_t launch_tiny(const float *left, int nl, const float *right, int nr, i
   const int nunits = (2 * H - 1) * (2 * W - 1);
   a.vec4 = ((H * W) % 4 == 0 && (reinterpret_cast<uintptr_t>(left) & 15) == 0 &&
             (reinterpret_cast<uintptr_t>(right) & 15) == 0) ? 1 : 0;
-  long long nc = (sm_count() + bp - 1) / bp;
-  if (nc > nunits) nc = nunits;
-  if (nc < 1) nc = 1;
+  // CTAs per block pair: about one CTA per SM, so a grid of bp * nc CTAs
+  // runs in ceil(bp * nc / SMs) waves of CTAs that each take 1/nc of a block
+  // pair: pick the nc with the fewest waves per unit of work (fewest CTAs on
+  // ties)
+  const long long sms = sm_count();
+  long long nc = 1;
+  {
+    const long long cap = nunits < 4 * sms ? nunits : 4 * sms;
+    double best = 1e30;
+    for (long long n = 1; n <= cap; ++n) {
+      const double t = double((bp * n + sms - 1) / sms) / double(n);
+      if (t < best * (1.0 - 1e-9)) {
+        best = t;
+        nc = n;
+      }
+    }
+  }
   a.nc = int(nc);
   const long long blocks = bp * a.nc;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
@@ -1307,7 +1340,7 @@ XPlan make_plan(const float *left, int nl, const float *right, int nr, int H, in
     const size_t bsmem = 2 * buf_floats * sizeof(float);
     const int ngp = (a.ngroups + 1) / 2;
     a.nrblk = (nr + 32 * kBRights - 1) / (32 * kBRights);
-    a.npairblk = (ngp + kWarps - 1) / kWarps;
+    a.npairblk = (ngp + kBPairs - 1) / kBPairs;
     const long long bblocks = (long long)nl * a.nrblk * a.npairblk * (2LL * H - 1);
     if (nr >= 32 && W >= 8 && bsmem <= kMaxBcastSmem && bblocks <= 0x7fffffffLL) {
       pl.kind = XKind::Bcast;
