@@ -31,6 +31,9 @@
 // per clock) is 73-91 % busy with dp4a depending on image and template size.
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <string.h>
+
+#include <type_traits>
 
 #include "internal.cuh"
 
@@ -61,6 +64,7 @@ constexpr int kThreads = 32 * kWarpsPerCta;
 constexpr int kSplit = CORR_NCC_KSPLIT;
 constexpr int kFixedThreads = kThreads * kSplit;
 constexpr uint32_t kOnes = 0x01010101u;
+constexpr int kStageBatch = 4;       // tile chunks per thread loaded ahead of the template
 
 struct NccArgs {
   const uint8_t *image;
@@ -257,27 +261,41 @@ __global__ void __launch_bounds__(kFixedThreads, CORR_NCC_MINB)
   const int trows = min(TY + a.ht - 1, a.h - yt);   // tile rows inside the image
 
   // ---- tile + halo -> shared memory (out-of-image bytes become zero) ----
-  if (V16) {
-    constexpr int C = RB / 16;
-    for (int i = threadIdx.x; i < trows * C; i += kFixedThreads) {
-      const int r = i / C, c = i - r * C;
-      const int x = xt + 16 * c;                    // w % 16 == 0: chunk in or out
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (x < a.w) v = __ldg(reinterpret_cast<const uint4 *>(a.image + size_t(yt + r) * a.w + x));
-      *reinterpret_cast<uint4 *>(tile + r * RB + 16 * c) = v;
-    }
-  } else {
-    constexpr int C = RB / 8;
-    for (int i = threadIdx.x; i < trows * C; i += kFixedThreads) {
-      const int r = i / C, c = i - r * C;
-      const int x = xt + 8 * c;                     // w % 8 == 0: pair in or out
-      uint2 v = make_uint2(0u, 0u);
-      if (x < a.w) v = __ldg(reinterpret_cast<const uint2 *>(a.image + size_t(yt + r) * a.w + x));
-      *reinterpret_cast<uint2 *>(tile + r * RB + 8 * c) = v;
-    }
+  // The first kStageBatch chunks per thread are loaded into registers and
+  // the template is staged while they are in flight, so a tile costs about
+  // one memory latency; taller tiles copy the rest afterwards.
+  using Chunk = typename std::conditional<V16, uint4, uint2>::type;
+  constexpr int CB = int(sizeof(Chunk));              // bytes per chunk
+  constexpr int C = RB / CB;                          // chunks per tile row
+  const int nchunks = trows * C;
+  auto chunk_load = [&](int i) {
+    Chunk v;
+    memset(&v, 0, sizeof(v));
+    const int r = i / C, c = i - r * C;
+    const int x = xt + CB * c;                        // w % CB == 0: chunk in or out
+    if (x < a.w) v = __ldg(reinterpret_cast<const Chunk *>(a.image + size_t(yt + r) * a.w + x));
+    return v;
+  };
+  auto chunk_store = [&](int i, const Chunk &v) {
+    const int r = i / C, c = i - r * C;
+    *reinterpret_cast<Chunk *>(tile + r * RB + CB * c) = v;
+  };
+  Chunk first[kStageBatch];
+#pragma unroll
+  for (int k = 0; k < kStageBatch; ++k) {
+    const int i = threadIdx.x + k * kFixedThreads;
+    if (i < nchunks) first[k] = chunk_load(i);
   }
   uint32_t sum_t, sum_t_sq;
   stage_template(a, tmpl_s, red, sum_t, sum_t_sq);   // ends with __syncthreads
+#pragma unroll
+  for (int k = 0; k < kStageBatch; ++k) {
+    const int i = threadIdx.x + k * kFixedThreads;
+    if (i < nchunks) chunk_store(i, first[k]);
+  }
+  for (int i = threadIdx.x + kStageBatch * kFixedThreads; i < nchunks; i += kFixedThreads)
+    chunk_store(i, chunk_load(i));
+  __syncthreads();
 
   const int warp_id = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int warp = warp_id % kWarpsPerCta;            // row group of the tile

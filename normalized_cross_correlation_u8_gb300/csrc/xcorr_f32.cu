@@ -926,8 +926,8 @@ __global__ void __launch_bounds__(32 * kBWarps, CORR_XC_BMINB) xcorr_bcast_kerne
 // interleaved as [y][x][matrix]; lane (lb = lane%8, rb = lane/8) owns lefts
 // 4lb..4lb+3 x rights 4rb..4rb+3 of one shift and walks its exact overlap:
 // per (y, x) two 16-byte loads feed 16 FMAs.  Shifts are dealt to the CTAs
-// of a block pair round-robin in a centre-first order and pulled by the
-// CTA's warps from a shared counter.
+// of a block pair in snake order over a centre-first ranking and pulled by
+// the CTA's warps from a shared counter.
 // ---------------------------------------------------------------------------
 constexpr int kTinyL = 32, kTinyR = 16, kTinyWarps = 16;
 
@@ -1000,13 +1000,16 @@ __global__ void __launch_bounds__(32 * kTinyWarps) xcorr_tiny_kernel(const TinyA
   const int lane = threadIdx.x & 31;
   const int lb = lane & 7, rb = lane >> 3;
   const int ndy = 2 * H - 1, ndx = 2 * W - 1, nunits = ndy * ndx;
-  const int mine = (nunits - c + a.nc - 1) / a.nc;   // units k = c, c+nc, ...
+  // this CTA's units: rank j * nc + (j even ? c : nc - 1 - c) of the
+  // centre-first order (snake order: every CTA gets a similar mix of costs)
+  const int rounds = nunits / a.nc, rem = nunits - rounds * a.nc;
+  const int mine = rounds + (((rounds & 1) ? a.nc - 1 - c : c) < rem ? 1 : 0);
   for (;;) {
     int u = 0;
     if (lane == 0) u = atomicAdd(&next_unit, 1);
     u = __shfl_sync(0xffffffffu, u, 0);
     if (u >= mine) break;
-    const int kk = c + u * a.nc;                     // centre-first rank
+    const int kk = u * a.nc + ((u & 1) ? a.nc - 1 - c : c);   // centre-first rank
     const int dy = centered(kk % ndy, ndy) - (H - 1);
     const int dx = centered(kk / ndy, ndx) - (W - 1);
     const int ylo = max(0, dy), yhi = min(H, H + dy);
