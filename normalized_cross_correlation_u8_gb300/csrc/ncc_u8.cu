@@ -11,8 +11,8 @@
 // independent output columns (and rows) per thread keep many accumulation
 // chains in flight (the section's instruction-level parallelism).
 //
-// GB300 layout of the work (fast path: wt in {16, 32, 64}, image and width
-// 8-byte aligned; every other shape takes the general path below):
+// GB300 layout of the work (fast path: wt a multiple of 4 up to 64, image
+// and width 8-byte aligned; every other shape takes the general path below):
 //   * a CTA owns 128 output columns x TY output rows; it copies the image
 //     tile plus its halo (TY+ht-1 rows x 128+wt+8 bytes) into shared memory
 //     with independent 16-byte vector loads (one memory latency per tile,
@@ -33,7 +33,9 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <array>
 #include <type_traits>
+#include <utility>
 
 #include "internal.cuh"
 
@@ -193,8 +195,16 @@ __device__ __forceinline__ float template_rsqrt(const NccArgs &a, uint32_t sum_t
 // One image row (tile-relative index rel = k - y0) against template rows
 // rel - r for the R output rows r of the unit; `mask` selects the rows r for
 // which 0 <= rel - r < ht (all of them when FULL).
+// Words of one staged image row a lane holds: the WT + 1 words its 8
+// windows reach, read as 8-byte pairs.
+template <int WT>
+struct RowWords {
+  static constexpr int kPairs = (WT + 3) / 2;
+  static constexpr int kWords = 2 * kPairs;
+};
+
 template <int R, int WT, bool FULL>
-__device__ __forceinline__ void row_fixed(const uint32_t (&wv)[WT + 2],
+__device__ __forceinline__ void row_fixed(const uint32_t (&wv)[RowWords<WT>::kWords],
                                           const uint32_t *tmpl_s, int rel,
                                           unsigned mask, uint32_t (&sI)[R][kCols],
                                           uint32_t (&sQ)[R][kCols],
@@ -317,11 +327,12 @@ __global__ void __launch_bounds__(kFixedThreads, CORR_NCC_MINB)
   // never stored).
   const int nrows = max(0, min(R + a.ht - 1, trows - warp * 2 * R));
   const uint8_t *lane_base = tile + hl * kCols;
-  auto load_row = [&](int rel, uint32_t (&dst)[WT + 2]) {
+  constexpr int NW = RowWords<WT>::kWords;
+  auto load_row = [&](int rel, uint32_t (&dst)[NW]) {
     const int r = min(yr0 + rel, trows - 1);
     const uint8_t *row = lane_base + r * RB;
 #pragma unroll
-    for (int p = 0; p < (WT + 2) / 2; ++p) {
+    for (int p = 0; p < RowWords<WT>::kPairs; ++p) {
       const uint2 v = *reinterpret_cast<const uint2 *>(row + 8 * p);
       dst[2 * p] = v.x;
       dst[2 * p + 1] = v.y;
@@ -329,7 +340,7 @@ __global__ void __launch_bounds__(kFixedThreads, CORR_NCC_MINB)
   };
   // tile row yr0 + rel meets template row rel - r for output row r; this
   // warp group takes template rows [j_lo, j_hi)
-  auto process = [&](const uint32_t (&wv)[WT + 2], int rel) {
+  auto process = [&](const uint32_t (&wv)[NW], int rel) {
     if (rel - (R - 1) >= j_lo && rel <= j_hi - 1) {
       row_fixed<R, WT, true>(wv, tmpl_s, rel, 0u, sI, sQ, sT);
     } else {
@@ -340,9 +351,8 @@ __global__ void __launch_bounds__(kFixedThreads, CORR_NCC_MINB)
       row_fixed<R, WT, false>(wv, tmpl_s, rel, mask, sI, sQ, sT);
     }
   };
-  static_assert(WT % 2 == 0, "fixed path expects an even word count");
   const int rel_end = min(nrows, j_hi + R - 1);
-  uint32_t wa[WT + 2], wb[WT + 2];
+  uint32_t wa[NW], wb[NW];
   if (j_lo < rel_end) load_row(j_lo, wa);
   for (int rel = j_lo; rel < rel_end; rel += 2) {
     if (rel + 1 < rel_end) load_row(rel + 1, wb);
@@ -472,6 +482,22 @@ cudaError_t launch_tiles(Kernel kernel, const NccArgs &a, size_t smem,
   return cudaGetLastError();
 }
 
+// Fast-path launchers for template widths of 1 .. kMaxFixedWords words.
+constexpr int kMaxFixedWords = 16;
+using FixedLauncher = cudaError_t (*)(const NccArgs &, size_t, bool, cudaStream_t);
+
+template <int R, int WT>
+cudaError_t launch_fixed(const NccArgs &a, size_t smem, bool aligned16, cudaStream_t stream) {
+  return aligned16 ? launch_tiles(ncc_u8_fixed_kernel<R, WT, true>, a, smem, stream)
+                   : launch_tiles(ncc_u8_fixed_kernel<R, WT, false>, a, smem, stream);
+}
+
+template <int R, int... Ks>
+constexpr std::array<FixedLauncher, sizeof...(Ks)> fixed_launchers(
+    std::integer_sequence<int, Ks...>) {
+  return {{launch_fixed<R, Ks + 1>...}};
+}
+
 }  // namespace
 
 cudaError_t ncc_u8_launch(const uint8_t *image, int w, int h,
@@ -497,7 +523,7 @@ cudaError_t ncc_u8_launch(const uint8_t *image, int w, int h,
 
   const bool aligned8 = (reinterpret_cast<uintptr_t>(image) & 7) == 0 && (w & 7) == 0;
   const bool aligned16 = (reinterpret_cast<uintptr_t>(image) & 15) == 0 && (w & 15) == 0;
-  if (aligned8 && (a.wtw == 4 || a.wtw == 8 || a.wtw == 16)) {
+  if (aligned8 && a.wtw >= 1 && a.wtw <= kMaxFixedWords) {
     constexpr int TY = 2 * R * kWarpsPerCta;
     a.tiles_x = (a.ow + kHalfUnitCols - 1) / kHalfUnitCols;
     const long long tiles = (long long)a.tiles_x * ((a.oh + TY - 1) / TY);
@@ -510,14 +536,8 @@ cudaError_t ncc_u8_launch(const uint8_t *image, int w, int h,
     };
     const size_t ts = tile_smem(a.wtw);
     if (ts > 200 * 1024) goto general;   // very tall template: general path
-    switch (a.wtw) {
-      case 4: return aligned16 ? launch_tiles(ncc_u8_fixed_kernel<R, 4, true>, a, ts, stream)
-                               : launch_tiles(ncc_u8_fixed_kernel<R, 4, false>, a, ts, stream);
-      case 8: return aligned16 ? launch_tiles(ncc_u8_fixed_kernel<R, 8, true>, a, ts, stream)
-                               : launch_tiles(ncc_u8_fixed_kernel<R, 8, false>, a, ts, stream);
-      default: return aligned16 ? launch_tiles(ncc_u8_fixed_kernel<R, 16, true>, a, ts, stream)
-                                : launch_tiles(ncc_u8_fixed_kernel<R, 16, false>, a, ts, stream);
-    }
+    static constexpr auto table = fixed_launchers<R>(std::make_integer_sequence<int, kMaxFixedWords>{});
+    return table[a.wtw - 1](a, ts, aligned16, stream);
   }
 general:
   a.tiles_x = (a.ow + kUnitCols - 1) / kUnitCols;

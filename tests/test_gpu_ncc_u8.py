@@ -62,14 +62,20 @@ def test_fixture(path):
     assert np.abs(c - fx["coef"]).max() <= COEF_TOL
 
 
-# fast path (wt in 16/32/64, w % 8 == 0) and general path shapes; ragged
-# tails in both directions (ow not a multiple of 256, oh odd)
+# fast path (wt a multiple of 4 up to 64, w % 8 == 0; rows 16-byte aligned
+# when w % 16 == 0) and general path shapes; ragged tails in both directions
+# (ow not a multiple of 128, oh odd)
 SHAPES = [
     (40, 64, 16, 16), (97, 296, 16, 16), (77, 520, 32, 32), (130, 264, 64, 64),
     (33, 1000, 32, 7), (50, 600, 64, 3), (21, 256, 16, 21),
     (45, 300, 4, 3), (39, 100, 12, 5), (61, 333, 20, 9), (70, 515, 36, 11),
     (16, 16, 16, 16), (9, 4, 4, 1), (5, 260, 128, 5), (300, 20, 8, 200),
     (1, 1024, 64, 1), (200, 8, 8, 64),
+    # fast path, every template width of 1 .. 15 words
+    (45, 304, 4, 3), (41, 136, 8, 9), (39, 104, 12, 5), (61, 336, 20, 9),
+    (50, 400, 24, 13), (66, 272, 28, 30), (70, 520, 36, 11), (80, 264, 40, 17),
+    (90, 512, 44, 19), (100, 384, 48, 48), (75, 200, 52, 21), (120, 640, 56, 56),
+    (64, 328, 60, 23),
 ]
 
 
