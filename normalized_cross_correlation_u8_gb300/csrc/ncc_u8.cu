@@ -11,8 +11,8 @@
 // independent output columns (and rows) per thread keep many accumulation
 // chains in flight (the section's instruction-level parallelism).
 //
-// GB300 layout of the work (fast path: wt a multiple of 4 up to 64, image
-// and width 8-byte aligned; every other shape takes the general path below):
+// GB300 layout of the work (fast path: wt a multiple of 4 up to 64, any
+// image alignment; wider templates take the general path below):
 //   * a CTA owns 128 output columns x TY output rows; it copies the image
 //     tile plus its halo (TY+ht-1 rows x 128+wt+8 bytes) into shared memory
 //     with independent 16-byte vector loads (one memory latency per tile,
@@ -238,8 +238,8 @@ __device__ __forceinline__ void row_fixed(const uint32_t (&wv)[RowWords<WT>::kWo
   }
 }
 
-// Fast path: template width WT words known at compile time, image pointer
-// and width 8-byte aligned.
+// Fast path: template width WT words known at compile time, any image
+// alignment (the staging unit VB follows it).
 //
 // A CTA owns a tile of 128 output columns x TY = 2*R*kWarpsPerCta output
 // rows.  It first copies the image tile plus halo -- TY+ht-1 rows of
@@ -255,7 +255,18 @@ struct TileGeom {
   static constexpr int kRowBytes = (kHalfUnitCols + 4 * WT + 8 + 15) & ~15;
 };
 
-template <int R, int WT, bool V16>
+// Tile staging unit by image alignment: VB = 16 or 8 when the image pointer
+// and width are that aligned (whole vector loads, a chunk lies wholly inside
+// or outside the image), VB = 1 otherwise (4-byte chunks assembled from byte
+// loads, each byte checked against w).
+template <int VB>
+struct StageChunk {
+  using type = typename std::conditional<VB == 16, uint4,
+               typename std::conditional<VB == 8, uint2, uint32_t>::type>::type;
+  static constexpr int kBytes = int(sizeof(type));
+};
+
+template <int R, int WT, int VB>
 __global__ void __launch_bounds__(kFixedThreads, CORR_NCC_MINB)
     ncc_u8_fixed_kernel(const NccArgs a) {
   constexpr int WTP = (WT + 3) & ~3;
@@ -274,16 +285,23 @@ __global__ void __launch_bounds__(kFixedThreads, CORR_NCC_MINB)
   // The first kStageBatch chunks per thread are loaded into registers and
   // the template is staged while they are in flight, so a tile costs about
   // one memory latency; taller tiles copy the rest afterwards.
-  using Chunk = typename std::conditional<V16, uint4, uint2>::type;
-  constexpr int CB = int(sizeof(Chunk));              // bytes per chunk
+  using Chunk = typename StageChunk<VB>::type;
+  constexpr int CB = StageChunk<VB>::kBytes;          // bytes per chunk
   constexpr int C = RB / CB;                          // chunks per tile row
   const int nchunks = trows * C;
   auto chunk_load = [&](int i) {
     Chunk v;
     memset(&v, 0, sizeof(v));
     const int r = i / C, c = i - r * C;
-    const int x = xt + CB * c;                        // w % CB == 0: chunk in or out
-    if (x < a.w) v = __ldg(reinterpret_cast<const Chunk *>(a.image + size_t(yt + r) * a.w + x));
+    const int x = xt + CB * c;
+    const uint8_t *row = a.image + size_t(yt + r) * a.w;
+    if constexpr (VB == 1) {
+#pragma unroll
+      for (int b = 0; b < 4; ++b)
+        if (x + b < a.w) v |= uint32_t(__ldg(row + x + b)) << (8 * b);
+    } else {
+      if (x < a.w) v = __ldg(reinterpret_cast<const Chunk *>(row + x));   // w % CB == 0
+    }
     return v;
   };
   auto chunk_store = [&](int i, const Chunk &v) {
@@ -484,12 +502,13 @@ cudaError_t launch_tiles(Kernel kernel, const NccArgs &a, size_t smem,
 
 // Fast-path launchers for template widths of 1 .. kMaxFixedWords words.
 constexpr int kMaxFixedWords = 16;
-using FixedLauncher = cudaError_t (*)(const NccArgs &, size_t, bool, cudaStream_t);
+using FixedLauncher = cudaError_t (*)(const NccArgs &, size_t, int, cudaStream_t);
 
 template <int R, int WT>
-cudaError_t launch_fixed(const NccArgs &a, size_t smem, bool aligned16, cudaStream_t stream) {
-  return aligned16 ? launch_tiles(ncc_u8_fixed_kernel<R, WT, true>, a, smem, stream)
-                   : launch_tiles(ncc_u8_fixed_kernel<R, WT, false>, a, smem, stream);
+cudaError_t launch_fixed(const NccArgs &a, size_t smem, int vb, cudaStream_t stream) {
+  return vb == 16 ? launch_tiles(ncc_u8_fixed_kernel<R, WT, 16>, a, smem, stream)
+       : vb == 8  ? launch_tiles(ncc_u8_fixed_kernel<R, WT, 8>, a, smem, stream)
+                  : launch_tiles(ncc_u8_fixed_kernel<R, WT, 1>, a, smem, stream);
 }
 
 template <int R, int... Ks>
@@ -523,7 +542,7 @@ cudaError_t ncc_u8_launch(const uint8_t *image, int w, int h,
 
   const bool aligned8 = (reinterpret_cast<uintptr_t>(image) & 7) == 0 && (w & 7) == 0;
   const bool aligned16 = (reinterpret_cast<uintptr_t>(image) & 15) == 0 && (w & 15) == 0;
-  if (aligned8 && a.wtw >= 1 && a.wtw <= kMaxFixedWords) {
+  if (a.wtw >= 1 && a.wtw <= kMaxFixedWords) {
     constexpr int TY = 2 * R * kWarpsPerCta;
     a.tiles_x = (a.ow + kHalfUnitCols - 1) / kHalfUnitCols;
     const long long tiles = (long long)a.tiles_x * ((a.oh + TY - 1) / TY);
@@ -537,7 +556,7 @@ cudaError_t ncc_u8_launch(const uint8_t *image, int w, int h,
     const size_t ts = tile_smem(a.wtw);
     if (ts > 200 * 1024) goto general;   // very tall template: general path
     static constexpr auto table = fixed_launchers<R>(std::make_integer_sequence<int, kMaxFixedWords>{});
-    return table[a.wtw - 1](a, ts, aligned16, stream);
+    return table[a.wtw - 1](a, ts, aligned16 ? 16 : aligned8 ? 8 : 1, stream);
   }
 general:
   a.tiles_x = (a.ow + kUnitCols - 1) / kUnitCols;
