@@ -49,8 +49,10 @@ extern "C" {
  * template).  Numerator and variance terms are exact 64-bit integers; the
  * final ratio is single precision (within 1e-5 absolute of the exact value).
  *
- *   image     device, w*h bytes, row-major, row pitch w bytes (any alignment;
- *             8-byte aligned image with w % 8 == 0 takes the fast path).
+ *   image     device, w*h bytes, row-major, row pitch w bytes, any alignment
+ *             (16- or 8-byte aligned rows are staged with vector loads).
+ *             Templates up to 64 wide take the tiled fast kernel; wider ones a
+ *             general kernel with the same results.
  *   w, h      image width and height in pixels, > 0.
  *   tmpl      device, wt*ht bytes, row-major, pitch wt.
  *   wt, ht    template size, 0 < wt <= w, 0 < ht <= h; wt must be a

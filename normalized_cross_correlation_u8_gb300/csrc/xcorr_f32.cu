@@ -358,7 +358,14 @@ struct XArgs {
 //   slot = ((pair * ndyb + dyb) * nbands + band) * nxseg + xseg.
 // ---------------------------------------------------------------------------
 constexpr int kChunk = 32;
-constexpr int kBandRows = 128;       // band height when bands are needed
+#ifndef CORR_XC_BANDROWS
+#define CORR_XC_BANDROWS 128
+#endif
+#ifndef CORR_XC_BANDMIN
+#define CORR_XC_BANDMIN 16
+#endif
+constexpr int kBandRows = CORR_XC_BANDROWS;   // band height when bands are needed
+constexpr int kBandMinCtasPerSm = CORR_XC_BANDMIN;   // fewer unbanded CTAs per SM: bands
 
 template <int Q, int CH = kChunk>
 struct ChunkGeom {
@@ -1405,7 +1412,7 @@ XPlan make_plan(const float *left, int nl, const float *right, int nr, int H, in
   }
   // row bands only where the grid would otherwise be short of CTAs
   const long long unbanded = pairs * a.ndyb * a.nsuper * a.nxseg;
-  if (unbanded >= 16LL * sm_count() || H <= kBandRows) {
+  if (unbanded >= (long long)kBandMinCtasPerSm * sm_count() || H <= kBandRows) {
     a.nbands = 1;
     a.band_rows = H;
   } else {
