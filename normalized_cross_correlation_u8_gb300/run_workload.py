@@ -3,13 +3,15 @@
     python -m normalized_cross_correlation_u8_gb300.run_workload NAME[,NAME...] [--reps N]
 
 NAME is one of ncc_256, ncc_1080p, ncc_4k (u8 NCC) or xcorr_1to1,
-xcorr_1tomany, xcorr_ntom (f32 cross-correlation); see workloads.py.  Each
-workload's inputs are moved to cuda:0 and the device entry point is called
-N times (default 2); nothing is checked or timed, so the launches can be
-captured by a profiler in isolation.
+xcorr_1tomany, xcorr_ntom (f32 cross-correlation); see workloads.py; or
+xcorr:NLxNRxHxW for an f32 batch of that shape with seeded uniform [-1, 1)
+inputs.  Each workload's inputs are moved to cuda:0 and the device entry
+point is called N times (default 2); nothing is checked or timed, so the
+launches can be captured by a profiler in isolation.
 """
 import argparse
 
+import numpy as np
 import torch
 
 from . import _binding as corr
@@ -32,12 +34,19 @@ def main(argv=None):
             c = torch.empty((h - ht + 1, ww - wt + 1), dtype=torch.float32, device=dev)
             for _ in range(args.reps):
                 corr.ncc_u8_into(img, tm, s, c)
-        elif name in wl.XCORR_WORKLOADS:
-            w = wl.XCORR_WORKLOADS[name]()
-            L = torch.from_numpy(w.left).to(dev)
-            R = torch.from_numpy(w.right).to(dev)
-            nl, H, W = w.left.shape
-            out = torch.empty((nl, w.right.shape[0], 2 * H - 1, 2 * W - 1),
+        elif name in wl.XCORR_WORKLOADS or name.startswith("xcorr:"):
+            if name.startswith("xcorr:"):
+                nl, nr, H, W = (int(v) for v in name[len("xcorr:"):].split("x"))
+                rng = np.random.default_rng(4242)
+                left = rng.uniform(-1, 1, size=(nl, H, W)).astype(np.float32)
+                right = rng.uniform(-1, 1, size=(nr, H, W)).astype(np.float32)
+            else:
+                w = wl.XCORR_WORKLOADS[name]()
+                left, right = w.left, w.right
+            L = torch.from_numpy(left).to(dev)
+            R = torch.from_numpy(right).to(dev)
+            nl, H, W = left.shape
+            out = torch.empty((nl, right.shape[0], 2 * H - 1, 2 * W - 1),
                               dtype=torch.float32, device=dev)
             for _ in range(args.reps):
                 corr.xcorr_f32_into(L, R, out)
