@@ -11,27 +11,30 @@
 // shuffle family), compute several neighbouring overlaps per thread
 // (grouped overlap), reuse one matrix against several others (multi-matrix),
 // and split one overlap's rows over several threads when there are few
-// overlaps (split-row).  The same ideas, laid out for sm_103a, in three
-// kernels chosen by shape:
+// overlaps (split-row).  The same ideas, laid out for sm_103a, in kernels
+// chosen by shape:
 //
-//  rows  (matrices too large to keep a pair in shared memory)
+//  rows  (any pair with 24+ rows and fewer than 32 rights per left)
 //    A CTA owns Q = 4 shifts dy x 8 warps x P = 8 shifts dx of one pair.
-//    The overlap rows y are the reduction: each lane of a warp sums its own
-//    rows, so every lane runs the same x loop.  Rows are staged 32 at a time
-//    into zero-padded shared rows (no bounds tests in the inner loop).
-//  pair  (a pair fits in shared memory: one-to-many and n-to-m of medium
-//    matrices) -- the whole pair is staged once; each warp then loops over
-//    (4 dy x 8 dx) output blocks with the same lane scheme.
+//    The overlap rows y are the reduction: lane i of every warp takes row i
+//    of a 32-row chunk, so every lane runs the same x loop.  Rows are staged
+//    whole into zero-padded shared rows, or, when too wide, as windows of
+//    the columns the CTA's shifts touch in one x segment (no bounds tests in
+//    the inner loop either way).  Row bands and x segments of one output
+//    block are added in a fixed order by a second pass.
+//  bcast (32+ rights per left) -- rights in lanes: every lane of a warp
+//    walks the same left row against its own rights, no cross-lane sums.
 //  tiny  (H*W <= 256, many pairs) -- 32 lefts and 16 rights are staged
 //    interleaved (matrix index fastest); each lane owns 4 lefts x 4 rights
 //    of one shift and walks that shift's exact overlap, so no product is
 //    wasted; warps pull shifts from a per-CTA list.
+//  direct (fewer than 24 rows, few pairs) -- bounds-checked reads through L1.
 //
-// Per lane and overlap row (rows / pair kernels): a float4 of L feeds 4 x
-// steps; for each of the Q rows a float4 of R enters a 12-entry register
-// ring holding R[x-dx0-p] for the P shifts, indexed at compile-time
-// positions by unrolling three 4-step blocks: 5 shared loads feed
-// 4*P*Q = 128 FMAs.  When the last pass has fewer rows than lanes, each row
+// Per lane and overlap row (rows / bcast kernels): a float4 of L feeds 4 x
+// steps; for each of the Q rows (or rights) a float4 of R enters a 12-entry
+// register ring holding R[x-dx0-p] for the P shifts, indexed at
+// compile-time positions by unrolling three 4-step blocks: 5 shared loads
+// feed 4*P*Q = 128 FMAs.  When a chunk has fewer rows than lanes, each row
 // is split into x sub-ranges over several lanes (split-row), and a shuffle
 // butterfly adds the lanes' partial sums before the stores.
 #include <cuda_runtime.h>
@@ -45,10 +48,10 @@
 namespace corr {
 namespace {
 
-constexpr int kP = 8;                // pair / bcast kernels: shifts dx per lane
-constexpr int kQ = 4;                // pair kernel: shifts dy per lane
-constexpr int kPadL = kP;            // pair / bcast kernels: zero columns left of a row
-constexpr int kWarps = 8;            // rows / pair kernels
+constexpr int kP = 8;                // rows / bcast kernels: shifts dx per lane
+constexpr int kQ = 4;                // rows kernel: shifts dy per lane
+constexpr int kPadL = kP;            // bcast kernel: zero columns left of a row
+constexpr int kWarps = 8;            // rows kernel
 constexpr int kThreads = 32 * kWarps;
 
 // rows kernel: shifts dx and dy per lane.
@@ -287,28 +290,6 @@ __device__ __forceinline__ void reduce_store(float (&acc)[Q][P], const Block &k,
     out_pair[size_t(dy + H - 1) * (2 * W - 1) + (dx + W - 1)] = v;
 }
 
-// Copy `rows` matrix rows (global float rows of W, src(r) = pointer or
-// nullptr for a zero row) into shared rows of stride S starting at float
-// `dst0`, data at column kPadL.  One warp per row.
-template <typename Src>
-__device__ __forceinline__ void stage_rows(float *sm, int dst0, int rows, int S, int W,
-                                           bool vec4, Src src) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  for (int r = warp; r < rows; r += nw) {
-    const float *g = src(r);
-    float *d = sm + dst0 + r * S + kPadL;
-    if (!g) {
-      for (int x = lane; x < W; x += 32) d[x] = 0.f;
-    } else if (vec4) {
-      const float4 *g4 = reinterpret_cast<const float4 *>(g);
-      float4 *d4 = reinterpret_cast<float4 *>(d);
-      for (int x = lane; x < (W >> 2); x += 32) d4[x] = __ldg(g4 + x);
-    } else {
-      for (int x = lane; x < W; x += 32) d[x] = __ldg(g + x);
-    }
-  }
-}
-
 __device__ __forceinline__ void zero_smem(float *sm, int n) {
   float4 *s4 = reinterpret_cast<float4 *>(sm);
   for (int i = threadIdx.x; i < (n >> 2); i += blockDim.x) s4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -324,7 +305,6 @@ struct XArgs {
   int ngroups;    // dx groups of kP
   int ndyb;       // dy blocks of kQ
   int nsuper;     // rows kernel: ceil(ngroups / kWarps)
-  int parts;      // pair kernel: CTAs per pair
   int vec4;       // rows can be read as float4
   int nbands;     // rows kernel: row bands (split-row)
   int band_rows;  // rows kernel: overlap rows per band
@@ -636,84 +616,6 @@ __global__ void xcorr_band_sum_kernel(const XArgs a) {
       }
     }
     a.out[i] = sum;
-  }
-}
-
-// ---------------------------------------------------------------------------
-// pair kernel: the CTA stages NSLOT whole pairs (pairs NSLOT*pb + s; R with
-// kQ-1 zero rows above and below), then its warps pull output blocks
-// (4 dy x 8 dx) from a shared counter.  Lane (s, ph) of a warp works on block
-// b of pair slot s and takes overlap rows ph, ph + NPH, ... (NPH = 32/NSLOT),
-// so a lane sums NSLOT times more rows per block than with one slot, and the
-// reduce-scatter runs over NPH lanes.
-// ---------------------------------------------------------------------------
-template <int NSLOT>
-__global__ void __launch_bounds__(kThreads, 2) xcorr_pair_kernel(const XArgs a) {
-  constexpr int NPH = 32 / NSLOT;
-  float *sm = reinterpret_cast<float *>(g_smem4);
-  __shared__ int next_item;
-  const int lane = threadIdx.x & 31;
-  const int H = a.H, W = a.W, S = a.S;
-  const int pb = blockIdx.x / a.parts, part = blockIdx.x - pb * a.parts;
-  const int npairs = a.nl * a.nr;
-  const size_t mat = size_t(H) * W;
-  constexpr int kPadY = kQ - 1;
-  const int rrows = H + 2 * kPadY;
-  const int slot_floats = (H + rrows) * S;
-  zero_smem(sm, NSLOT * slot_floats);
-  if (threadIdx.x == 0) next_item = 0;
-  __syncthreads();
-#pragma unroll
-  for (int sl = 0; sl < NSLOT; ++sl) {
-    const int pair = NSLOT * pb + sl;
-    if (pair >= npairs) continue;
-    const int li = pair / a.nr, ri = pair - li * a.nr;
-    const float *L = a.left + li * mat;
-    const float *R = a.right + ri * mat;
-    stage_rows(sm, sl * slot_floats, H, S, W, a.vec4,
-               [&](int r) -> const float * { return L + size_t(r) * W; });
-    stage_rows(sm, sl * slot_floats + H * S, rrows, S, W, a.vec4, [&](int r) -> const float * {
-      const int yr = r - kPadY;
-      return (yr >= 0 && yr < H) ? R + size_t(yr) * W : nullptr;
-    });
-  }
-  __syncthreads();
-
-  const int slot = lane / NPH, ph = lane - slot * NPH;
-  const int pair = NSLOT * pb + slot;
-  const bool pair_ok = pair < npairs;
-  const int base = slot * slot_floats;
-  float acc[kQ][kP];
-#pragma unroll
-  for (int q = 0; q < kQ; ++q)
-#pragma unroll
-    for (int p = 0; p < kP; ++p) acc[q][p] = 0.f;
-  float *out_pair = a.out + size_t(pair_ok ? pair : 0) * (2 * H - 1) * (2 * W - 1);
-  const int nitems = a.ndyb * a.ngroups;
-  const int mine = (nitems - part + a.parts - 1) / a.parts;   // items part + k*parts
-  for (;;) {
-    int u = 0;
-    if (lane == 0) u = atomicAdd(&next_item, 1);
-    u = __shfl_sync(0xffffffffu, u, 0);
-    if (u >= mine) break;
-    const int it = part + u * a.parts;                      // centre-first rank
-    const int dyb = centered(it % a.ndyb, a.ndyb);
-    const int g = centered(it / a.ndyb, a.ngroups);
-    const Block k = make_block<kP, kQ>(H, W, dyb * kQ - (H - 1), a.dxbase + g * kP);
-    if (pair_ok)
-      for (int y = k.ylo; y < k.yhi; y += NPH)
-        warp_pass<kP, kQ, NPH>(acc, k, y, min(NPH, k.yhi - y), ph,
-                               [&](int yy) { return base + yy * S + kPadL; },
-                               [&](int yr) { return base + (H + kPadY + yr) * S + kPadL; });
-    float v[32 / NPH];
-    reduce_scatter_group<kP, kQ, NPH>(acc, lane, v);
-#pragma unroll
-    for (int i = 0; i < 32 / NPH; ++i) {
-      const int idx = (32 / NPH) * ph + i;
-      const int dy = k.dy0 + idx / kP, dx = k.dx0 + idx % kP;
-      if (pair_ok && dy > -H && dy < H && dx > -W && dx < W)
-        out_pair[size_t(dy + H - 1) * (2 * W - 1) + (dx + W - 1)] = v[i];
-    }
   }
 }
 
@@ -1282,7 +1184,7 @@ cudaError_t scratch_alloc(float **ptr, size_t bytes, cudaStream_t stream) {
 
 }  // namespace
 
-// Largest shared staging area of the rows / pair kernels (two CTAs per SM),
+// Largest shared staging area of the rows kernels (two CTAs per SM),
 // and of the bcast kernel (one CTA per SM at worst).
 constexpr size_t kMaxStageSmem = 110 * 1024;
 constexpr size_t kMaxBcastSmem = 200 * 1024;
@@ -1290,7 +1192,7 @@ constexpr size_t kMaxBcastSmem = 200 * 1024;
 namespace {
 
 // Which kernel a shape takes, its arguments and the split-row scratch it needs.
-enum class XKind { Tiny, Bcast, Pair, Rows, Direct };
+enum class XKind { Tiny, Bcast, Rows, Direct };
 
 struct XPlan {
   XKind kind;
@@ -1298,7 +1200,6 @@ struct XPlan {
   size_t smem;           // dynamic shared memory of the pair / rows kernel
   long long blocks;      // grid of the pair / rows kernel
   size_t part_bytes;     // rows kernel with several bands: scratch bytes
-  int nslot;             // pair kernel: pairs staged per CTA
   int chunk;             // rows kernel: 32 / 16 (whole rows) or 0 (windows)
 };
 
@@ -1308,7 +1209,6 @@ XPlan make_plan(const float *left, int nl, const float *right, int nr, int H, in
   pl.smem = 0;
   pl.blocks = 0;
   pl.part_bytes = 0;
-  pl.nslot = 1;
   pl.chunk = 0;
   const long long pairs = (long long)nl * nr;
   XArgs &a = pl.a;
@@ -1331,7 +1231,6 @@ XPlan make_plan(const float *left, int nl, const float *right, int nr, int H, in
   a.nsuper = (a.ngroups + kWarps - 1) / kWarps;
   a.vec4 = ((W & 3) == 0 && (reinterpret_cast<uintptr_t>(left) & 15) == 0 &&
             (reinterpret_cast<uintptr_t>(right) & 15) == 0) ? 1 : 0;
-  a.parts = 1;
   a.nbands = 1;
   a.band_rows = H;
   a.nxseg = 1;
@@ -1356,25 +1255,6 @@ XPlan make_plan(const float *left, int nl, const float *right, int nr, int H, in
       pl.kind = XKind::Bcast;
       pl.smem = bsmem;
       pl.blocks = bblocks;
-      return pl;
-    }
-  }
-  // pair kernel: whole pairs fit (two per CTA when possible), and there are
-  // enough rows per lane
-  const size_t slot_smem = size_t(H + H + 2 * (kQ - 1)) * a.S * sizeof(float);
-  if (slot_smem <= kMaxStageSmem && H >= 24) {
-    pl.nslot = (pairs >= 2 && 2 * slot_smem <= kMaxStageSmem) ? 2 : 1;
-    const long long pblocks = (pairs + pl.nslot - 1) / pl.nslot;
-    const int items = a.ndyb * a.ngroups;
-    long long parts = (8LL * sm_count() + pblocks - 1) / pblocks;
-    const long long max_parts = (items + kWarps - 1) / kWarps;
-    if (parts > max_parts) parts = max_parts;
-    if (parts < 1) parts = 1;
-    a.parts = int(parts);
-    if (pblocks * a.parts <= 0x7fffffffLL) {
-      pl.kind = XKind::Pair;
-      pl.smem = pl.nslot * slot_smem;
-      pl.blocks = pblocks * a.parts;
       return pl;
     }
   }
@@ -1445,13 +1325,6 @@ cudaError_t run_plan(XPlan &pl, float *fixed, cudaStream_t stream) {
     cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void *>(xcorr_bcast_kernel));
     if (e != cudaSuccess) return e;
     xcorr_bcast_kernel<<<unsigned(pl.blocks), 32 * kBWarps, pl.smem, stream>>>(a);
-    return cudaGetLastError();
-  }
-  if (pl.kind == XKind::Pair) {
-    auto kern = pl.nslot == 2 ? xcorr_pair_kernel<2> : xcorr_pair_kernel<1>;
-    cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void *>(kern));
-    if (e != cudaSuccess) return e;
-    kern<<<unsigned(pl.blocks), kThreads, pl.smem, stream>>>(a);
     return cudaGetLastError();
   }
   auto rows_kernel = pl.chunk == 32   ? xcorr_rows_kernel<kRowsP, kRowsQ, 32>
