@@ -14,7 +14,7 @@
 // overlaps (split-row).  The same ideas, laid out for sm_103a, in kernels
 // chosen by shape:
 //
-//  rows  (any pair with 24+ rows and fewer than 32 rights per left)
+//  rows  (every shape the next two do not take)
 //    A CTA owns Q = 4 shifts dy x 8 warps x P = 8 shifts dx of one pair.
 //    The overlap rows y are the reduction: lane i of every warp takes row i
 //    of a 32-row chunk, so every lane runs the same x loop.  Rows are staged
@@ -28,7 +28,6 @@
 //    interleaved (matrix index fastest); each lane owns 4 lefts x 4 rights
 //    of one shift and walks that shift's exact overlap, so no product is
 //    wasted; warps pull shifts from a per-CTA list.
-//  direct (fewer than 24 rows, few pairs) -- bounds-checked reads through L1.
 //
 // Per lane and overlap row (rows / bcast kernels): a float4 of L feeds 4 x
 // steps; for each of the Q rows (or rights) a float4 of R enters a 12-entry
@@ -311,6 +310,7 @@ struct XArgs {
   int nxseg;      // rows kernel: x segments (split-row along x)
   int xseg;       // rows kernel: columns per x segment (multiple of 4)
   int SL, SR;     // rows kernel: shared L / R row strides in floats (% 8 == 4)
+  long long items; // rows kernels: work items (CTAs loop over them)
   int part_row;   // rows kernel: floats per partial-sum row (P * ngroups)
   float *part;    // rows kernel: partial sums (nbands * nxseg > 1)
   int nrblk;      // bcast kernel: blocks of 32 rights
@@ -441,20 +441,20 @@ __device__ __forceinline__ void issue_rows(uint32_t sbase, int S, int pad, int W
   }
 }
 
+// One work item (pair, dy block, CTA column of dx groups, band) of the
+// whole-row kernel.  The staging buffer's padding is zero on entry.
 template <int P, int Q, int CH>
-__global__ void __launch_bounds__(kThreads, 2) xcorr_rows_kernel(const XArgs a) {
+__device__ __forceinline__ void rows_item(const XArgs &a, long long item) {
   using C = ChunkGeom<Q, CH>;
-  float *sm = reinterpret_cast<float *>(g_smem4);
   const uint32_t sbase = uint32_t(__cvta_generic_to_shared(g_smem4));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = a.H, W = a.W, S = a.S;
-  int item = blockIdx.x;
-  const int band = item % a.nbands;
+  const int band = int(item % a.nbands);
   item /= a.nbands;
-  const int pair = item % (a.nl * a.nr);
+  const int pair = int(item % (a.nl * a.nr));
   item /= a.nl * a.nr;
-  const int dyb = centered(item % a.ndyb, a.ndyb);
-  const int dxs = centered(item / a.ndyb, a.nsuper);
+  const int dyb = centered(int(item % a.ndyb), a.ndyb);
+  const int dxs = centered(int(item / a.ndyb), a.nsuper);
   const int li = pair / a.nr, ri = pair - li * a.nr;
   const size_t mat = size_t(H) * W;
   const float *L = a.left + li * mat;
@@ -469,7 +469,6 @@ __global__ void __launch_bounds__(kThreads, 2) xcorr_rows_kernel(const XArgs a) 
   const int y_end = min(k.yhi, (band + 1) * a.band_rows);
   if (y_begin >= y_end) return;           // CTA-uniform: this band is empty
 
-  zero_smem(sm, C::kRows * S);            // padding columns stay zero
   float acc[Q][P];
 #pragma unroll
   for (int q = 0; q < Q; ++q)
@@ -480,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 2) xcorr_rows_kernel(const XArgs a) 
   for (int c = 0; c < nchunks; ++c) {
     const int yc = y_begin + c * CH;
     const int yr_first = yc - dy0 - (Q - 1);
-    __syncthreads();            // the buffer is free (zeroed, or chunk c-1 consumed)
+    __syncthreads();            // the buffer is free (the previous chunk consumed)
     issue_rows<Q, CH>(sbase, S, P, W, a.vec4, L, R, yc, y_end, yr_first, H);
     cp_async_commit();
     cp_async_wait_all();        // this thread's copies have landed
@@ -500,22 +499,28 @@ __global__ void __launch_bounds__(kThreads, 2) xcorr_rows_kernel(const XArgs a) 
   }
 }
 
-// Windowed variant (any width).
+template <int P, int Q, int CH>
+__global__ void __launch_bounds__(kThreads, 2) xcorr_rows_kernel(const XArgs a) {
+  zero_smem(reinterpret_cast<float *>(g_smem4), ChunkGeom<Q, CH>::kRows * a.S);   // padding
+  for (long long it = blockIdx.x; it < a.items; it += gridDim.x) rows_item<P, Q, CH>(a, it);
+}
+
+// One work item (pair, dy block, CTA column of dx groups, x segment, band)
+// of the windowed variant (any width).
 template <int P, int Q>
-__global__ void __launch_bounds__(kThreads, 2) xcorr_rows_win_kernel(const XArgs a) {
+__device__ __forceinline__ void rows_win_item(const XArgs &a, long long item) {
   using C = ChunkGeom<Q>;
   const uint32_t sbase = uint32_t(__cvta_generic_to_shared(g_smem4));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = a.H, W = a.W, SL = a.SL, SR = a.SR;
-  int item = blockIdx.x;
-  const int band = item % a.nbands;
+  const int band = int(item % a.nbands);
   item /= a.nbands;
-  const int xseg = item % a.nxseg;
+  const int xseg = int(item % a.nxseg);
   item /= a.nxseg;
-  const int pair = item % (a.nl * a.nr);
+  const int pair = int(item % (a.nl * a.nr));
   item /= a.nl * a.nr;
-  const int dyb = centered(item % a.ndyb, a.ndyb);
-  const int dxs = centered(item / a.ndyb, a.nsuper);
+  const int dyb = centered(int(item % a.ndyb), a.ndyb);
+  const int dxs = centered(int(item / a.ndyb), a.nsuper);
   const int li = pair / a.nr, ri = pair - li * a.nr;
   const size_t mat = size_t(H) * W;
   const float *L = a.left + li * mat;
@@ -555,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 2) xcorr_rows_win_kernel(const XArgs
   for (int c = 0; c < nchunks; ++c) {
     const int yc = y_begin + c * kChunk;
     const int yr_first = yc - dy0 - (Q - 1);
-    if (c > 0) __syncthreads();     // chunk c-1 is consumed
+    __syncthreads();                // the previous chunk (of this or an earlier item) is consumed
     for (int r = warp; r < C::kL + C::kR; r += kWarps) {
       if (r < C::kL) {
         const int y = yc + r;
@@ -585,6 +590,11 @@ __global__ void __launch_bounds__(kThreads, 2) xcorr_rows_win_kernel(const XArgs
     const size_t slot = ((size_t(pair) * a.ndyb + dyb) * a.nbands + band) * a.nxseg + xseg;
     a.part[(slot * Q + lane / P) * a.part_row + group * P + lane % P] = v;
   }
+}
+
+template <int P, int Q>
+__global__ void __launch_bounds__(kThreads, 2) xcorr_rows_win_kernel(const XArgs a) {
+  for (long long it = blockIdx.x; it < a.items; it += gridDim.x) rows_win_item<P, Q>(a, it);
 }
 
 // Second pass of the rows kernel: out = sum of the partial sums of the
@@ -964,135 +974,6 @@ __global__ void __launch_bounds__(32 * kTinyWarps) xcorr_tiny_kernel(const TinyA
   }
 }
 
-// ---------------------------------------------------------------------------
-// General fallback for matrices too wide to stage: a warp owns one pair group
-// x one shift dy x 8 shifts dx; lanes sum interleaved rows; operands are read
-// through L1 with bounds predicates instead of zero-padded shared rows.
-// ---------------------------------------------------------------------------
-constexpr int kDirectP = 8;
-constexpr int kDirectWarps = 4;
-
-struct DirectArgs {
-  const float *left;
-  const float *right;
-  float *out;
-  int nl, nr, H, W;
-  int pairs;
-  int G;          // pair slots per warp (power of two, 1..32)
-  int log_ph;     // log2(32 / G)
-  int groups_x;   // dx groups per output row: ceil((2W-1) / kDirectP)
-  int pair_blocks;
-  long long units;
-};
-
-__global__ void __launch_bounds__(32 * kDirectWarps) xcorr_direct_kernel(const DirectArgs a) {
-  constexpr int P = kDirectP;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long unit = (long long)blockIdx.x * kDirectWarps + warp;
-  if (unit >= a.units) return;
-  const int oh = 2 * a.H - 1, ow = 2 * a.W - 1;
-  const int gx = int(unit % a.groups_x);
-  const long long rest = unit / a.groups_x;
-  const int oy = int(rest % oh);
-  const int pb = int(rest / oh);
-  const int dy = oy - (a.H - 1);
-  const int dx0 = gx * P - (a.W - 1);
-
-  const int ph_count = 1 << a.log_ph;
-  const int g = lane >> a.log_ph, ph = lane & (ph_count - 1);
-  const int pair = pb * a.G + g;
-  const bool pair_ok = pair < a.pairs;
-  const int li = pair_ok ? pair / a.nr : 0, ri = pair_ok ? pair % a.nr : 0;
-  const size_t mat = size_t(a.H) * a.W;
-  const float *L = a.left + li * mat;
-  const float *R = a.right + ri * mat;
-  const int ylo = max(0, dy), yhi = min(a.H, a.H + dy);
-  const int xlo = max(0, dx0), xhi = min(a.W, a.W + dx0 + P - 1);
-  const int W = a.W;
-
-  float acc[P];
-#pragma unroll
-  for (int p = 0; p < P; ++p) acc[p] = 0.f;
-  if (pair_ok) {
-    for (int y = ylo + ph; y < yhi; y += ph_count) {
-      const float *Lrow = L + size_t(y) * W;
-      const float *Rrow = R + size_t(y - dy) * W;
-      // ring position of the element for shift p at x step s: (s - p) mod P
-      float buf[P];
-      buf[0] = 0.f;
-#pragma unroll
-      for (int p = 1; p < P; ++p) {
-        const int v = xlo - dx0 - p;
-        buf[P - p] = (v >= 0 && v < W) ? __ldg(Rrow + v) : 0.f;
-      }
-      int x = xlo;
-      for (; x + P <= xhi; x += P) {
-#pragma unroll
-        for (int s = 0; s < P; ++s) {
-          const int v = x + s - dx0;
-          buf[s] = v < W ? __ldg(Rrow + v) : 0.f;
-          const float l = __ldg(Lrow + x + s);
-#pragma unroll
-          for (int p = 0; p < P; ++p) acc[p] = fmaf(l, buf[(s - p + P) % P], acc[p]);
-        }
-      }
-#pragma unroll
-      for (int s = 0; s < P; ++s) {
-        if (x + s < xhi) {
-          const int v = x + s - dx0;
-          buf[s] = v < W ? __ldg(Rrow + v) : 0.f;
-          const float l = __ldg(Lrow + x + s);
-#pragma unroll
-          for (int p = 0; p < P; ++p) acc[p] = fmaf(l, buf[(s - p + P) % P], acc[p]);
-        }
-      }
-    }
-  }
-  for (int o = 1; o < ph_count; o <<= 1) {
-#pragma unroll
-    for (int p = 0; p < P; ++p) acc[p] += __shfl_xor_sync(0xffffffffu, acc[p], o);
-  }
-  if (!pair_ok) return;
-  float *orow = a.out + size_t(pair) * oh * ow + size_t(oy) * ow;
-  // every lane of the slot holds the totals; lane ph stores p = ph mod 32/G
-#pragma unroll
-  for (int p = 0; p < P; ++p) {
-    const int dx = dx0 + p;
-    if ((p & (ph_count - 1)) == ph && dx < a.W) orow[dx + a.W - 1] = acc[p];
-  }
-}
-
-int ilog2(int v) {
-  int r = 0;
-  while ((1 << (r + 1)) <= v) ++r;
-  return r;
-}
-
-cudaError_t launch_direct(const float *left, int nl, const float *right, int nr,
-                          int H, int W, float *out, cudaStream_t stream) {
-  DirectArgs a;
-  a.left = left;
-  a.right = right;
-  a.out = out;
-  a.nl = nl;
-  a.nr = nr;
-  a.H = H;
-  a.W = W;
-  a.pairs = nl * nr;
-  int G = 1;
-  while (G < 32 && (32 / G) * 4 > H) G <<= 1;
-  while (G > 1 && G / 2 >= a.pairs) G >>= 1;
-  a.G = G;
-  a.log_ph = ilog2(32 / G);
-  a.groups_x = (2 * W - 1 + kDirectP - 1) / kDirectP;
-  a.pair_blocks = (a.pairs + G - 1) / G;
-  a.units = (long long)a.pair_blocks * (2 * H - 1) * a.groups_x;
-  const long long blocks = (a.units + kDirectWarps - 1) / kDirectWarps;
-  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  xcorr_direct_kernel<<<unsigned(blocks), 32 * kDirectWarps, 0, stream>>>(a);
-  return cudaGetLastError();
-}
-
 int sm_count() { return device_sm_count(); }
 
 cudaError_t launch_tiny(const float *left, int nl, const float *right, int nr, int H,
@@ -1188,11 +1069,12 @@ cudaError_t scratch_alloc(float **ptr, size_t bytes, cudaStream_t stream) {
 // and of the bcast kernel (one CTA per SM at worst).
 constexpr size_t kMaxStageSmem = 110 * 1024;
 constexpr size_t kMaxBcastSmem = 200 * 1024;
+constexpr long long kMaxRowsGrid = 1LL << 30;   // rows kernels loop over more items
 
 namespace {
 
 // Which kernel a shape takes, its arguments and the split-row scratch it needs.
-enum class XKind { Tiny, Bcast, Rows, Direct };
+enum class XKind { Tiny, Bcast, Rows };
 
 struct XPlan {
   XKind kind;
@@ -1233,6 +1115,7 @@ XPlan make_plan(const float *left, int nl, const float *right, int nr, int H, in
             (reinterpret_cast<uintptr_t>(right) & 15) == 0) ? 1 : 0;
   a.nbands = 1;
   a.band_rows = H;
+  a.items = 0;
   a.nxseg = 1;
   a.xseg = 0;
   a.SL = a.SR = 0;
@@ -1300,13 +1183,9 @@ XPlan make_plan(const float *left, int nl, const float *right, int nr, int H, in
     a.band_rows = kBandRows;
   }
   a.part_row = kRowsP * a.ngroups;
-  const long long blocks = unbanded * a.nbands;
-  if (blocks > 0x7fffffffLL || H < 24) {
-    pl.kind = XKind::Direct;
-    return pl;
-  }
+  a.items = unbanded * a.nbands;
   pl.kind = XKind::Rows;
-  pl.blocks = blocks;
+  pl.blocks = a.items < kMaxRowsGrid ? a.items : kMaxRowsGrid;
   if (a.nbands * a.nxseg > 1)
     pl.part_bytes = size_t(pairs) * a.ndyb * a.nbands * a.nxseg * kRowsQ * a.part_row *
                     sizeof(float);
@@ -1319,8 +1198,6 @@ cudaError_t run_plan(XPlan &pl, float *fixed, cudaStream_t stream) {
   XArgs &a = pl.a;
   if (pl.kind == XKind::Tiny)
     return launch_tiny(a.left, a.nl, a.right, a.nr, a.H, a.W, a.out, stream);
-  if (pl.kind == XKind::Direct)
-    return launch_direct(a.left, a.nl, a.right, a.nr, a.H, a.W, a.out, stream);
   if (pl.kind == XKind::Bcast) {
     cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void *>(xcorr_bcast_kernel));
     if (e != cudaSuccess) return e;

@@ -75,8 +75,8 @@ def test_fixture(path):
     # row kernel, windows of three x segments (rows too wide to stage whole),
     # also with W % 4 != 0 (element-wise staging)
     (1, 1, 24, 800), (1, 1, 30, 799),
-    # too short to give lanes rows: the bounds-checked fallback kernel
-    (1, 1, 5, 400), (2, 2, 3, 700), (1, 6, 4, 520),
+    # row kernel with fewer rows than lanes (rows split along x over lanes)
+    (1, 1, 5, 400), (2, 2, 3, 700), (1, 6, 4, 520), (1, 1, 16, 1000),
 ])
 def test_shapes(nl, nr, H, W):
     check(rand(nl, H, W), rand(nr, H, W, "normal"))
