@@ -645,16 +645,11 @@ __global__ void xcorr_band_sum_kernel(const XArgs a) {
 #ifndef CORR_XC_BROWS
 #define CORR_XC_BROWS 4
 #endif
-#ifndef CORR_XC_BR
-#define CORR_XC_BR 2
-#endif
 #ifndef CORR_XC_BMINB
 #define CORR_XC_BMINB 1
 #endif
 constexpr int kBRows = CORR_XC_BROWS;     // overlap rows per chunk
-constexpr int kBRights = CORR_XC_BR;      // rights per lane
 static_assert(kBRows % 2 == 0, "two row halves");
-constexpr int kBMats = 1 + 32 * kBRights; // matrices staged per chunk
 #ifndef CORR_XC_BPAIRS
 #define CORR_XC_BPAIRS 8
 #endif
@@ -663,15 +658,18 @@ constexpr int kBPairs = CORR_XC_BPAIRS;          // dx-group pairs per CTA
 constexpr int kBParts = kBWarps / kBPairs;       // row parts of a chunk
 static_assert(kBRows % kBParts == 0, "whole rows per row part");
 
-__device__ __forceinline__ int bcast_slab(int S) { return kBRows * S + 4; }
-__device__ __forceinline__ int bcast_buf(int S) {
-  return kBRows * S + 32 * kBRights * bcast_slab(S);
+// BR rights per lane (2, or 1 when that still leaves fewer CTAs than two
+// per SM): 1 + 32 BR matrices staged per chunk.
+__host__ __device__ inline int bcast_slab(int S) { return kBRows * S + 4; }
+__host__ __device__ inline int bcast_buf(int S, int BR) {
+  return kBRows * S + 32 * BR * bcast_slab(S);
 }
 
 // Issue one chunk: left rows yc .. yc+kBRows-1 (zero past yhi) and, for each
-// of the CTA's 32*kBRights rights, rows yc-dy .. (zero past nr or past yhi).
+// of the CTA's 32*BR rights, rows yc-dy .. (zero past nr or past yhi).
 // A row's addresses are formed once: a row of n copies goes to the smallest
 // of 4, 8, 16 or 32 lanes that covers it (lanes along the row).
+template <int BR>
 __device__ __forceinline__ void issue_bchunk(const XArgs &a, uint32_t sbase, int buf,
                                              const float *L, int r_first, int yc,
                                              int yhi, int dy) {
@@ -684,7 +682,7 @@ __device__ __forceinline__ void issue_bchunk(const XArgs &a, uint32_t sbase, int
   const int lpr = n <= 4 ? 4 : n <= 8 ? 8 : n <= 16 ? 16 : 32;   // lanes per row
   const int rpw = 32 / lpr;                     // rows per warp step
   const int sub = lane / lpr, col0 = lane % lpr;
-  for (int row = warp * rpw + sub; row < kBMats * kBRows; row += kBWarps * rpw) {
+  for (int row = warp * rpw + sub; row < (1 + 32 * BR) * kBRows; row += kBWarps * rpw) {
     const int m = row / kBRows, r = row % kBRows;
     const int y = yc + r;
     bool ok = y < yhi;
@@ -722,7 +720,9 @@ __device__ __forceinline__ XGroup make_xgroup(int W, int dx0) {
 }
 
 
+template <int BR>
 __global__ void __launch_bounds__(32 * kBWarps, CORR_XC_BMINB) xcorr_bcast_kernel(const XArgs a) {
+  constexpr int kBRights = BR;
   const uint32_t sbase = uint32_t(__cvta_generic_to_shared(g_smem4));
   float *sm = reinterpret_cast<float *>(g_smem4);
   const int warp_id = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -751,7 +751,7 @@ __global__ void __launch_bounds__(32 * kBWarps, CORR_XC_BMINB) xcorr_bcast_kerne
   const XGroup xb = make_xgroup(W, a.dxbase + gB * kP);
   const int r_first = rb * 32 * kBRights;   // lane owns rights r_first + lane + 32 j
 
-  const int bufn = bcast_buf(S), slab = bcast_slab(S);
+  const int bufn = bcast_buf(S, BR), slab = bcast_slab(S);
   zero_smem(sm, 2 * bufn);
   __syncthreads();
   float accA[kBRights][kP], accB[kBRights][kP];
@@ -761,7 +761,7 @@ __global__ void __launch_bounds__(32 * kBWarps, CORR_XC_BMINB) xcorr_bcast_kerne
     for (int p = 0; p < kP; ++p) accA[j][p] = accB[j][p] = 0.f;
 
   const int nchunks = (yhi - ylo + kBRows - 1) / kBRows;
-  if (nchunks > 0) issue_bchunk(a, sbase, 0, L, r_first, ylo, yhi, dy);
+  if (nchunks > 0) issue_bchunk<BR>(a, sbase, 0, L, r_first, ylo, yhi, dy);
   cp_async_commit();
   for (int c = 0; c < nchunks; ++c) {
     const int yc = ylo + c * kBRows;
@@ -769,7 +769,7 @@ __global__ void __launch_bounds__(32 * kBWarps, CORR_XC_BMINB) xcorr_bcast_kerne
     cp_async_wait_all();
     __syncthreads();
     if (c + 1 < nchunks) {
-      issue_bchunk(a, sbase, ((c + 1) & 1) * bufn, L, r_first, yc + kBRows, yhi, dy);
+      issue_bchunk<BR>(a, sbase, ((c + 1) & 1) * bufn, L, r_first, yc + kBRows, yhi, dy);
       cp_async_commit();
     }
     if (!gp_ok) continue;
@@ -1083,6 +1083,7 @@ struct XPlan {
   long long blocks;      // grid of the pair / rows kernel
   size_t part_bytes;     // rows kernel with several bands: scratch bytes
   int chunk;             // rows kernel: 32 / 16 (whole rows) or 0 (windows)
+  int bcast_rights;      // bcast kernel: rights per lane (1 or 2)
 };
 
 XPlan make_plan(const float *left, int nl, const float *right, int nr, int H, int W,
@@ -1092,6 +1093,7 @@ XPlan make_plan(const float *left, int nl, const float *right, int nr, int H, in
   pl.blocks = 0;
   pl.part_bytes = 0;
   pl.chunk = 0;
+  pl.bcast_rights = 2;
   const long long pairs = (long long)nl * nr;
   XArgs &a = pl.a;
   a.left = left;
@@ -1127,14 +1129,34 @@ XPlan make_plan(const float *left, int nl, const float *right, int nr, int H, in
   // bcast kernel: at least 32 rights per left, rows of 8+ floats, and two
   // chunk buffers fit
   {
-    const size_t buf_floats =
-        size_t(kBRows) * a.S + 32 * kBRights * (size_t(kBRows) * a.S + 4);
+    // rights per lane: estimated time = max(executed work / SMs, largest
+    // CTA) (work in overlap rows x rights per lane, padding rights of a
+    // partial block included), one right per lane counted 1.2x slower per
+    // row (two loads feed 32 FMAs instead of three feeding 64)
+    int br = 2;
+    {
+      const int ngp0 = (a.ngroups + 1) / 2;
+      const double npb = (ngp0 + kBPairs - 1) / kBPairs, sms = sm_count();
+      const double rows = double(H) * H;   // sum over dy of the overlap rows
+      auto est = [&](int b) {
+        const double nrblk = (nr + 32 * b - 1) / (32 * b);
+        const double total = double(nl) * nrblk * npb * rows * b;
+        const double t = total / sms > double(H) * b ? total / sms : double(H) * b;
+        return b == 1 ? 1.2 * t : t;
+      };
+      if (est(1) < est(2)) br = 1;
+    }
+    pl.bcast_rights = br;
+    const size_t buf_floats = size_t(bcast_buf(a.S, br));
     const size_t bsmem = 2 * buf_floats * sizeof(float);
     const int ngp = (a.ngroups + 1) / 2;
-    a.nrblk = (nr + 32 * kBRights - 1) / (32 * kBRights);
+    a.nrblk = (nr + 32 * br - 1) / (32 * br);
     a.npairblk = (ngp + kBPairs - 1) / kBPairs;
     const long long bblocks = (long long)nl * a.nrblk * a.npairblk * (2LL * H - 1);
-    if (nr >= 32 && W >= 8 && bsmem <= kMaxBcastSmem && bblocks <= 0x7fffffffLL) {
+#ifndef CORR_XC_BCAST
+#define CORR_XC_BCAST 1
+#endif
+    if (CORR_XC_BCAST && nr >= 32 && W >= 8 && bsmem <= kMaxBcastSmem && bblocks <= 0x7fffffffLL) {
       pl.kind = XKind::Bcast;
       pl.smem = bsmem;
       pl.blocks = bblocks;
@@ -1199,9 +1221,10 @@ cudaError_t run_plan(XPlan &pl, float *fixed, cudaStream_t stream) {
   if (pl.kind == XKind::Tiny)
     return launch_tiny(a.left, a.nl, a.right, a.nr, a.H, a.W, a.out, stream);
   if (pl.kind == XKind::Bcast) {
-    cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void *>(xcorr_bcast_kernel));
+    auto kern = pl.bcast_rights == 1 ? xcorr_bcast_kernel<1> : xcorr_bcast_kernel<2>;
+    cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void *>(kern));
     if (e != cudaSuccess) return e;
-    xcorr_bcast_kernel<<<unsigned(pl.blocks), 32 * kBWarps, pl.smem, stream>>>(a);
+    kern<<<unsigned(pl.blocks), 32 * kBWarps, pl.smem, stream>>>(a);
     return cudaGetLastError();
   }
   auto rows_kernel = pl.chunk == 32   ? xcorr_rows_kernel<kRowsP, kRowsQ, 32>
