@@ -1103,7 +1103,10 @@ XPlan make_plan(const float *left, int nl, const float *right, int nr, int H, in
   a.nr = nr;
   a.H = H;
   a.W = W;
-  if (H * W <= 256 && pairs >= 64) {
+#ifndef CORR_XC_TINY
+#define CORR_XC_TINY 1
+#endif
+  if (CORR_XC_TINY && H * W <= 256 && pairs >= 64) {
     pl.kind = XKind::Tiny;
     return pl;
   }
