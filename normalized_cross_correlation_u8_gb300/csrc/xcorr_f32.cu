@@ -39,6 +39,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <stdlib.h>
+
 #include <mutex>
 #include <utility>
 
@@ -443,8 +445,8 @@ __device__ __forceinline__ void issue_rows(uint32_t sbase, int S, int pad, int W
 
 // One work item (pair, dy block, CTA column of dx groups, band) of the
 // whole-row kernel.  The staging buffer's padding is zero on entry.
-template <int P, int Q, int CH>
-__device__ __forceinline__ void rows_item(const XArgs &a, long long item) {
+template <int P, int Q, int CH, typename Index>
+__device__ __forceinline__ void rows_item(const XArgs &a, Index item) {
   using C = ChunkGeom<Q, CH>;
   const uint32_t sbase = uint32_t(__cvta_generic_to_shared(g_smem4));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -499,16 +501,23 @@ __device__ __forceinline__ void rows_item(const XArgs &a, long long item) {
   }
 }
 
-template <int P, int Q, int CH>
+// LOOP = false: one item per CTA (grid = items < 2^30, 32-bit indices);
+// LOOP = true: CTAs loop over more items than a grid holds.
+template <int P, int Q, int CH, bool LOOP>
 __global__ void __launch_bounds__(kThreads, 2) xcorr_rows_kernel(const XArgs a) {
   zero_smem(reinterpret_cast<float *>(g_smem4), ChunkGeom<Q, CH>::kRows * a.S);   // padding
-  for (long long it = blockIdx.x; it < a.items; it += gridDim.x) rows_item<P, Q, CH>(a, it);
+  if (LOOP) {
+    for (long long it = blockIdx.x; it < a.items; it += gridDim.x)
+      rows_item<P, Q, CH, long long>(a, it);
+  } else {
+    rows_item<P, Q, CH, int>(a, int(blockIdx.x));
+  }
 }
 
 // One work item (pair, dy block, CTA column of dx groups, x segment, band)
 // of the windowed variant (any width).
-template <int P, int Q>
-__device__ __forceinline__ void rows_win_item(const XArgs &a, long long item) {
+template <int P, int Q, typename Index>
+__device__ __forceinline__ void rows_win_item(const XArgs &a, Index item) {
   using C = ChunkGeom<Q>;
   const uint32_t sbase = uint32_t(__cvta_generic_to_shared(g_smem4));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -592,9 +601,14 @@ __device__ __forceinline__ void rows_win_item(const XArgs &a, long long item) {
   }
 }
 
-template <int P, int Q>
+template <int P, int Q, bool LOOP>
 __global__ void __launch_bounds__(kThreads, 2) xcorr_rows_win_kernel(const XArgs a) {
-  for (long long it = blockIdx.x; it < a.items; it += gridDim.x) rows_win_item<P, Q>(a, it);
+  if (LOOP) {
+    for (long long it = blockIdx.x; it < a.items; it += gridDim.x)
+      rows_win_item<P, Q, long long>(a, it);
+  } else {
+    rows_win_item<P, Q, int>(a, int(blockIdx.x));
+  }
 }
 
 // Second pass of the rows kernel: out = sum of the partial sums of the
@@ -1071,6 +1085,19 @@ constexpr size_t kMaxStageSmem = 110 * 1024;
 constexpr size_t kMaxBcastSmem = 200 * 1024;
 constexpr long long kMaxRowsGrid = 1LL << 30;   // rows kernels loop over more items
 
+// Grid cap of the rows kernels: kMaxRowsGrid, or the positive integer in
+// the environment variable CORR_XCORR_MAX_GRID (read on every call; lets a
+// test run the item loop on ordinary shapes).
+long long rows_grid_cap() {
+  const char *v = getenv("CORR_XCORR_MAX_GRID");
+  if (v && *v) {
+    char *end = nullptr;
+    const long long n = strtoll(v, &end, 10);
+    if (end && *end == '\0' && n > 0 && n < kMaxRowsGrid) return n;
+  }
+  return kMaxRowsGrid;
+}
+
 namespace {
 
 // Which kernel a shape takes, its arguments and the split-row scratch it needs.
@@ -1210,7 +1237,8 @@ XPlan make_plan(const float *left, int nl, const float *right, int nr, int H, in
   a.part_row = kRowsP * a.ngroups;
   a.items = unbanded * a.nbands;
   pl.kind = XKind::Rows;
-  pl.blocks = a.items < kMaxRowsGrid ? a.items : kMaxRowsGrid;
+  const long long max_grid = rows_grid_cap();
+  pl.blocks = a.items < max_grid ? a.items : max_grid;
   if (a.nbands * a.nxseg > 1)
     pl.part_bytes = size_t(pairs) * a.ndyb * a.nbands * a.nxseg * kRowsQ * a.part_row *
                     sizeof(float);
@@ -1230,9 +1258,14 @@ cudaError_t run_plan(XPlan &pl, float *fixed, cudaStream_t stream) {
     kern<<<unsigned(pl.blocks), 32 * kBWarps, pl.smem, stream>>>(a);
     return cudaGetLastError();
   }
-  auto rows_kernel = pl.chunk == 32   ? xcorr_rows_kernel<kRowsP, kRowsQ, 32>
-                     : pl.chunk == 16 ? xcorr_rows_kernel<kRowsP, kRowsQ, 16>
-                                      : xcorr_rows_win_kernel<kRowsP, kRowsQ>;
+  const bool loop = a.items > pl.blocks;
+  auto rows_kernel =
+      loop ? (pl.chunk == 32   ? xcorr_rows_kernel<kRowsP, kRowsQ, 32, true>
+              : pl.chunk == 16 ? xcorr_rows_kernel<kRowsP, kRowsQ, 16, true>
+                               : xcorr_rows_win_kernel<kRowsP, kRowsQ, true>)
+           : (pl.chunk == 32   ? xcorr_rows_kernel<kRowsP, kRowsQ, 32, false>
+              : pl.chunk == 16 ? xcorr_rows_kernel<kRowsP, kRowsQ, 16, false>
+                               : xcorr_rows_win_kernel<kRowsP, kRowsQ, false>);
   cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void *>(rows_kernel));
   if (e != cudaSuccess) return e;
   const bool banded = a.nbands * a.nxseg > 1;

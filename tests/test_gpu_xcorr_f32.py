@@ -141,3 +141,12 @@ def test_workload_one_to_many_full():
 def test_workload_n_to_m_full():
     w = wl.xcorr_n_to_m()
     check(w.left, w.right)
+
+
+@pytest.mark.parametrize("nl,nr,H,W", [(1, 2, 130, 257), (1, 1, 24, 800), (2, 2, 3, 700)])
+def test_rows_kernels_item_loop(nl, nr, H, W, monkeypatch):
+    """The rows kernels' work-item loop (taken by grids larger than 2^30
+    CTAs) on ordinary shapes: the library caps the grid at
+    CORR_XCORR_MAX_GRID, so each CTA loops over several items."""
+    monkeypatch.setenv("CORR_XCORR_MAX_GRID", "37")
+    check(rand(nl, H, W), rand(nr, H, W, "normal"))
