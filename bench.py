@@ -296,7 +296,8 @@ def run_ours(args, world, rank, local):
     sm_mhz = clocks["sm_mhz"] if clocks else SM_MAX_MHZ_NOMINAL
     dp4a_peak = sms * DP4A_PER_SM_CLK * SM_MAX_MHZ_NOMINAL * 1e6
     achieved = w.offsets * dp4a_per_offset(w) / avg_launch_s
-    ncc_src = [os.path.join(ROOT, "normalized_cross_correlation_u8_gb300", "csrc", "ncc_u8.cu")]
+    ncc_src = [os.path.join(ROOT, "normalized_cross_correlation_u8_gb300", "csrc", f)
+               for f in ("ncc_u8.cu", "ncc_u8_kernels.cuh")]
     roofline = {
         "bound": "alu", "kernel": "ncc_u8_fixed_kernel (unsigned dp4a issue)",
         "achieved": achieved / 1e12, "peak": dp4a_peak / 1e12, "unit": "Tdp4a/s",

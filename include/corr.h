@@ -51,8 +51,8 @@ extern "C" {
  *
  *   image     device, w*h bytes, row-major, row pitch w bytes, any alignment
  *             (16- or 8-byte aligned rows are staged with vector loads).
- *             Templates up to 64 wide take the tiled fast kernel; wider ones a
- *             general kernel with the same results.
+ *             Templates up to 128 wide take the tiled fast kernel; wider ones
+ *             a general kernel with the same results.
  *   w, h      image width and height in pixels, > 0.
  *   tmpl      device, wt*ht bytes, row-major, pitch wt.
  *   wt, ht    template size, 0 < wt <= w, 0 < ht <= h; wt must be a

@@ -1,0 +1,534 @@
+// ncc_u8_kernels.cuh -- 8-bit normalized cross-correlation on sm_103a:
+// kernels and launch helpers shared by ncc_u8.cu and ncc_u8_wide.cu.
+//
+// Method (The CUDA Handbook, ch. 15 "Image Processing: Normalized
+// Correlation", section 15.5 "Instruction-Level Parallelism and DP4A"):
+// four pixels are packed into one 32-bit word and each of the three sums
+// advances by one *unsigned* __dp4a per word (SumI against 0x01010101,
+// SumISq against the word itself, SumIT against the packed template word).
+// Consecutive output columns slide the window by one byte, so a thread's
+// window words are cut out of two aligned image words with __funnelshift_r;
+// the template, whose width is a multiple of four, packs directly.  Several
+// independent output columns (and rows) per thread keep many accumulation
+// chains in flight (the section's instruction-level parallelism).
+//
+// GB300 layout of the work (fast path: wt a multiple of 4 up to 64, any
+// image alignment; wider templates take the general path below):
+//   * a CTA owns 128 output columns x TY output rows; it copies the image
+//     tile plus its halo (TY+ht-1 rows x 128+wt+8 bytes) into shared memory
+//     with independent 16-byte vector loads (one memory latency per tile,
+//     out-of-image bytes zero), and stages the template as packed words;
+//   * each half-warp owns R output rows, each lane 8 adjacent columns whose
+//     words start 8-byte aligned; the half-warp walks its R+ht-1 tile rows
+//     once, cutting each row into the lane's 8 windows with funnel shifts
+//     (windows of columns 4..7 at word i equal those of columns 0..3 at word
+//     i+1, so 3 shifts per word serve 8 columns) and pairing it with
+//     template row k-r for each of its R output rows;
+//   * the template row is read as warp-uniform 16-byte shared broadcasts;
+//     each CTA also reduces SumT / SumTSq from it;
+//   * the epilogue forms N*SumIT - SumI*SumT and N*SumISq - SumI^2 exactly in
+//     64-bit integers before the single-precision ratio.
+// Measured on GB300 (R = 1, 2-warp CTAs): the unsigned dp4a pipe (64 per SM
+// per clock) is 73-91 % busy with dp4a depending on image and template size.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <array>
+#include <type_traits>
+#include <utility>
+
+#include "internal.cuh"
+
+namespace corr {
+namespace ncc {
+
+constexpr int kCols = 8;                   // output columns per lane
+constexpr int kUnitCols = 32 * kCols;      // output columns per warp unit (general path)
+constexpr int kHalfUnitCols = 16 * kCols;  // output columns per warp unit (fast path)
+// Warps per CTA and output rows per half-warp (compile-time tuning knobs).
+#ifndef CORR_NCC_WARPS
+#define CORR_NCC_WARPS 2
+#endif
+#ifndef CORR_NCC_ROWS
+#define CORR_NCC_ROWS 1
+#endif
+#ifndef CORR_NCC_MINB
+#define CORR_NCC_MINB 1
+#endif
+#ifndef CORR_NCC_KSPLIT
+#define CORR_NCC_KSPLIT 2
+#endif
+constexpr int kWarpsPerCta = CORR_NCC_WARPS;
+constexpr int kThreads = 32 * kWarpsPerCta;
+// Fast path: the template rows of a tile are split into kSplit ranges, one
+// per group of kWarpsPerCta warps; the groups' partial sums are added in
+// shared memory (integer sums: exact in any order).
+constexpr int kSplit = CORR_NCC_KSPLIT;
+constexpr int kFixedThreads = kThreads * kSplit;
+constexpr uint32_t kOnes = 0x01010101u;
+constexpr int kStageBatch = 4;       // tile chunks per thread loaded ahead of the template
+
+struct NccArgs {
+  const uint8_t *image;
+  const uint8_t *tmpl;
+  uint32_t *sums;
+  float *coef;
+  size_t plane;      // ow * oh
+  int w, h, wt, ht;
+  int wtw;           // template words per row (wt / 4)
+  int wtp;           // shared-memory template row stride in words (multiple of 4)
+  int ow, oh;
+  int tiles_x;       // units across a row of outputs
+  int units;         // warp units (fast path: 128 cols x 2R rows)
+};
+
+__device__ __forceinline__ uint32_t fshr(uint32_t lo, uint32_t hi, int bytes) {
+  return __funnelshift_r(lo, hi, 8 * bytes);
+}
+
+// Four bytes of image row `row` starting at byte `off`; bytes at or past w
+// read as zero (they only ever feed columns past the last valid offset).
+__device__ __forceinline__ uint32_t load_word_bytes(const uint8_t *row, int off,
+                                                    int w) {
+  uint32_t v = 0;
+#pragma unroll
+  for (int b = 0; b < 4; ++b)
+    if (off + b < w) v |= uint32_t(__ldg(row + off + b)) << (8 * b);
+  return v;
+}
+
+// Stage the template into shared memory as 32-bit words (row stride wtp,
+// zero padded) and reduce SumT, SumTSq over the CTA.
+__device__ __forceinline__ void stage_template(const NccArgs &a, uint32_t *tmpl_s,
+                                               uint32_t *red, uint32_t &sum_t,
+                                               uint32_t &sum_t_sq) {
+  if (threadIdx.x < 2) red[threadIdx.x] = 0;
+  __syncthreads();
+  const bool aligned4 = (reinterpret_cast<uintptr_t>(a.tmpl) & 3) == 0;
+  uint32_t s = 0, q = 0;
+  const int total = a.ht * a.wtp;
+  for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
+    const int j = idx / a.wtp, i = idx - j * a.wtp;
+    uint32_t v = 0;
+    if (i < a.wtw) {
+      const int byte = j * a.wt + 4 * i;
+      if (aligned4) {
+        v = __ldg(reinterpret_cast<const uint32_t *>(a.tmpl + byte));
+      } else {
+#pragma unroll
+        for (int b = 0; b < 4; ++b) v |= uint32_t(__ldg(a.tmpl + byte + b)) << (8 * b);
+      }
+    }
+    tmpl_s[idx] = v;
+    s = __dp4a(v, kOnes, s);
+    q = __dp4a(v, v, q);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    s += __shfl_xor_sync(0xffffffffu, s, o);
+    q += __shfl_xor_sync(0xffffffffu, q, o);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    atomicAdd(&red[0], s);
+    atomicAdd(&red[1], q);
+  }
+  __syncthreads();
+  sum_t = red[0];
+  sum_t_sq = red[1];
+}
+
+// Three unsigned dp4a per window: the section's inner step.
+template <int R>
+__device__ __forceinline__ void accum_window(uint32_t (&sI)[R][kCols],
+                                             uint32_t (&sQ)[R][kCols],
+                                             uint32_t (&sT)[R][kCols], int r,
+                                             int c, uint32_t win, uint32_t tw) {
+  sI[r][c] = __dp4a(win, kOnes, sI[r][c]);
+  sQ[r][c] = __dp4a(win, win, sQ[r][c]);
+  sT[r][c] = __dp4a(win, tw, sT[r][c]);
+}
+
+// Write the sums and the coefficient of one lane's R x 8 block.  The
+// numerator and the window variance term are exact 64-bit integers; the
+// ratio is num * rsqrt(dI) * rsqrt(dT) in single precision (a few ulp of
+// |coef| <= 1, far inside the 1e-5 bound).  rs_t = rsqrt(dT) is per template.
+template <int R>
+__device__ __forceinline__ void epilogue(const NccArgs &a, int x0, int y0,
+                                         const uint32_t (&sI)[R][kCols],
+                                         const uint32_t (&sQ)[R][kCols],
+                                         const uint32_t (&sT)[R][kCols],
+                                         uint32_t sum_t, float rs_t) {
+  const int64_t n = int64_t(a.wt) * a.ht;
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int y = y0 + r;
+    if (y >= a.oh) break;
+#pragma unroll
+    for (int c = 0; c < kCols; ++c) {
+      const int x = x0 + c;
+      if (x >= a.ow) break;
+      const size_t o = size_t(y) * a.ow + x;
+      if (a.sums) {
+        a.sums[o] = sI[r][c];
+        a.sums[a.plane + o] = sQ[r][c];
+        a.sums[2 * a.plane + o] = sT[r][c];
+      }
+      if (a.coef) {
+        const int64_t si = sI[r][c];
+        const int64_t num = n * int64_t(sT[r][c]) - si * int64_t(sum_t);
+        const int64_t d_i = n * int64_t(sQ[r][c]) - si * si;
+        a.coef[o] = d_i > 0 ? float(num) * rsqrtf(float(d_i)) * rs_t : 0.f;
+      }
+    }
+  }
+}
+
+// rsqrt of the template variance term N*SumTSq - SumT^2, or 0 for a flat
+// template (which makes every coefficient 0).
+__device__ __forceinline__ float template_rsqrt(const NccArgs &a, uint32_t sum_t,
+                                                uint32_t sum_t_sq) {
+  const int64_t n = int64_t(a.wt) * a.ht;
+  const int64_t d_t = n * int64_t(sum_t_sq) - int64_t(sum_t) * int64_t(sum_t);
+  return d_t > 0 ? rsqrtf(float(d_t)) : 0.f;
+}
+
+// One image row (tile-relative index rel = k - y0) against template rows
+// rel - r for the R output rows r of the unit; `mask` selects the rows r for
+// which 0 <= rel - r < ht (all of them when FULL).
+// Words of one staged image row a lane holds: the WT + 1 words its 8
+// windows reach, read as 8-byte pairs.
+template <int WT>
+struct RowWords {
+  static constexpr int kPairs = (WT + 3) / 2;
+  static constexpr int kWords = 2 * kPairs;
+};
+
+template <int R, int WT, bool FULL>
+__device__ __forceinline__ void row_fixed(const uint32_t (&wv)[RowWords<WT>::kWords],
+                                          const uint32_t *tmpl_s, int rel,
+                                          unsigned mask, uint32_t (&sI)[R][kCols],
+                                          uint32_t (&sQ)[R][kCols],
+                                          uint32_t (&sT)[R][kCols]) {
+  constexpr int WTP = (WT + 3) & ~3;
+#pragma unroll
+  for (int ib = 0; ib < WT; ib += 4) {
+    uint4 tq[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+      if (FULL || ((mask >> r) & 1u))
+        tq[r] = *reinterpret_cast<const uint4 *>(tmpl_s + (rel - r) * WTP + ib);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int i = ib + m;
+      if (i >= WT) break;
+      uint32_t win[kCols];
+#pragma unroll
+      for (int c = 0; c < kCols; ++c) {
+        const int k = i + (c >> 2), s = c & 3;
+        win[c] = s == 0 ? wv[k] : fshr(wv[k], wv[k + 1], s);
+      }
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        if (!(FULL || ((mask >> r) & 1u))) continue;
+        const uint32_t tw = m == 0 ? tq[r].x : m == 1 ? tq[r].y : m == 2 ? tq[r].z : tq[r].w;
+#pragma unroll
+        for (int c = 0; c < kCols; ++c) accum_window<R>(sI, sQ, sT, r, c, win[c], tw);
+      }
+    }
+  }
+}
+
+// Fast path: template width WT words known at compile time, any image
+// alignment (the staging unit VB follows it).
+//
+// A CTA owns a tile of 128 output columns x TY = 2*R*kWarpsPerCta output
+// rows.  It first copies the image tile plus halo -- TY+ht-1 rows of
+// 128+4*WT+8 bytes (rounded to 16) -- into shared memory with 16-byte (or
+// 8-byte) vector loads that are all independent, so the tile costs one
+// memory latency instead of one per image row.  Then half-warp h of warp w
+// takes output rows w*2R + h*R .. +R-1 (each lane 8 adjacent columns) and
+// walks its R+ht-1 tile rows from shared memory; each row is cut into
+// windows once and paired with template row k-r for each of its R rows.
+// Words of the next tile row are read while the current one is consumed.
+template <int WT>
+struct TileGeom {
+  static constexpr int kRowBytes = (kHalfUnitCols + 4 * WT + 8 + 15) & ~15;
+};
+
+// Tile staging unit by image alignment: VB = 16 or 8 when the image pointer
+// and width are that aligned (whole vector loads, a chunk lies wholly inside
+// or outside the image), VB = 1 otherwise (4-byte chunks assembled from byte
+// loads, each byte checked against w).
+template <int VB>
+struct StageChunk {
+  using type = typename std::conditional<VB == 16, uint4,
+               typename std::conditional<VB == 8, uint2, uint32_t>::type>::type;
+  static constexpr int kBytes = int(sizeof(type));
+};
+
+template <int R, int WT, int VB>
+__global__ void __launch_bounds__(kFixedThreads, CORR_NCC_MINB)
+    ncc_u8_fixed_kernel(const NccArgs a) {
+  constexpr int WTP = (WT + 3) & ~3;
+  constexpr int RB = TileGeom<WT>::kRowBytes;
+  constexpr int TY = 2 * R * kWarpsPerCta;
+  extern __shared__ uint4 smem_u4[];
+  uint32_t *tmpl_s = reinterpret_cast<uint32_t *>(smem_u4);
+  uint8_t *tile = reinterpret_cast<uint8_t *>(smem_u4) + size_t(a.ht) * WTP * 4;
+  __shared__ uint32_t red[2];
+
+  const int tx = blockIdx.x % a.tiles_x, ty = blockIdx.x / a.tiles_x;
+  const int xt = tx * kHalfUnitCols, yt = ty * TY;
+  const int trows = min(TY + a.ht - 1, a.h - yt);   // tile rows inside the image
+
+  // ---- tile + halo -> shared memory (out-of-image bytes become zero) ----
+  // The first kStageBatch chunks per thread are loaded into registers and
+  // the template is staged while they are in flight, so a tile costs about
+  // one memory latency; taller tiles copy the rest afterwards.
+  using Chunk = typename StageChunk<VB>::type;
+  constexpr int CB = StageChunk<VB>::kBytes;          // bytes per chunk
+  constexpr int C = RB / CB;                          // chunks per tile row
+  const int nchunks = trows * C;
+  auto chunk_load = [&](int i) {
+    Chunk v;
+    memset(&v, 0, sizeof(v));
+    const int r = i / C, c = i - r * C;
+    const int x = xt + CB * c;
+    const uint8_t *row = a.image + size_t(yt + r) * a.w;
+    if constexpr (VB == 1) {
+#pragma unroll
+      for (int b = 0; b < 4; ++b)
+        if (x + b < a.w) v |= uint32_t(__ldg(row + x + b)) << (8 * b);
+    } else {
+      if (x < a.w) v = __ldg(reinterpret_cast<const Chunk *>(row + x));   // w % CB == 0
+    }
+    return v;
+  };
+  auto chunk_store = [&](int i, const Chunk &v) {
+    const int r = i / C, c = i - r * C;
+    *reinterpret_cast<Chunk *>(tile + r * RB + CB * c) = v;
+  };
+  Chunk first[kStageBatch];
+#pragma unroll
+  for (int k = 0; k < kStageBatch; ++k) {
+    const int i = threadIdx.x + k * kFixedThreads;
+    if (i < nchunks) first[k] = chunk_load(i);
+  }
+  uint32_t sum_t, sum_t_sq;
+  stage_template(a, tmpl_s, red, sum_t, sum_t_sq);   // ends with __syncthreads
+#pragma unroll
+  for (int k = 0; k < kStageBatch; ++k) {
+    const int i = threadIdx.x + k * kFixedThreads;
+    if (i < nchunks) chunk_store(i, first[k]);
+  }
+  for (int i = threadIdx.x + kStageBatch * kFixedThreads; i < nchunks; i += kFixedThreads)
+    chunk_store(i, chunk_load(i));
+  __syncthreads();
+
+  const int warp_id = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = warp_id % kWarpsPerCta;            // row group of the tile
+  const int ks = warp_id / kWarpsPerCta;              // template-row range
+  const int j_lo = ks * a.ht / kSplit, j_hi = (ks + 1) * a.ht / kSplit;
+  const int half = lane >> 4, hl = lane & 15;
+  const int yr0 = warp * 2 * R + half * R;           // tile-relative first row
+  const int x0 = xt + hl * kCols;
+  const int y0 = yt + yr0;
+
+  uint32_t sI[R][kCols], sQ[R][kCols], sT[R][kCols];
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+#pragma unroll
+    for (int c = 0; c < kCols; ++c) sI[r][c] = sQ[r][c] = sT[r][c] = 0;
+
+  // Warp-uniform row count: rows of the lower half past the tile's rows in
+  // the image read the last staged row (their outputs are past oh and are
+  // never stored).
+  const int nrows = max(0, min(R + a.ht - 1, trows - warp * 2 * R));
+  const uint8_t *lane_base = tile + hl * kCols;
+  constexpr int NW = RowWords<WT>::kWords;
+  auto load_row = [&](int rel, uint32_t (&dst)[NW]) {
+    const int r = min(yr0 + rel, trows - 1);
+    const uint8_t *row = lane_base + r * RB;
+#pragma unroll
+    for (int p = 0; p < RowWords<WT>::kPairs; ++p) {
+      const uint2 v = *reinterpret_cast<const uint2 *>(row + 8 * p);
+      dst[2 * p] = v.x;
+      dst[2 * p + 1] = v.y;
+    }
+  };
+  // tile row yr0 + rel meets template row rel - r for output row r; this
+  // warp group takes template rows [j_lo, j_hi)
+  auto process = [&](const uint32_t (&wv)[NW], int rel) {
+    if (rel - (R - 1) >= j_lo && rel <= j_hi - 1) {
+      row_fixed<R, WT, true>(wv, tmpl_s, rel, 0u, sI, sQ, sT);
+    } else {
+      unsigned mask = 0;
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+        if (rel - r >= j_lo && rel - r < j_hi) mask |= 1u << r;
+      row_fixed<R, WT, false>(wv, tmpl_s, rel, mask, sI, sQ, sT);
+    }
+  };
+  const int rel_end = min(nrows, j_hi + R - 1);
+  uint32_t wa[NW], wb[NW];
+  if (j_lo < rel_end) load_row(j_lo, wa);
+  for (int rel = j_lo; rel < rel_end; rel += 2) {
+    if (rel + 1 < rel_end) load_row(rel + 1, wb);
+    process(wa, rel);
+    if (rel + 1 >= rel_end) break;
+    if (rel + 2 < rel_end) load_row(rel + 2, wa);
+    process(wb, rel + 1);
+  }
+  if (kSplit > 1) {
+    // groups 1.. hand their partial sums to group 0 through shared memory
+    constexpr int E = 3 * R * kCols;
+    uint32_t *part = reinterpret_cast<uint32_t *>(tile + size_t(TY + a.ht - 1) * RB);
+    __syncthreads();                        // tile reads done; part may be written
+    if (ks > 0) {
+      uint32_t *dst = part + ((ks - 1) * kWarpsPerCta + warp) * E * 32 + lane;
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int c = 0; c < kCols; ++c) {
+          const int e = (r * kCols + c) * 3;
+          dst[(e + 0) * 32] = sI[r][c];
+          dst[(e + 1) * 32] = sQ[r][c];
+          dst[(e + 2) * 32] = sT[r][c];
+        }
+    }
+    __syncthreads();
+    if (ks > 0) return;
+#pragma unroll 1
+    for (int g = 1; g < kSplit; ++g) {
+      const uint32_t *src = part + ((g - 1) * kWarpsPerCta + warp) * E * 32 + lane;
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int c = 0; c < kCols; ++c) {
+          const int e = (r * kCols + c) * 3;
+          sI[r][c] += src[(e + 0) * 32];
+          sQ[r][c] += src[(e + 1) * 32];
+          sT[r][c] += src[(e + 2) * 32];
+        }
+    }
+  }
+  epilogue<R>(a, x0, y0, sI, sQ, sT, sum_t, template_rsqrt(a, sum_t, sum_t_sq));
+}
+
+// General path: any template width (multiple of 4) and any image alignment.
+// Same decomposition; words are assembled from bytes and the template row is
+// walked one word at a time.
+template <int R>
+__global__ void __launch_bounds__(kThreads)
+    ncc_u8_general_kernel(const NccArgs a) {
+  extern __shared__ uint4 smem_u4[];
+  uint32_t *tmpl_s = reinterpret_cast<uint32_t *>(smem_u4);
+  __shared__ uint32_t red[2];
+  uint32_t sum_t, sum_t_sq;
+  stage_template(a, tmpl_s, red, sum_t, sum_t_sq);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int unit = blockIdx.x * kWarpsPerCta + warp;
+  if (unit >= a.units) return;
+  const int tx = unit % a.tiles_x, rb = unit / a.tiles_x;
+  const int x0 = tx * kUnitCols + lane * kCols;
+  const int y0 = rb * R;
+
+  uint32_t sI[R][kCols], sQ[R][kCols], sT[R][kCols];
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+#pragma unroll
+    for (int c = 0; c < kCols; ++c) sI[r][c] = sQ[r][c] = sT[r][c] = 0;
+
+  const int nrows = min(R + a.ht - 1, a.h - y0);
+  for (int rel = 0; rel < nrows; ++rel) {
+    const uint8_t *row = a.image + size_t(y0 + rel) * a.w;
+    unsigned mask = 0;
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+      if (rel - r >= 0 && rel - r < a.ht) mask |= 1u << r;
+    uint32_t w0 = load_word_bytes(row, x0, a.w);
+    uint32_t w1 = load_word_bytes(row, x0 + 4, a.w);
+    for (int i = 0; i < a.wtw; ++i) {
+      const uint32_t w2 = load_word_bytes(row, x0 + 4 * (i + 2), a.w);
+      uint32_t win[kCols];
+      win[0] = w0;
+      win[1] = fshr(w0, w1, 1);
+      win[2] = fshr(w0, w1, 2);
+      win[3] = fshr(w0, w1, 3);
+      win[4] = w1;
+      win[5] = fshr(w1, w2, 1);
+      win[6] = fshr(w1, w2, 2);
+      win[7] = fshr(w1, w2, 3);
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        if (!((mask >> r) & 1u)) continue;
+        const uint32_t tw = tmpl_s[(rel - r) * a.wtp + i];
+#pragma unroll
+        for (int c = 0; c < kCols; ++c) accum_window<R>(sI, sQ, sT, r, c, win[c], tw);
+      }
+      w0 = w1;
+      w1 = w2;
+    }
+  }
+  epilogue<R>(a, x0, y0, sI, sQ, sT, sum_t, template_rsqrt(a, sum_t, sum_t_sq));
+}
+
+template <typename Kernel>
+cudaError_t set_smem(Kernel kernel, size_t smem) {
+  if (smem > 48 * 1024) return allow_dynamic_smem(reinterpret_cast<const void *>(kernel));
+  return cudaSuccess;
+}
+
+template <typename Kernel>
+cudaError_t launch(Kernel kernel, const NccArgs &a, size_t smem,
+                   cudaStream_t stream) {
+  cudaError_t e = set_smem(kernel, smem);
+  if (e != cudaSuccess) return e;
+  const int blocks = (a.units + kWarpsPerCta - 1) / kWarpsPerCta;
+  kernel<<<blocks, kThreads, smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+// One CTA per tile.
+template <typename Kernel>
+cudaError_t launch_tiles(Kernel kernel, const NccArgs &a, size_t smem,
+                         cudaStream_t stream) {
+  cudaError_t e = set_smem(kernel, smem);
+  if (e != cudaSuccess) return e;
+  kernel<<<a.units, kFixedThreads, smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+// Fast-path launchers for template widths of 1 .. kMaxFixedWords words:
+// words 1 .. kNarrowWords are instantiated in ncc_u8.cu, the rest in
+// ncc_u8_wide.cu (two translation units compile in parallel).
+constexpr int kMaxFixedWords = 32;
+constexpr int kNarrowWords = 16;
+using FixedLauncher = cudaError_t (*)(const NccArgs &, size_t, int, cudaStream_t);
+
+template <int R, int WT>
+cudaError_t launch_fixed(const NccArgs &a, size_t smem, int vb, cudaStream_t stream) {
+  return vb == 16 ? launch_tiles(ncc_u8_fixed_kernel<R, WT, 16>, a, smem, stream)
+       : vb == 8  ? launch_tiles(ncc_u8_fixed_kernel<R, WT, 8>, a, smem, stream)
+                  : launch_tiles(ncc_u8_fixed_kernel<R, WT, 1>, a, smem, stream);
+}
+
+// Launchers of template words FIRST + 0 .. FIRST + sizeof...(Ks) - 1.
+template <int R, int FIRST, int... Ks>
+constexpr std::array<FixedLauncher, sizeof...(Ks)> fixed_launchers(
+    std::integer_sequence<int, Ks...>) {
+  return {{launch_fixed<R, FIRST + Ks>...}};
+}
+
+}  // namespace ncc
+
+// Fast path for templates of kNarrowWords + 1 .. kMaxFixedWords words
+// (ncc_u8_wide.cu).
+cudaError_t ncc_u8_launch_fixed_wide(const ncc::NccArgs &a, size_t smem, int vb,
+                                     cudaStream_t stream);
+
+}  // namespace corr

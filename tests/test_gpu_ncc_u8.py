@@ -62,9 +62,9 @@ def test_fixture(path):
     assert np.abs(c - fx["coef"]).max() <= COEF_TOL
 
 
-# fast path (wt a multiple of 4 up to 64, w % 8 == 0; rows 16-byte aligned
-# when w % 16 == 0) and general path shapes; ragged tails in both directions
-# (ow not a multiple of 128, oh odd)
+# fast path (wt a multiple of 4 up to 128; rows staged with 16- or 8-byte
+# loads when w is a multiple of 16 or 8, else byte loads) and general path
+# shapes; ragged tails in both directions (ow not a multiple of 128, oh odd)
 SHAPES = [
     (40, 64, 16, 16), (97, 296, 16, 16), (77, 520, 32, 32), (130, 264, 64, 64),
     (33, 1000, 32, 7), (50, 600, 64, 3), (21, 256, 16, 21),
@@ -76,6 +76,10 @@ SHAPES = [
     (50, 400, 24, 13), (66, 272, 28, 30), (70, 520, 36, 11), (80, 264, 40, 17),
     (90, 512, 44, 19), (100, 384, 48, 48), (75, 200, 52, 21), (120, 640, 56, 56),
     (64, 328, 60, 23),
+    # fast path, templates of 17 .. 32 words (68 .. 128 wide), all three
+    # staging units
+    (40, 264, 68, 9), (36, 336, 96, 7), (30, 300, 124, 5), (140, 512, 128, 128),
+    (50, 208, 112, 21),
 ]
 
 
