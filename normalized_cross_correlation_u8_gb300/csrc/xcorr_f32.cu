@@ -24,7 +24,8 @@
 //    block are added in a fixed order by a second pass.
 //  bcast (32+ rights per left) -- rights in lanes: every lane of a warp
 //    walks the same left row against its own rights, no cross-lane sums.
-//  tiny  (H*W <= 256, many pairs) -- 32 lefts and 16 rights are staged
+//  tiny  (H*W <= 256, many pairs) -- a block of lefts x rights (32 x 16,
+//    16 x 32, 8 x 64 or 64 x 8, whichever pads the batch least) is staged
 //    interleaved (matrix index fastest); each lane owns 4 lefts x 4 rights
 //    of one shift and walks that shift's exact overlap, so no product is
 //    wasted; warps pull shifts from a per-CTA list.
@@ -855,14 +856,15 @@ __global__ void __launch_bounds__(32 * kBWarps, CORR_XC_BMINB) xcorr_bcast_kerne
 }
 
 // ---------------------------------------------------------------------------
-// tiny kernel: H*W <= 256.  A CTA stages a block of 32 lefts and 16 rights
-// interleaved as [y][x][matrix]; lane (lb = lane%8, rb = lane/8) owns lefts
-// 4lb..4lb+3 x rights 4rb..4rb+3 of one shift and walks its exact overlap:
+// tiny kernel: H*W <= 256.  A CTA stages a block of kTinyL lefts and kTinyR
+// rights (32 x 16, 16 x 32, 8 x 64 or 64 x 8) interleaved as
+// [y][x][matrix]; lane (lb = lane % (kTinyL/4), rb = lane / (kTinyL/4)) owns
+// lefts 4lb..4lb+3 x rights 4rb..4rb+3 of one shift and walks its exact overlap:
 // per (y, x) two 16-byte loads feed 16 FMAs.  Shifts are dealt to the CTAs
 // of a block pair in snake order over a centre-first ranking and pulled by
 // the CTA's warps from a shared counter.
 // ---------------------------------------------------------------------------
-constexpr int kTinyL = 32, kTinyR = 16, kTinyWarps = 16;
+constexpr int kTinyWarps = 16;
 
 struct TinyArgs {
   const float *left;
@@ -874,7 +876,11 @@ struct TinyArgs {
   int vec4;              // matrices can be read as float4 (H*W % 4 == 0, aligned)
 };
 
+// kTinyL x kTinyR: the block of lefts x rights a CTA stages; a lane owns 4
+// x 4 of them, so (kTinyL / 4) * (kTinyR / 4) = 32.
+template <int kTinyL, int kTinyR>
 __global__ void __launch_bounds__(32 * kTinyWarps) xcorr_tiny_kernel(const TinyArgs a) {
+  static_assert((kTinyL / 4) * (kTinyR / 4) == 32, "one 4 x 4 block per lane");
   float *Ls = reinterpret_cast<float *>(g_smem4);
   const int H = a.H, W = a.W, HW = H * W;
   float *Rs = Ls + HW * kTinyL;
@@ -931,7 +937,7 @@ __global__ void __launch_bounds__(32 * kTinyWarps) xcorr_tiny_kernel(const TinyA
   __syncthreads();
 
   const int lane = threadIdx.x & 31;
-  const int lb = lane & 7, rb = lane >> 3;
+  const int lb = lane % (kTinyL / 4), rb = lane / (kTinyL / 4);
   const int ndy = 2 * H - 1, ndx = 2 * W - 1, nunits = ndy * ndx;
   // this CTA's units: rank j * nc + (j even ? c : nc - 1 - c) of the
   // centre-first order (snake order: every CTA gets a similar mix of costs)
@@ -1000,6 +1006,20 @@ cudaError_t launch_tiny(const float *left, int nl, const float *right, int nr, i
   a.nr = nr;
   a.H = H;
   a.W = W;
+  // block shape: the one of 32 x 16, 16 x 32, 8 x 64 and 64 x 8 lefts x
+  // rights that pads the batch least (32 x 16 on ties)
+  static const int shapes[4][2] = {{32, 16}, {16, 32}, {8, 64}, {64, 8}};
+  int best = 0;
+  long long best_pad = -1;
+  for (int i = 0; i < 4; ++i) {
+    const long long tl = shapes[i][0], tr = shapes[i][1];
+    const long long pad = ((nl + tl - 1) / tl) * tl * ((nr + tr - 1) / tr) * tr;
+    if (best_pad < 0 || pad < best_pad) {
+      best_pad = pad;
+      best = i;
+    }
+  }
+  const int kTinyL = shapes[best][0], kTinyR = shapes[best][1];
   a.lblocks = (nl + kTinyL - 1) / kTinyL;
   a.rblocks = (nr + kTinyR - 1) / kTinyR;
   const long long bp = (long long)a.lblocks * a.rblocks;
@@ -1027,9 +1047,13 @@ cudaError_t launch_tiny(const float *left, int nl, const float *right, int nr, i
   const long long blocks = bp * a.nc;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   const size_t smem = size_t(H) * W * (kTinyL + kTinyR) * sizeof(float);
-  cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void *>(xcorr_tiny_kernel));
+  auto kern = best == 0 ? xcorr_tiny_kernel<32, 16>
+            : best == 1 ? xcorr_tiny_kernel<16, 32>
+            : best == 2 ? xcorr_tiny_kernel<8, 64>
+                        : xcorr_tiny_kernel<64, 8>;
+  cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void *>(kern));
   if (e != cudaSuccess) return e;
-  xcorr_tiny_kernel<<<unsigned(blocks), 32 * kTinyWarps, smem, stream>>>(a);
+  kern<<<unsigned(blocks), 32 * kTinyWarps, smem, stream>>>(a);
   return cudaGetLastError();
 }
 

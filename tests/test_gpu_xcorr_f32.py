@@ -64,6 +64,8 @@ def test_fixture(path):
     (1, 1, 1, 1), (1, 1, 1, 3), (1, 1, 3, 1), (1, 1, 2, 2), (1, 1, 3, 5),
     (1, 1, 16, 16), (1, 1, 17, 33), (1, 1, 40, 9), (1, 1, 100, 130),
     (1, 5, 31, 29), (1, 37, 64, 64), (3, 4, 7, 11), (5, 9, 16, 16),
+    # small matrices in batches: block shapes 16 x 32, 8 x 64 and 64 x 8
+    (16, 40, 10, 10), (8, 64, 12, 12), (70, 5, 6, 7),
     (2, 3, 50, 8), (33, 3, 5, 5), (1, 1, 1, 300), (1, 1, 300, 1),
     # rights in lanes: ragged right block, W % 4 != 0, short H, several lefts
     (2, 40, 20, 12), (1, 33, 30, 10), (3, 64, 9, 40), (1, 96, 33, 8),
