@@ -55,9 +55,11 @@ extern "C" {
  *             a general kernel with the same results.
  *   w, h      image width and height in pixels, > 0.
  *   tmpl      device, wt*ht bytes, row-major, pitch wt.
- *   wt, ht    template size, 0 < wt <= w, 0 < ht <= h; wt must be a
- *             multiple of 4 (the template packs into whole 32-bit words) and
+ *   wt, ht    template size, 0 < wt <= w, 0 < ht <= h, and
  *             wt*ht <= CORR_NCC_MAX_TEMPLATE_PIXELS, else CORR_EUNSUPPORTED.
+ *             Any width: the template packs into 32-bit words with the last
+ *             word of a row zero-padded, and that word's SumI / SumISq take
+ *             only its template bytes.
  *   sums_out  device, 3 planes [3][oh][ow] of uint32 (SumI, SumISq, SumIT),
  *             ow = w-wt+1, oh = h-ht+1, dense, y-major; or NULL to skip.
  *   coef_out  device, [oh][ow] float32, dense; or NULL to skip.

@@ -26,7 +26,6 @@ int corr_ncc_u8(const uint8_t *image, int w, int h, const uint8_t *tmpl,
   if (!image || !tmpl || (!sums_out && !coef_out)) return CORR_EINVAL;
   if (w <= 0 || h <= 0 || wt <= 0 || ht <= 0) return CORR_EINVAL;
   if (wt > w || ht > h) return CORR_EINVAL;
-  if (wt % 4 != 0) return CORR_EUNSUPPORTED;
   if (int64_t(wt) * ht > CORR_NCC_MAX_TEMPLATE_PIXELS) return CORR_EUNSUPPORTED;
   // output planes are addressed with size_t, coordinates with int
   return cuda_status(corr::ncc_u8_launch(image, w, h, tmpl, wt, ht, sums_out,

@@ -21,7 +21,10 @@ cudaError_t ncc_u8_launch(const uint8_t *image, int w, int h,
   a.h = h;
   a.wt = wt;
   a.ht = ht;
-  a.wtw = wt / 4;
+  a.wtw = (wt + 3) / 4;
+  a.tail = wt % 4;
+  a.tail_ones = a.tail ? 0x01010101u >> (8 * (4 - a.tail)) : 0x01010101u;
+  a.tail_mask = a.tail ? 0xffffffffu >> (8 * (4 - a.tail)) : 0xffffffffu;
   a.wtp = (a.wtw + 3) & ~3;
   a.ow = w - wt + 1;
   a.oh = h - ht + 1;

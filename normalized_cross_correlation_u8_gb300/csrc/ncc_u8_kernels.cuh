@@ -8,12 +8,14 @@
 // SumISq against the word itself, SumIT against the packed template word).
 // Consecutive output columns slide the window by one byte, so a thread's
 // window words are cut out of two aligned image words with __funnelshift_r;
-// the template, whose width is a multiple of four, packs directly.  Several
+// the template packs directly into words (a width that is not a multiple of
+// four zero-pads each row's last word, whose SumI / SumISq then take only
+// the template bytes: a generalization the section does not state).  Several
 // independent output columns (and rows) per thread keep many accumulation
 // chains in flight (the section's instruction-level parallelism).
 //
-// GB300 layout of the work (fast path: wt a multiple of 4 up to 64, any
-// image alignment; wider templates take the general path below):
+// GB300 layout of the work (fast path: wt up to 128, any image alignment;
+// wider templates take the general path below):
 //   * a CTA owns 128 output columns x TY output rows; it copies the image
 //     tile plus its halo (TY+ht-1 rows x 128+wt+8 bytes) into shared memory
 //     with independent 16-byte vector loads (one memory latency per tile,
@@ -78,7 +80,10 @@ struct NccArgs {
   float *coef;
   size_t plane;      // ow * oh
   int w, h, wt, ht;
-  int wtw;           // template words per row (wt / 4)
+  int wtw;           // template words per row (ceil(wt / 4))
+  int tail;          // wt % 4: bytes of the last word that are template pixels (0: all)
+  uint32_t tail_ones;  // SumI multiplier of the last word (0x01 in its template bytes)
+  uint32_t tail_mask;  // SumISq mask of the last word (0xff in its template bytes)
   int wtp;           // shared-memory template row stride in words (multiple of 4)
   int ow, oh;
   int tiles_x;       // units across a row of outputs
@@ -107,7 +112,7 @@ __device__ __forceinline__ void stage_template(const NccArgs &a, uint32_t *tmpl_
                                                uint32_t &sum_t_sq) {
   if (threadIdx.x < 2) red[threadIdx.x] = 0;
   __syncthreads();
-  const bool aligned4 = (reinterpret_cast<uintptr_t>(a.tmpl) & 3) == 0;
+  const bool aligned4 = (reinterpret_cast<uintptr_t>(a.tmpl) & 3) == 0 && a.tail == 0;
   uint32_t s = 0, q = 0;
   const int total = a.ht * a.wtp;
   for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
@@ -119,7 +124,8 @@ __device__ __forceinline__ void stage_template(const NccArgs &a, uint32_t *tmpl_
         v = __ldg(reinterpret_cast<const uint32_t *>(a.tmpl + byte));
       } else {
 #pragma unroll
-        for (int b = 0; b < 4; ++b) v |= uint32_t(__ldg(a.tmpl + byte + b)) << (8 * b);
+        for (int b = 0; b < 4; ++b)
+          if (4 * i + b < a.wt) v |= uint32_t(__ldg(a.tmpl + byte + b)) << (8 * b);
       }
     }
     tmpl_s[idx] = v;
@@ -148,6 +154,20 @@ __device__ __forceinline__ void accum_window(uint32_t (&sI)[R][kCols],
                                              int c, uint32_t win, uint32_t tw) {
   sI[r][c] = __dp4a(win, kOnes, sI[r][c]);
   sQ[r][c] = __dp4a(win, win, sQ[r][c]);
+  sT[r][c] = __dp4a(win, tw, sT[r][c]);
+}
+
+// The last word of a template row whose width is not a multiple of 4: its
+// pad bytes are zero in the template word (SumIT needs nothing more), while
+// SumI and SumISq take only the template bytes of the window.
+template <int R>
+__device__ __forceinline__ void accum_window_tail(uint32_t (&sI)[R][kCols],
+                                                  uint32_t (&sQ)[R][kCols],
+                                                  uint32_t (&sT)[R][kCols], int r,
+                                                  int c, uint32_t win, uint32_t tw,
+                                                  uint32_t ones, uint32_t mask) {
+  sI[r][c] = __dp4a(win, ones, sI[r][c]);
+  sQ[r][c] = __dp4a(win & mask, win, sQ[r][c]);
   sT[r][c] = __dp4a(win, tw, sT[r][c]);
 }
 
@@ -211,7 +231,7 @@ __device__ __forceinline__ void row_fixed(const uint32_t (&wv)[RowWords<WT>::kWo
                                           const uint32_t *tmpl_s, int rel,
                                           unsigned mask, uint32_t (&sI)[R][kCols],
                                           uint32_t (&sQ)[R][kCols],
-                                          uint32_t (&sT)[R][kCols]) {
+                                          uint32_t (&sT)[R][kCols], const NccArgs &a) {
   constexpr int WTP = (WT + 3) & ~3;
 #pragma unroll
   for (int ib = 0; ib < WT; ib += 4) {
@@ -234,8 +254,14 @@ __device__ __forceinline__ void row_fixed(const uint32_t (&wv)[RowWords<WT>::kWo
       for (int r = 0; r < R; ++r) {
         if (!(FULL || ((mask >> r) & 1u))) continue;
         const uint32_t tw = m == 0 ? tq[r].x : m == 1 ? tq[r].y : m == 2 ? tq[r].z : tq[r].w;
+        if (i == WT - 1 && a.tail) {   // partial last word (warp-uniform)
 #pragma unroll
-        for (int c = 0; c < kCols; ++c) accum_window<R>(sI, sQ, sT, r, c, win[c], tw);
+          for (int c = 0; c < kCols; ++c)
+            accum_window_tail<R>(sI, sQ, sT, r, c, win[c], tw, a.tail_ones, a.tail_mask);
+        } else {
+#pragma unroll
+          for (int c = 0; c < kCols; ++c) accum_window<R>(sI, sQ, sT, r, c, win[c], tw);
+        }
       }
     }
   }
@@ -363,13 +389,13 @@ __global__ void __launch_bounds__(kFixedThreads, CORR_NCC_MINB)
   // warp group takes template rows [j_lo, j_hi)
   auto process = [&](const uint32_t (&wv)[NW], int rel) {
     if (rel - (R - 1) >= j_lo && rel <= j_hi - 1) {
-      row_fixed<R, WT, true>(wv, tmpl_s, rel, 0u, sI, sQ, sT);
+      row_fixed<R, WT, true>(wv, tmpl_s, rel, 0u, sI, sQ, sT, a);
     } else {
       unsigned mask = 0;
 #pragma unroll
       for (int r = 0; r < R; ++r)
         if (rel - r >= j_lo && rel - r < j_hi) mask |= 1u << r;
-      row_fixed<R, WT, false>(wv, tmpl_s, rel, mask, sI, sQ, sT);
+      row_fixed<R, WT, false>(wv, tmpl_s, rel, mask, sI, sQ, sT, a);
     }
   };
   const int rel_end = min(nrows, j_hi + R - 1);
@@ -463,12 +489,19 @@ __global__ void __launch_bounds__(kThreads)
       win[5] = fshr(w1, w2, 1);
       win[6] = fshr(w1, w2, 2);
       win[7] = fshr(w1, w2, 3);
+      const bool tail = a.tail && i == a.wtw - 1;   // partial last word (warp-uniform)
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         if (!((mask >> r) & 1u)) continue;
         const uint32_t tw = tmpl_s[(rel - r) * a.wtp + i];
+        if (tail) {
 #pragma unroll
-        for (int c = 0; c < kCols; ++c) accum_window<R>(sI, sQ, sT, r, c, win[c], tw);
+          for (int c = 0; c < kCols; ++c)
+            accum_window_tail<R>(sI, sQ, sT, r, c, win[c], tw, a.tail_ones, a.tail_mask);
+        } else {
+#pragma unroll
+          for (int c = 0; c < kCols; ++c) accum_window<R>(sI, sQ, sT, r, c, win[c], tw);
+        }
       }
       w0 = w1;
       w1 = w2;

@@ -60,7 +60,8 @@ def test_stream_is_thread_local_setting():
     ((FAKE, 0, 16, FAKE, 4, 4, FAKE, FAKE), -1),             # empty image
     ((FAKE, 16, 16, FAKE, 20, 4, FAKE, FAKE), -1),           # template wider
     ((FAKE, 16, 16, FAKE, 4, 17, FAKE, FAKE), -1),           # template taller
-    ((FAKE, 16, 16, FAKE, 6, 4, FAKE, FAKE), -2),            # wt % 4 != 0
+    ((FAKE, 16, 16, FAKE, 0, 4, FAKE, FAKE), -1),            # empty template
+    ((FAKE, 300, 300, FAKE, 257, 258, FAKE, FAKE), -2),      # odd width, > 66052 pixels
     ((FAKE, 1000, 1000, FAKE, 260, 260, FAKE, FAKE), -2),    # > 66052 pixels
     ((FAKE, 16, 16, FAKE, -4, 4, FAKE, FAKE), -1),
 ])

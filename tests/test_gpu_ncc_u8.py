@@ -62,7 +62,7 @@ def test_fixture(path):
     assert np.abs(c - fx["coef"]).max() <= COEF_TOL
 
 
-# fast path (wt a multiple of 4 up to 128; rows staged with 16- or 8-byte
+# fast path (wt up to 128; rows staged with 16- or 8-byte
 # loads when w is a multiple of 16 or 8, else byte loads) and general path
 # shapes; ragged tails in both directions (ow not a multiple of 128, oh odd)
 SHAPES = [
@@ -80,6 +80,11 @@ SHAPES = [
     # staging units
     (40, 264, 68, 9), (36, 336, 96, 7), (30, 300, 124, 5), (140, 512, 128, 128),
     (50, 208, 112, 21),
+    # template widths that are not a multiple of 4 (partial last word):
+    # fast path with each staging unit, and the general path (wt > 128)
+    (20, 64, 1, 5), (21, 136, 2, 3), (30, 64, 3, 30), (40, 304, 15, 15),
+    (33, 200, 31, 17), (35, 301, 17, 9), (70, 520, 63, 41), (60, 264, 127, 7),
+    (9, 300, 129, 3), (12, 270, 201, 5),
 ]
 
 
@@ -171,9 +176,9 @@ def test_guard_bands_untouched():
 
 def test_argument_errors_raise():
     dev = torch.device("cuda", 0)
-    img = torch.zeros(32, 32, dtype=torch.uint8, device=dev)
-    with pytest.raises(corr.CorrError) as e:
-        corr.ncc_u8(img, torch.zeros(4, 6, dtype=torch.uint8, device=dev))
+    img = torch.zeros(300, 300, dtype=torch.uint8, device=dev)
+    with pytest.raises(corr.CorrError) as e:   # 258 x 257 > 66052 template pixels
+        corr.ncc_u8(img, torch.zeros(258, 257, dtype=torch.uint8, device=dev))
     assert e.value.code == -2
 
 
