@@ -69,6 +69,31 @@ int corr_ncc_u8(const uint8_t *image, int w, int h, const uint8_t *tmpl,
                 int wt, int ht, uint32_t *sums_out, float *coef_out);
 
 /*
+ * corr_ncc_set_method / corr_ncc_get_method -- how corr_ncc_u8 forms SumI
+ * and SumISq on its tiled fast kernel (templates up to 128 wide; wider ones
+ * always use the first method).  Thread-local, like the stream.  Both
+ * methods give bit-identical sums and coefficients.
+ *
+ *   CORR_NCC_METHOD_DP4A  the section's method: all three sums by unsigned
+ *                         dp4a in the tiled kernel.  Allocates nothing.
+ *   CORR_NCC_METHOD_BOX   SumI and SumISq as box filters of I and I^2
+ *                         (a horizontal and a vertical sliding-sum pass,
+ *                         exact in unsigned 32-bit arithmetic), so the tiled
+ *                         kernel runs one dp4a per 4 pixels (SumIT) instead
+ *                         of three.  Not on the pages.  Takes stream-ordered
+ *                         temporary device memory from a library pool:
+ *                         8*h*ow bytes, plus 8*oh*ow when sums_out is NULL;
+ *                         returns CORR_ECUDA if that allocation fails.
+ *
+ * corr_ncc_set_method returns CORR_EINVAL for any other value (the method
+ * is then unchanged).  The default is CORR_NCC_METHOD_BOX.
+ */
+#define CORR_NCC_METHOD_DP4A 0
+#define CORR_NCC_METHOD_BOX 1
+int corr_ncc_set_method(int method);
+int corr_ncc_get_method(void);
+
+/*
  * corr_xcorr_f32 -- float32 full 2D cross-correlation, all overlaps.
  *
  * Defined by the "Efficient GPU-accelerated Parallel Cross-correlation"

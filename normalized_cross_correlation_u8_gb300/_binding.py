@@ -23,8 +23,11 @@ CORR_EINVAL = -1
 CORR_EUNSUPPORTED = -2
 CORR_ECUDA = -3
 NCC_MAX_TEMPLATE_PIXELS = 66052
+NCC_METHOD_DP4A = 0
+NCC_METHOD_BOX = 1
+_NCC_METHODS = {"dp4a": NCC_METHOD_DP4A, "box": NCC_METHOD_BOX}
 
-EXPORTS = ["corr_ncc_u8", "corr_xcorr_f32", "corr_xcorr_f32_noalloc", "corr_set_stream",
+EXPORTS = ["corr_ncc_u8", "corr_ncc_set_method", "corr_ncc_get_method", "corr_xcorr_f32", "corr_xcorr_f32_noalloc", "corr_set_stream",
            "corr_get_stream", "corr_strerror", "corr_last_cuda_error",
            "corr_version", "corr_peak_dp4a", "corr_peak_ffma"]
 
@@ -64,6 +67,8 @@ def load(build_if_missing=True):
         lib = ctypes.CDLL(path)
         c_int, vp, c_dbl_p = ctypes.c_int, ctypes.c_void_p, ctypes.POINTER(ctypes.c_double)
         lib.corr_ncc_u8.argtypes = [vp, c_int, c_int, vp, c_int, c_int, vp, vp]
+        lib.corr_ncc_set_method.argtypes = [c_int]
+        lib.corr_ncc_get_method.argtypes = []
         lib.corr_xcorr_f32.argtypes = [vp, c_int, vp, c_int, c_int, c_int, vp]
         lib.corr_xcorr_f32_noalloc.argtypes = [vp, c_int, vp, c_int, c_int, c_int, vp]
         lib.corr_set_stream.argtypes = [vp]
@@ -75,7 +80,8 @@ def load(build_if_missing=True):
         lib.corr_version.argtypes = []
         lib.corr_peak_dp4a.argtypes = [c_int, c_dbl_p, c_dbl_p]
         lib.corr_peak_ffma.argtypes = [c_dbl_p, c_dbl_p]
-        for f in (lib.corr_ncc_u8, lib.corr_xcorr_f32, lib.corr_xcorr_f32_noalloc,
+        for f in (lib.corr_ncc_u8, lib.corr_ncc_set_method, lib.corr_ncc_get_method,
+                  lib.corr_xcorr_f32, lib.corr_xcorr_f32_noalloc,
                   lib.corr_set_stream,
                   lib.corr_last_cuda_error, lib.corr_version,
                   lib.corr_peak_dp4a, lib.corr_peak_ffma):
@@ -111,10 +117,27 @@ def _u32_empty(shape, device):
         return torch.empty(shape, dtype=torch.int32, device=device)
 
 
-def ncc_u8_into(image, tmpl, sums_out, coef_out):
+def ncc_set_method(method):
+    """Select how this thread's ncc_u8 calls form SumI / SumISq on the fast
+    kernel: "dp4a" (three dp4a per 4 pixels, no scratch) or "box" (box-filter
+    passes, then one dp4a per 4 pixels for SumIT; the default).  Results are
+    bit-identical."""
+    if method not in _NCC_METHODS:
+        raise ValueError(f"method must be one of {sorted(_NCC_METHODS)}")
+    _check(load().corr_ncc_set_method(_NCC_METHODS[method]))
+
+
+def ncc_get_method():
+    """This thread's ncc_u8 method name ("dp4a" or "box")."""
+    code = load().corr_ncc_get_method()
+    return {v: k for k, v in _NCC_METHODS.items()}[code]
+
+
+def ncc_u8_into(image, tmpl, sums_out, coef_out, method=None):
     """Device call: image [h,w] uint8, tmpl [ht,wt] uint8, sums_out
     [3,oh,ow] 32-bit (or None), coef_out [oh,ow] float32 (or None), all on
-    the same CUDA device and contiguous.  Runs on the current stream."""
+    the same CUDA device and contiguous.  Runs on the current stream.
+    `method` ("dp4a" / "box") overrides this thread's method for the call."""
     if image.dtype != torch.uint8 or tmpl.dtype != torch.uint8:
         raise TypeError("image and template must be uint8")
     if image.dim() != 2 or tmpl.dim() != 2:
@@ -134,17 +157,25 @@ def ncc_u8_into(image, tmpl, sums_out, coef_out):
     if coef_out is not None and coef_out.dtype != torch.float32:
         raise TypeError("coef_out must be float32")
     image, tmpl = image.contiguous(), tmpl.contiguous()
+    if method is not None and method not in _NCC_METHODS:
+        raise ValueError(f"method must be one of {sorted(_NCC_METHODS)}")
     with torch.cuda.device(dev):
         lib = _bind_stream(dev)
-        _check(lib.corr_ncc_u8(
-            ctypes.c_void_p(image.data_ptr()), w, h,
-            ctypes.c_void_p(tmpl.data_ptr()), wt, ht,
-            ctypes.c_void_p(sums_out.data_ptr() if sums_out is not None else 0),
-            ctypes.c_void_p(coef_out.data_ptr() if coef_out is not None else 0)))
+        prev = lib.corr_ncc_get_method()
+        if method is not None:
+            _check(lib.corr_ncc_set_method(_NCC_METHODS[method]))
+        try:
+            _check(lib.corr_ncc_u8(
+                ctypes.c_void_p(image.data_ptr()), w, h,
+                ctypes.c_void_p(tmpl.data_ptr()), wt, ht,
+                ctypes.c_void_p(sums_out.data_ptr() if sums_out is not None else 0),
+                ctypes.c_void_p(coef_out.data_ptr() if coef_out is not None else 0)))
+        finally:
+            lib.corr_ncc_set_method(prev)
     return sums_out, coef_out
 
 
-def ncc_u8(image, tmpl, sums=True, coef=True, device=None):
+def ncc_u8(image, tmpl, sums=True, coef=True, device=None, method=None):
     """Normalized cross-correlation of a uint8 image with a uint8 template.
 
     Returns (sums [3, oh, ow] uint32 planes SumI/SumISq/SumIT or None,
@@ -166,7 +197,7 @@ def ncc_u8(image, tmpl, sums=True, coef=True, device=None):
         raise CorrError(CORR_EINVAL, "template larger than image")
     s = _u32_empty((3, oh, ow), dev) if sums else None
     c = torch.empty((oh, ow), dtype=torch.float32, device=dev) if coef else None
-    ncc_u8_into(image, tmpl, s, c)
+    ncc_u8_into(image, tmpl, s, c, method=method)
     if host:
         s = s.cpu() if s is not None else None
         c = c.cpu() if c is not None else None

@@ -10,6 +10,7 @@ namespace {
 
 thread_local cudaStream_t tls_stream = nullptr;
 thread_local int tls_cuda_error = 0;
+thread_local int tls_ncc_method = CORR_NCC_METHOD_BOX;
 
 int cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return CORR_OK;
@@ -28,9 +29,19 @@ int corr_ncc_u8(const uint8_t *image, int w, int h, const uint8_t *tmpl,
   if (wt > w || ht > h) return CORR_EINVAL;
   if (int64_t(wt) * ht > CORR_NCC_MAX_TEMPLATE_PIXELS) return CORR_EUNSUPPORTED;
   // output planes are addressed with size_t, coordinates with int
+  const int method = tls_ncc_method == CORR_NCC_METHOD_BOX ? corr::kMethodBox
+                                                            : corr::kMethodDp4a;
   return cuda_status(corr::ncc_u8_launch(image, w, h, tmpl, wt, ht, sums_out,
-                                         coef_out, tls_stream));
+                                         coef_out, method, tls_stream));
 }
+
+int corr_ncc_set_method(int method) {
+  if (method != CORR_NCC_METHOD_DP4A && method != CORR_NCC_METHOD_BOX) return CORR_EINVAL;
+  tls_ncc_method = method;
+  return CORR_OK;
+}
+
+int corr_ncc_get_method(void) { return tls_ncc_method; }
 
 int corr_xcorr_f32(const float *left, int nl, const float *right, int nr,
                    int H, int W, float *out) {

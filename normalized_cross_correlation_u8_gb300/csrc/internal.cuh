@@ -16,11 +16,19 @@ int device_sm_count();
 // (device, kernel).
 cudaError_t allow_dynamic_smem(const void *kernel);
 
+// Stream-ordered temporary device memory from the library's pool on the
+// current device (scratch.cu); release it with cudaFreeAsync on `stream`.
+cudaError_t scratch_alloc(void **ptr, size_t bytes, cudaStream_t stream);
+
+// Methods of the u8 fast path (corr.h: CORR_NCC_METHOD_*).
+constexpr int kMethodDp4a = 0;   // SumI, SumISq, SumIT all by dp4a in the tiled kernel
+constexpr int kMethodBox = 1;    // SumI, SumISq by box passes; SumIT by dp4a
+
 // Launches the u8 normalized cross-correlation on `stream`.  Arguments are
 // already validated by the C ABI layer (corr_api.cu).
 cudaError_t ncc_u8_launch(const uint8_t *image, int w, int h,
                           const uint8_t *tmpl, int wt, int ht,
-                          uint32_t *sums_out, float *coef_out,
+                          uint32_t *sums_out, float *coef_out, int method,
                           cudaStream_t stream);
 
 // Launches the f32 full cross-correlation on `stream` (validated arguments).

@@ -9,7 +9,7 @@ using namespace ncc;
 
 cudaError_t ncc_u8_launch(const uint8_t *image, int w, int h,
                           const uint8_t *tmpl, int wt, int ht,
-                          uint32_t *sums_out, float *coef_out,
+                          uint32_t *sums_out, float *coef_out, int method,
                           cudaStream_t stream) {
   constexpr int R = CORR_NCC_ROWS;
   NccArgs a;
@@ -29,27 +29,27 @@ cudaError_t ncc_u8_launch(const uint8_t *image, int w, int h,
   a.ow = w - wt + 1;
   a.oh = h - ht + 1;
   a.plane = size_t(a.ow) * a.oh;
-  const size_t smem = size_t(ht) * a.wtp * 4;
+  a.box_i = a.box_q = nullptr;
+  const size_t smem = size_t(ht) * a.wtp * 4;   // general path: the template
 
   const bool aligned8 = (reinterpret_cast<uintptr_t>(image) & 7) == 0 && (w & 7) == 0;
   const bool aligned16 = (reinterpret_cast<uintptr_t>(image) & 15) == 0 && (w & 15) == 0;
   if (a.wtw >= 1 && a.wtw <= kMaxFixedWords) {
-    constexpr int TY = 2 * R * kWarpsPerCta;
+    const bool box = method == kMethodBox;
+    const int rows = box ? kBoxRows : R;
+    const int ty = 2 * rows * kWarpsPerCta;
+    const size_t ts = fixed_tile_smem(ht, a.wtw, a.wtp, rows, box ? kBoxSplit : kSplit,
+                                      box ? 1 : 3);
+    if (ts > 200 * 1024) goto general;   // very tall template: general path
     a.tiles_x = (a.ow + kHalfUnitCols - 1) / kHalfUnitCols;
-    const long long tiles = (long long)a.tiles_x * ((a.oh + TY - 1) / TY);
+    const long long tiles = (long long)a.tiles_x * ((a.oh + ty - 1) / ty);
     if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     a.units = int(tiles);
-    auto tile_smem = [&](int wtw) {
-      const size_t rb = (kHalfUnitCols + 4 * wtw + 8 + 15) & ~15;
-      const size_t part = size_t(kSplit - 1) * kWarpsPerCta * 32 * 3 * R * kCols * 4;
-      return smem + size_t(TY + ht - 1) * rb + part;
-    };
-    const size_t ts = tile_smem(a.wtw);
-    if (ts > 200 * 1024) goto general;   // very tall template: general path
     const int vb = aligned16 ? 16 : aligned8 ? 8 : 1;
+    if (box) return ncc_u8_launch_box(a, ts, vb, stream);
     if (a.wtw > kNarrowWords) return ncc_u8_launch_fixed_wide(a, ts, vb, stream);
     static constexpr auto table =
-        fixed_launchers<R, 1>(std::make_integer_sequence<int, kNarrowWords>{});
+        fixed_launchers<R, false, 1>(std::make_integer_sequence<int, kNarrowWords>{});
     return table[a.wtw - 1](a, ts, vb, stream);
   }
 general:

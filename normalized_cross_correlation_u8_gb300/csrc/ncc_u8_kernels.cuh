@@ -63,13 +63,43 @@ constexpr int kHalfUnitCols = 16 * kCols;  // output columns per warp unit (fast
 #ifndef CORR_NCC_KSPLIT
 #define CORR_NCC_KSPLIT 2
 #endif
+// Output rows per half-warp of the SumIT-only kernel (box-sum variant).
+#ifndef CORR_NCC_BOX_ROWS
+#define CORR_NCC_BOX_ROWS 2
+#endif
+#ifndef CORR_NCC_BOX_MINB
+#define CORR_NCC_BOX_MINB 1
+#endif
+// Template-row ranges (warp groups) per tile of the SumIT-only kernel.
+#ifndef CORR_NCC_BOX_KSPLIT
+#define CORR_NCC_BOX_KSPLIT 2
+#endif
 constexpr int kWarpsPerCta = CORR_NCC_WARPS;
 constexpr int kThreads = 32 * kWarpsPerCta;
 // Fast path: the template rows of a tile are split into kSplit ranges, one
 // per group of kWarpsPerCta warps; the groups' partial sums are added in
 // shared memory (integer sums: exact in any order).
 constexpr int kSplit = CORR_NCC_KSPLIT;
-constexpr int kFixedThreads = kThreads * kSplit;
+constexpr int kBoxRows = CORR_NCC_BOX_ROWS;
+constexpr int kBoxSplit = CORR_NCC_BOX_KSPLIT;
+// Warp groups and threads of the fast kernel (BOX: the SumIT-only form).
+template <bool BOX>
+struct FixedShape {
+  static constexpr int kGroups = BOX ? kBoxSplit : kSplit;
+  static constexpr int kThreadsPerCta = kThreads * kGroups;
+};
+
+
+// Shared memory of a fast-path tile: the packed template (ht rows of wtp
+// words), the image tile plus halo (TY+ht-1 rows of 128+4*wtw+8 bytes,
+// rounded to 16) and the exchange area of the template-row split (groups
+// warp groups, ns sums per output).
+inline size_t fixed_tile_smem(int ht, int wtw, int wtp, int rows, int groups, int ns) {
+  const int ty = 2 * rows * kWarpsPerCta;
+  const size_t rb = (kHalfUnitCols + 4 * wtw + 8 + 15) & ~15;
+  const size_t part = size_t(groups - 1) * kWarpsPerCta * 32 * ns * rows * kCols * 4;
+  return size_t(ht) * wtp * 4 + size_t(ty + ht - 1) * rb + part;
+}
 constexpr uint32_t kOnes = 0x01010101u;
 constexpr int kStageBatch = 4;       // tile chunks per thread loaded ahead of the template
 
@@ -86,6 +116,8 @@ struct NccArgs {
   uint32_t tail_mask;  // SumISq mask of the last word (0xff in its template bytes)
   int wtp;           // shared-memory template row stride in words (multiple of 4)
   int ow, oh;
+  const uint32_t *box_i;  // BOX kernels: SumI / SumISq planes from the box passes
+  const uint32_t *box_q;  //   (row stride ow; may be the sums_out planes themselves)
   int tiles_x;       // units across a row of outputs
   int units;         // warp units (fast path: 128 cols x 2R rows)
 };
@@ -171,11 +203,24 @@ __device__ __forceinline__ void accum_window_tail(uint32_t (&sI)[R][kCols],
   sT[r][c] = __dp4a(win, tw, sT[r][c]);
 }
 
+// Single-precision value of an integer |v| < 2^55 from two 32-bit
+// conversions: v = hi * 2^24 + lo with lo < 2^24 exact in float, hi rounded
+// once and the sum once (relative error below 2^-23).  A direct 64-bit
+// conversion would issue on the FP64 unit, which this part provides at a few
+// lanes per clock.
+__device__ __forceinline__ float i64_to_f32(int64_t v) {
+  const int32_t hi = int32_t(v >> 24);
+  const uint32_t lo = uint32_t(v) & 0xffffffu;
+  return fmaf(float(hi), 16777216.f, float(lo));
+}
+
 // Write the sums and the coefficient of one lane's R x 8 block.  The
 // numerator and the window variance term are exact 64-bit integers; the
 // ratio is num * rsqrt(dI) * rsqrt(dT) in single precision (a few ulp of
 // |coef| <= 1, far inside the 1e-5 bound).  rs_t = rsqrt(dT) is per template.
-template <int R>
+// BOX: SumI and SumISq come from the box planes (already written to the
+// sums planes when those are the outputs); only SumIT is stored here.
+template <int R, bool BOX = false>
 __device__ __forceinline__ void epilogue(const NccArgs &a, int x0, int y0,
                                          const uint32_t (&sI)[R][kCols],
                                          const uint32_t (&sQ)[R][kCols],
@@ -191,16 +236,20 @@ __device__ __forceinline__ void epilogue(const NccArgs &a, int x0, int y0,
       const int x = x0 + c;
       if (x >= a.ow) break;
       const size_t o = size_t(y) * a.ow + x;
+      const uint32_t vi = BOX ? a.box_i[o] : sI[r][c];
+      const uint32_t vq = BOX ? a.box_q[o] : sQ[r][c];
       if (a.sums) {
-        a.sums[o] = sI[r][c];
-        a.sums[a.plane + o] = sQ[r][c];
+        if (!BOX) {
+          a.sums[o] = vi;
+          a.sums[a.plane + o] = vq;
+        }
         a.sums[2 * a.plane + o] = sT[r][c];
       }
       if (a.coef) {
-        const int64_t si = sI[r][c];
+        const int64_t si = vi;
         const int64_t num = n * int64_t(sT[r][c]) - si * int64_t(sum_t);
-        const int64_t d_i = n * int64_t(sQ[r][c]) - si * si;
-        a.coef[o] = d_i > 0 ? float(num) * rsqrtf(float(d_i)) * rs_t : 0.f;
+        const int64_t d_i = n * int64_t(vq) - si * si;
+        a.coef[o] = d_i > 0 ? i64_to_f32(num) * rsqrtf(i64_to_f32(d_i)) * rs_t : 0.f;
       }
     }
   }
@@ -226,7 +275,7 @@ struct RowWords {
   static constexpr int kWords = 2 * kPairs;
 };
 
-template <int R, int WT, bool FULL>
+template <int R, int WT, bool FULL, bool BOX>
 __device__ __forceinline__ void row_fixed(const uint32_t (&wv)[RowWords<WT>::kWords],
                                           const uint32_t *tmpl_s, int rel,
                                           unsigned mask, uint32_t (&sI)[R][kCols],
@@ -254,7 +303,10 @@ __device__ __forceinline__ void row_fixed(const uint32_t (&wv)[RowWords<WT>::kWo
       for (int r = 0; r < R; ++r) {
         if (!(FULL || ((mask >> r) & 1u))) continue;
         const uint32_t tw = m == 0 ? tq[r].x : m == 1 ? tq[r].y : m == 2 ? tq[r].z : tq[r].w;
-        if (i == WT - 1 && a.tail) {   // partial last word (warp-uniform)
+        if (BOX) {                      // SumIT only; pad template bytes are zero
+#pragma unroll
+          for (int c = 0; c < kCols; ++c) sT[r][c] = __dp4a(win[c], tw, sT[r][c]);
+        } else if (i == WT - 1 && a.tail) {   // partial last word (warp-uniform)
 #pragma unroll
           for (int c = 0; c < kCols; ++c)
             accum_window_tail<R>(sI, sQ, sT, r, c, win[c], tw, a.tail_ones, a.tail_mask);
@@ -295,9 +347,12 @@ struct StageChunk {
   static constexpr int kBytes = int(sizeof(type));
 };
 
-template <int R, int WT, int VB>
-__global__ void __launch_bounds__(kFixedThreads, CORR_NCC_MINB)
+template <int R, int WT, int VB, bool BOX>
+__global__ void __launch_bounds__(FixedShape<BOX>::kThreadsPerCta,
+                                  BOX ? CORR_NCC_BOX_MINB : CORR_NCC_MINB)
     ncc_u8_fixed_kernel(const NccArgs a) {
+  constexpr int KS = FixedShape<BOX>::kGroups;
+  constexpr int kFixedThreads = FixedShape<BOX>::kThreadsPerCta;
   constexpr int WTP = (WT + 3) & ~3;
   constexpr int RB = TileGeom<WT>::kRowBytes;
   constexpr int TY = 2 * R * kWarpsPerCta;
@@ -357,7 +412,7 @@ __global__ void __launch_bounds__(kFixedThreads, CORR_NCC_MINB)
   const int warp_id = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int warp = warp_id % kWarpsPerCta;            // row group of the tile
   const int ks = warp_id / kWarpsPerCta;              // template-row range
-  const int j_lo = ks * a.ht / kSplit, j_hi = (ks + 1) * a.ht / kSplit;
+  const int j_lo = ks * a.ht / KS, j_hi = (ks + 1) * a.ht / KS;
   const int half = lane >> 4, hl = lane & 15;
   const int yr0 = warp * 2 * R + half * R;           // tile-relative first row
   const int x0 = xt + hl * kCols;
@@ -385,32 +440,41 @@ __global__ void __launch_bounds__(kFixedThreads, CORR_NCC_MINB)
       dst[2 * p + 1] = v.y;
     }
   };
-  // tile row yr0 + rel meets template row rel - r for output row r; this
-  // warp group takes template rows [j_lo, j_hi)
-  auto process = [&](const uint32_t (&wv)[NW], int rel) {
-    if (rel - (R - 1) >= j_lo && rel <= j_hi - 1) {
-      row_fixed<R, WT, true>(wv, tmpl_s, rel, 0u, sI, sQ, sT, a);
-    } else {
-      unsigned mask = 0;
-#pragma unroll
-      for (int r = 0; r < R; ++r)
-        if (rel - r >= j_lo && rel - r < j_hi) mask |= 1u << r;
-      row_fixed<R, WT, false>(wv, tmpl_s, rel, mask, sI, sQ, sT, a);
-    }
-  };
+  // Tile row yr0 + rel meets template row rel - r for output row r; this
+  // warp group takes template rows [j_lo, j_hi).  Rows [body_lo, body_hi)
+  // meet all R output rows and run unmasked, two at a time with the next
+  // row's words read ahead (load_row clamps its row, so reading one row
+  // past the end is harmless); the first and last R-1 rows are masked.
   const int rel_end = min(nrows, j_hi + R - 1);
-  uint32_t wa[NW], wb[NW];
-  if (j_lo < rel_end) load_row(j_lo, wa);
-  for (int rel = j_lo; rel < rel_end; rel += 2) {
-    if (rel + 1 < rel_end) load_row(rel + 1, wb);
-    process(wa, rel);
-    if (rel + 1 >= rel_end) break;
-    if (rel + 2 < rel_end) load_row(rel + 2, wa);
-    process(wb, rel + 1);
+  const int body_lo = min(j_lo + R - 1, rel_end);
+  const int body_hi = max(body_lo, min(j_hi, rel_end));
+  auto masked_row = [&](int rel) {
+    uint32_t wv[NW];
+    load_row(rel, wv);
+    unsigned mask = 0;
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+      if (rel - r >= j_lo && rel - r < j_hi) mask |= 1u << r;
+    row_fixed<R, WT, false, BOX>(wv, tmpl_s, rel, mask, sI, sQ, sT, a);
+  };
+  for (int rel = j_lo; rel < body_lo; ++rel) masked_row(rel);
+  {
+    uint32_t wa[NW], wb[NW];
+    int rel = body_lo;
+    load_row(rel, wa);
+    for (; rel + 1 < body_hi; rel += 2) {
+      load_row(rel + 1, wb);
+      row_fixed<R, WT, true, BOX>(wa, tmpl_s, rel, 0u, sI, sQ, sT, a);
+      load_row(rel + 2, wa);
+      row_fixed<R, WT, true, BOX>(wb, tmpl_s, rel + 1, 0u, sI, sQ, sT, a);
+    }
+    if (rel < body_hi) row_fixed<R, WT, true, BOX>(wa, tmpl_s, rel, 0u, sI, sQ, sT, a);
   }
-  if (kSplit > 1) {
+  for (int rel = body_hi; rel < rel_end; ++rel) masked_row(rel);
+  if (KS > 1) {
     // groups 1.. hand their partial sums to group 0 through shared memory
-    constexpr int E = 3 * R * kCols;
+    constexpr int NS = BOX ? 1 : 3;          // sums exchanged per column
+    constexpr int E = NS * R * kCols;
     uint32_t *part = reinterpret_cast<uint32_t *>(tile + size_t(TY + a.ht - 1) * RB);
     __syncthreads();                        // tile reads done; part may be written
     if (ks > 0) {
@@ -419,29 +483,37 @@ __global__ void __launch_bounds__(kFixedThreads, CORR_NCC_MINB)
       for (int r = 0; r < R; ++r)
 #pragma unroll
         for (int c = 0; c < kCols; ++c) {
-          const int e = (r * kCols + c) * 3;
-          dst[(e + 0) * 32] = sI[r][c];
-          dst[(e + 1) * 32] = sQ[r][c];
-          dst[(e + 2) * 32] = sT[r][c];
+          const int e = (r * kCols + c) * NS;
+          if (BOX) {
+            dst[e * 32] = sT[r][c];
+          } else {
+            dst[(e + 0) * 32] = sI[r][c];
+            dst[(e + 1) * 32] = sQ[r][c];
+            dst[(e + 2) * 32] = sT[r][c];
+          }
         }
     }
     __syncthreads();
     if (ks > 0) return;
 #pragma unroll 1
-    for (int g = 1; g < kSplit; ++g) {
+    for (int g = 1; g < KS; ++g) {
       const uint32_t *src = part + ((g - 1) * kWarpsPerCta + warp) * E * 32 + lane;
 #pragma unroll
       for (int r = 0; r < R; ++r)
 #pragma unroll
         for (int c = 0; c < kCols; ++c) {
-          const int e = (r * kCols + c) * 3;
-          sI[r][c] += src[(e + 0) * 32];
-          sQ[r][c] += src[(e + 1) * 32];
-          sT[r][c] += src[(e + 2) * 32];
+          const int e = (r * kCols + c) * NS;
+          if (BOX) {
+            sT[r][c] += src[e * 32];
+          } else {
+            sI[r][c] += src[(e + 0) * 32];
+            sQ[r][c] += src[(e + 1) * 32];
+            sT[r][c] += src[(e + 2) * 32];
+          }
         }
     }
   }
-  epilogue<R>(a, x0, y0, sI, sQ, sT, sum_t, template_rsqrt(a, sum_t, sum_t_sq));
+  epilogue<R, BOX>(a, x0, y0, sI, sQ, sT, sum_t, template_rsqrt(a, sum_t, sum_t_sq));
 }
 
 // General path: any template width (multiple of 4) and any image alignment.
@@ -526,13 +598,13 @@ cudaError_t launch(Kernel kernel, const NccArgs &a, size_t smem,
   return cudaGetLastError();
 }
 
-// One CTA per tile.
+// One CTA of `threads` per tile.
 template <typename Kernel>
-cudaError_t launch_tiles(Kernel kernel, const NccArgs &a, size_t smem,
+cudaError_t launch_tiles(Kernel kernel, const NccArgs &a, size_t smem, int threads,
                          cudaStream_t stream) {
   cudaError_t e = set_smem(kernel, smem);
   if (e != cudaSuccess) return e;
-  kernel<<<a.units, kFixedThreads, smem, stream>>>(a);
+  kernel<<<a.units, threads, smem, stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -543,25 +615,33 @@ constexpr int kMaxFixedWords = 32;
 constexpr int kNarrowWords = 16;
 using FixedLauncher = cudaError_t (*)(const NccArgs &, size_t, int, cudaStream_t);
 
-template <int R, int WT>
+template <int R, int WT, bool BOX>
 cudaError_t launch_fixed(const NccArgs &a, size_t smem, int vb, cudaStream_t stream) {
-  return vb == 16 ? launch_tiles(ncc_u8_fixed_kernel<R, WT, 16>, a, smem, stream)
-       : vb == 8  ? launch_tiles(ncc_u8_fixed_kernel<R, WT, 8>, a, smem, stream)
-                  : launch_tiles(ncc_u8_fixed_kernel<R, WT, 1>, a, smem, stream);
+  constexpr int T = FixedShape<BOX>::kThreadsPerCta;
+  return vb == 16 ? launch_tiles(ncc_u8_fixed_kernel<R, WT, 16, BOX>, a, smem, T, stream)
+       : vb == 8  ? launch_tiles(ncc_u8_fixed_kernel<R, WT, 8, BOX>, a, smem, T, stream)
+                  : launch_tiles(ncc_u8_fixed_kernel<R, WT, 1, BOX>, a, smem, T, stream);
 }
 
 // Launchers of template words FIRST + 0 .. FIRST + sizeof...(Ks) - 1.
-template <int R, int FIRST, int... Ks>
+template <int R, bool BOX, int FIRST, int... Ks>
 constexpr std::array<FixedLauncher, sizeof...(Ks)> fixed_launchers(
     std::integer_sequence<int, Ks...>) {
-  return {{launch_fixed<R, FIRST + Ks>...}};
+  return {{launch_fixed<R, FIRST + Ks, BOX>...}};
 }
 
 }  // namespace ncc
 
 // Fast path for templates of kNarrowWords + 1 .. kMaxFixedWords words
-// (ncc_u8_wide.cu).
+// (ncc_u8_wide.cu), and its SumIT-only form (ncc_u8_box_wide.cu).
 cudaError_t ncc_u8_launch_fixed_wide(const ncc::NccArgs &a, size_t smem, int vb,
                                      cudaStream_t stream);
+cudaError_t ncc_u8_launch_fixed_box_wide(const ncc::NccArgs &a, size_t smem, int vb,
+                                         cudaStream_t stream);
+
+// Box-sum variant of the fast path (ncc_u8_box.cu): horizontal and vertical
+// box passes for SumI / SumISq (into a.sums planes 0 and 1, or into pool
+// scratch when a.sums is null), then the SumIT-only tiled kernel.
+cudaError_t ncc_u8_launch_box(ncc::NccArgs a, size_t smem, int vb, cudaStream_t stream);
 
 }  // namespace corr

@@ -11,7 +11,7 @@ cudaError_t ncc_u8_launch_fixed_wide(const ncc::NccArgs &a, size_t smem, int vb,
   constexpr int R = CORR_NCC_ROWS;
   constexpr int kWide = kMaxFixedWords - kNarrowWords;
   static constexpr auto table =
-      fixed_launchers<R, kNarrowWords + 1>(std::make_integer_sequence<int, kWide>{});
+      fixed_launchers<R, false, kNarrowWords + 1>(std::make_integer_sequence<int, kWide>{});
   if (a.wtw <= kNarrowWords || a.wtw > kMaxFixedWords) return cudaErrorInvalidValue;
   return table[a.wtw - kNarrowWords - 1](a, smem, vb, stream);
 }

@@ -1059,49 +1059,6 @@ cudaError_t launch_tiny(const float *left, int nl, const float *right, int nr, i
 
 }  // namespace
 
-// Temporary device memory for split-row partial sums: stream-ordered
-// allocations from one library-owned pool per device whose release threshold
-// is unlimited, so blocks freed by one call are reused by the next without
-// going back to the driver.
-namespace {
-
-constexpr int kMaxDevices = 64;
-std::mutex g_pool_mu;
-cudaMemPool_t g_pools[kMaxDevices] = {};
-
-cudaError_t scratch_pool(cudaMemPool_t *pool) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_pool_mu);
-  if (!g_pools[dev]) {
-    cudaMemPoolProps props = {};
-    props.allocType = cudaMemAllocationTypePinned;
-    props.location.type = cudaMemLocationTypeDevice;
-    props.location.id = dev;
-    cudaMemPool_t p;
-    if ((e = cudaMemPoolCreate(&p, &props)) != cudaSuccess) return e;
-    uint64_t keep = ~uint64_t(0);
-    if ((e = cudaMemPoolSetAttribute(p, cudaMemPoolAttrReleaseThreshold, &keep)) !=
-        cudaSuccess) {
-      cudaMemPoolDestroy(p);
-      return e;
-    }
-    g_pools[dev] = p;
-  }
-  *pool = g_pools[dev];
-  return cudaSuccess;
-}
-
-cudaError_t scratch_alloc(float **ptr, size_t bytes, cudaStream_t stream) {
-  cudaMemPool_t pool;
-  cudaError_t e = scratch_pool(&pool);
-  if (e != cudaSuccess) return e;
-  return cudaMallocFromPoolAsync(reinterpret_cast<void **>(ptr), bytes, pool, stream);
-}
-
-}  // namespace
 
 // Largest shared staging area of the rows kernels (two CTAs per SM),
 // and of the bcast kernel (one CTA per SM at worst).
@@ -1295,7 +1252,7 @@ cudaError_t run_plan(XPlan &pl, float *fixed, cudaStream_t stream) {
   const bool banded = a.nbands * a.nxseg > 1;
   const bool pooled = banded && fixed == nullptr;
   a.part = banded ? fixed : nullptr;
-  if (pooled && (e = scratch_alloc(&a.part, pl.part_bytes, stream)) != cudaSuccess) return e;
+  if (pooled && (e = scratch_alloc(reinterpret_cast<void **>(&a.part), pl.part_bytes, stream)) != cudaSuccess) return e;
   rows_kernel<<<unsigned(pl.blocks), kThreads, pl.smem, stream>>>(a);
   e = cudaGetLastError();
   if (banded && e == cudaSuccess) {

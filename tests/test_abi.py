@@ -53,6 +53,16 @@ def test_stream_is_thread_local_setting():
     assert lib.corr_get_stream() is None
 
 
+def test_ncc_method_setting():
+    lib = corr.load()
+    assert lib.corr_ncc_get_method() == 1                  # box by default
+    assert lib.corr_ncc_set_method(0) == 0
+    assert lib.corr_ncc_get_method() == 0
+    assert lib.corr_ncc_set_method(2) == -1                # unknown: unchanged
+    assert lib.corr_ncc_get_method() == 0
+    assert lib.corr_ncc_set_method(1) == 0
+
+
 @pytest.mark.parametrize("args,code", [
     ((None, 16, 16, FAKE, 4, 4, FAKE, FAKE), -1),            # null image
     ((FAKE, 16, 16, None, 4, 4, FAKE, FAKE), -1),            # null template

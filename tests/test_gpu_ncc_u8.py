@@ -24,10 +24,10 @@ NT = max(1, os.cpu_count() or 1)
 RNG = np.random.default_rng(424242)
 
 
-def run_gpu(image, tmpl, sums=True, coef=True):
+def run_gpu(image, tmpl, sums=True, coef=True, method=None):
     dev = torch.device("cuda", 0)
     s, c = corr.ncc_u8(torch.from_numpy(image).to(dev), torch.from_numpy(tmpl).to(dev),
-                       sums=sums, coef=coef)
+                       sums=sums, coef=coef, method=method)
     torch.cuda.synchronize()
     s = s.cpu().numpy().view(np.uint32) if s is not None else None
     c = c.cpu().numpy() if c is not None else None
@@ -88,13 +88,39 @@ SHAPES = [
 ]
 
 
+@pytest.mark.parametrize("method", ["box", "dp4a"])
 @pytest.mark.parametrize("h,w,wt,ht", SHAPES)
-def test_random_shapes(h, w, wt, ht):
+def test_random_shapes(h, w, wt, ht, method):
     image, tmpl = rand_u8(h, w), rand_u8(ht, wt)
     tmpl[0, :] = 255
     tmpl[-1, -1] = 0
-    s, c = run_gpu(image, tmpl)
+    s, c = run_gpu(image, tmpl, method=method)
     assert_parity(image, tmpl, s, c)
+
+
+def test_methods_agree_bit_for_bit():
+    """Box passes + SumIT kernel and the three-dp4a kernel: the same sums
+    and the same coefficient bits (the epilogue is shared)."""
+    image, tmpl = rand_u8(300, 700), rand_u8(23, 45)
+    sb, cb = run_gpu(image, tmpl, method="box")
+    sd, cd = run_gpu(image, tmpl, method="dp4a")
+    np.testing.assert_array_equal(sb, sd)
+    np.testing.assert_array_equal(cb.view(np.uint32), cd.view(np.uint32))
+    assert_parity(image, tmpl, sb, cb)
+
+
+def test_method_setting_is_per_thread_and_restored():
+    assert corr.ncc_get_method() == "box"
+    corr.ncc_set_method("dp4a")
+    try:
+        image, tmpl = rand_u8(40, 100), rand_u8(5, 7)
+        s, c = run_gpu(image, tmpl, method="box")      # per-call override
+        assert corr.ncc_get_method() == "dp4a"
+        assert_parity(image, tmpl, s, c)
+    finally:
+        corr.ncc_set_method("box")
+    with pytest.raises(ValueError):
+        corr.ncc_set_method("fft")
 
 
 def test_byte_order_single_hot_byte():
@@ -127,12 +153,17 @@ def test_single_offset_and_thin_shapes():
         assert_parity(image, tmpl, s, c)
 
 
-def test_largest_template():
-    """wt*ht = 66048 <= 66052: SumISq close to the uint32 limit."""
-    image, tmpl = rand_u8(260, 264, 200, 256), rand_u8(258, 256, 200, 256)
-    s, c = run_gpu(image, tmpl)
-    assert_parity(image, tmpl, s, c)
-    assert s[1].max() > 2 ** 31   # the top bit of SumISq is in use
+@pytest.mark.parametrize("h,w,wt,ht", [(260, 264, 256, 258), (560, 300, 128, 500)])
+def test_largest_template(h, w, wt, ht):
+    """wt*ht close to 66052: SumISq near the uint32 limit, on the general
+    path (256 x 258) and on the fast path (128 x 500, the tallest 128-wide
+    template whose tile fits) with both methods (the box passes' slides wrap
+    modulo 2^32 and must still land on the exact sums)."""
+    image, tmpl = rand_u8(h, w, 200, 256), rand_u8(ht, wt, 200, 256)
+    for method in ("box", "dp4a"):
+        s, c = run_gpu(image, tmpl, method=method)
+        assert_parity(image, tmpl, s, c)
+        assert s[1].max() > 2 ** 31   # the top bit of SumISq is in use
 
 
 def test_flat_window_and_flat_template_give_zero():
@@ -147,12 +178,14 @@ def test_flat_window_and_flat_template_give_zero():
     assert_parity(image, np.full((8, 16), 9, np.uint8), s, c)
 
 
-def test_sums_only_and_coef_only():
+@pytest.mark.parametrize("method", ["box", "dp4a"])
+def test_sums_only_and_coef_only(method):
+    """Coefficient only: the box method keeps SumI / SumISq in scratch."""
     image, tmpl = rand_u8(70, 270), rand_u8(16, 16)
     ref = oracle.ncc_u8(image, tmpl, nthreads=NT)
-    s, _ = run_gpu(image, tmpl, sums=True, coef=False)
+    s, _ = run_gpu(image, tmpl, sums=True, coef=False, method=method)
     assert_parity(image, tmpl, s, None, ref)
-    _, c = run_gpu(image, tmpl, sums=False, coef=True)
+    _, c = run_gpu(image, tmpl, sums=False, coef=True, method=method)
     assert_parity(image, tmpl, None, c, ref)
 
 
