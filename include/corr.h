@@ -70,20 +70,19 @@ int corr_ncc_u8(const uint8_t *image, int w, int h, const uint8_t *tmpl,
 
 /*
  * corr_ncc_set_method / corr_ncc_get_method -- how corr_ncc_u8 forms SumI
- * and SumISq on its tiled fast kernel (templates up to 128 wide; wider ones
- * always use the first method).  Thread-local, like the stream.  Both
- * methods give bit-identical sums and coefficients.
+ * and SumISq on its tiled fast kernel (templates up to 128 wide; wider or
+ * very tall ones always use the first method).  Thread-local, like the
+ * stream.  Both methods give bit-identical sums and coefficients, and
+ * neither allocates memory.
  *
  *   CORR_NCC_METHOD_DP4A  the section's method: all three sums by unsigned
- *                         dp4a in the tiled kernel.  Allocates nothing.
- *   CORR_NCC_METHOD_BOX   SumI and SumISq as box filters of I and I^2
- *                         (a horizontal and a vertical sliding-sum pass,
- *                         exact in unsigned 32-bit arithmetic), so the tiled
- *                         kernel runs one dp4a per 4 pixels (SumIT) instead
- *                         of three.  Not on the pages.  Takes stream-ordered
- *                         temporary device memory from a library pool:
- *                         8*h*ow bytes, plus 8*oh*ow when sums_out is NULL;
- *                         returns CORR_ECUDA if that allocation fails.
+ *                         dp4a in the tiled kernel.
+ *   CORR_NCC_METHOD_BOX   SumI and SumISq as box filters of I and I^2,
+ *                         formed in the kernel from its staged tile by
+ *                         sliding column and row sums (exact in unsigned
+ *                         32-bit arithmetic), so the dp4a loop runs one
+ *                         dp4a per 4 pixels (SumIT) instead of three.  A
+ *                         reformulation that is not on the pages.
  *
  * corr_ncc_set_method returns CORR_EINVAL for any other value (the method
  * is then unchanged).  The default is CORR_NCC_METHOD_BOX.

@@ -119,9 +119,9 @@ def _u32_empty(shape, device):
 
 def ncc_set_method(method):
     """Select how this thread's ncc_u8 calls form SumI / SumISq on the fast
-    kernel: "dp4a" (three dp4a per 4 pixels, no scratch) or "box" (box-filter
-    passes, then one dp4a per 4 pixels for SumIT; the default).  Results are
-    bit-identical."""
+    kernel: "dp4a" (three dp4a per 4 pixels) or "box" (box filters of the
+    staged tile, then one dp4a per 4 pixels for SumIT; the default).
+    Results are bit-identical."""
     if method not in _NCC_METHODS:
         raise ValueError(f"method must be one of {sorted(_NCC_METHODS)}")
     _check(load().corr_ncc_set_method(_NCC_METHODS[method]))

@@ -16,6 +16,7 @@ int device_sm_count();
 // (device, kernel).
 cudaError_t allow_dynamic_smem(const void *kernel);
 
+
 // Stream-ordered temporary device memory from the library's pool on the
 // current device (scratch.cu); release it with cudaFreeAsync on `stream`.
 cudaError_t scratch_alloc(void **ptr, size_t bytes, cudaStream_t stream);

@@ -29,7 +29,6 @@ cudaError_t ncc_u8_launch(const uint8_t *image, int w, int h,
   a.ow = w - wt + 1;
   a.oh = h - ht + 1;
   a.plane = size_t(a.ow) * a.oh;
-  a.box_i = a.box_q = nullptr;
   const size_t smem = size_t(ht) * a.wtp * 4;   // general path: the template
 
   const bool aligned8 = (reinterpret_cast<uintptr_t>(image) & 7) == 0 && (w & 7) == 0;
@@ -38,8 +37,8 @@ cudaError_t ncc_u8_launch(const uint8_t *image, int w, int h,
     const bool box = method == kMethodBox;
     const int rows = box ? kBoxRows : R;
     const int ty = 2 * rows * kWarpsPerCta;
-    const size_t ts = fixed_tile_smem(ht, a.wtw, a.wtp, rows, box ? kBoxSplit : kSplit,
-                                      box ? 1 : 3);
+    const size_t ts = fixed_tile_layout(ht, a.wtw, a.wtp, rows, box ? kBoxSplit : kSplit,
+                                        box ? 1 : 3, box, wt).total;
     if (ts > 200 * 1024) goto general;   // very tall template: general path
     a.tiles_x = (a.ow + kHalfUnitCols - 1) / kHalfUnitCols;
     const long long tiles = (long long)a.tiles_x * ((a.oh + ty - 1) / ty);

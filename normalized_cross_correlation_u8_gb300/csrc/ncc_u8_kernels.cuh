@@ -94,11 +94,43 @@ struct FixedShape {
 // words), the image tile plus halo (TY+ht-1 rows of 128+4*wtw+8 bytes,
 // rounded to 16) and the exchange area of the template-row split (groups
 // warp groups, ns sums per output).
-inline size_t fixed_tile_smem(int ht, int wtw, int wtp, int rows, int groups, int ns) {
+// Box-sum form: the column sums of the tile's TY output rows (row stride
+// box_v_stride words, stored at x + x/8) and the finished SumI / SumISq of
+// its TY x 128 outputs, each for I and I^2.
+__host__ __device__ inline int box_v_stride(int wt) {
+  const int nv = kHalfUnitCols + wt - 1;              // columns a tile's windows reach
+  const int last = (nv - 1) + ((nv - 1) >> 3);        // skewed index of the last one
+  return ((last + 1 - 16 + 31) & ~31) + 16;           // = 16 mod 32: conflict-free rows
+}
+// The box-sum form reuses dead regions: once the dp4a loop is done, the
+// column sums overwrite the template and the finished SumI / SumISq the
+// tile, so its layout is [tile | exchange | template], each of the first
+// and last at least as large as what later takes its place.
+struct TileLayout {
+  size_t tile, part, tmpl, total;   // byte offsets of the regions, total size
+};
+inline TileLayout fixed_tile_layout(int ht, int wtw, int wtp, int rows, int groups, int ns,
+                                    bool box, int wt) {
   const int ty = 2 * rows * kWarpsPerCta;
   const size_t rb = (kHalfUnitCols + 4 * wtw + 8 + 15) & ~15;
+  const size_t tile = size_t(ty + ht - 1) * rb;
   const size_t part = size_t(groups - 1) * kWarpsPerCta * 32 * ns * rows * kCols * 4;
-  return size_t(ht) * wtp * 4 + size_t(ty + ht - 1) * rb + part;
+  const size_t tmpl = size_t(ht) * wtp * 4;
+  TileLayout l;
+  if (!box) {
+    l.tmpl = 0;
+    l.tile = tmpl;
+    l.part = tmpl + tile;
+    l.total = tmpl + tile + part;
+  } else {
+    const size_t s = size_t(2) * ty * kHalfUnitCols * 4;
+    const size_t v = size_t(2) * ty * box_v_stride(wt) * 4;
+    l.tile = 0;
+    l.part = tile > s ? tile : s;
+    l.tmpl = l.part + part;
+    l.total = l.tmpl + (tmpl > v ? tmpl : v);
+  }
+  return l;
 }
 constexpr uint32_t kOnes = 0x01010101u;
 constexpr int kStageBatch = 4;       // tile chunks per thread loaded ahead of the template
@@ -116,8 +148,6 @@ struct NccArgs {
   uint32_t tail_mask;  // SumISq mask of the last word (0xff in its template bytes)
   int wtp;           // shared-memory template row stride in words (multiple of 4)
   int ow, oh;
-  const uint32_t *box_i;  // BOX kernels: SumI / SumISq planes from the box passes
-  const uint32_t *box_q;  //   (row stride ow; may be the sums_out planes themselves)
   int tiles_x;       // units across a row of outputs
   int units;         // warp units (fast path: 128 cols x 2R rows)
 };
@@ -218,9 +248,7 @@ __device__ __forceinline__ float i64_to_f32(int64_t v) {
 // numerator and the window variance term are exact 64-bit integers; the
 // ratio is num * rsqrt(dI) * rsqrt(dT) in single precision (a few ulp of
 // |coef| <= 1, far inside the 1e-5 bound).  rs_t = rsqrt(dT) is per template.
-// BOX: SumI and SumISq come from the box planes (already written to the
-// sums planes when those are the outputs); only SumIT is stored here.
-template <int R, bool BOX = false>
+template <int R>
 __device__ __forceinline__ void epilogue(const NccArgs &a, int x0, int y0,
                                          const uint32_t (&sI)[R][kCols],
                                          const uint32_t (&sQ)[R][kCols],
@@ -236,13 +264,10 @@ __device__ __forceinline__ void epilogue(const NccArgs &a, int x0, int y0,
       const int x = x0 + c;
       if (x >= a.ow) break;
       const size_t o = size_t(y) * a.ow + x;
-      const uint32_t vi = BOX ? a.box_i[o] : sI[r][c];
-      const uint32_t vq = BOX ? a.box_q[o] : sQ[r][c];
+      const uint32_t vi = sI[r][c], vq = sQ[r][c];
       if (a.sums) {
-        if (!BOX) {
-          a.sums[o] = vi;
-          a.sums[a.plane + o] = vq;
-        }
+        a.sums[o] = vi;
+        a.sums[a.plane + o] = vq;
         a.sums[2 * a.plane + o] = sT[r][c];
       }
       if (a.coef) {
@@ -319,6 +344,71 @@ __device__ __forceinline__ void row_fixed(const uint32_t (&wv)[RowWords<WT>::kWo
   }
 }
 
+// Box-sum form, column step: for each tile column x that a window of the
+// tile reaches (x < 128 + wt - 1) and each output row y < TY of the tile,
+// v[y][x] = sum_{i<ht} tile[y+i][x] and the same of squares; the first
+// window is summed directly, the next TY-1 slide down by one row (exact in
+// unsigned 32-bit arithmetic).  Rows of the tile past the image were not
+// staged; they only reach outputs past oh, which are never stored.
+template <int TY, int RB>
+__device__ __forceinline__ void box_columns(const uint8_t *tile, int ht, int nv, int vs,
+                                            uint32_t *v_i, uint32_t *v_q, int tid,
+                                            int nthreads) {
+  for (int x = tid; x < nv; x += nthreads) {
+    const uint8_t *col = tile + x;
+    uint32_t s = 0, q = 0;
+#pragma unroll 4
+    for (int i = 0; i < ht; ++i) {
+      const uint32_t b = col[i * RB];
+      s += b;
+      q += b * b;
+    }
+    const int xs = x + (x >> 3);
+    v_i[xs] = s;
+    v_q[xs] = q;
+#pragma unroll
+    for (int y = 1; y < TY; ++y) {
+      const uint32_t bi = col[(y + ht - 1) * RB], bo = col[(y - 1) * RB];
+      s += bi - bo;
+      q += bi * bi - bo * bo;
+      v_i[y * vs + xs] = s;
+      v_q[y * vs + xs] = q;
+    }
+  }
+}
+
+// Box-sum form, row step: SumI[y][c] = sum_{j<wt} v[y][c+j] (and SumISq)
+// for the tile's TY x 128 outputs, a thread per run of 8 columns (the first
+// sum direct, the next 7 sliding by one column), into s_i / s_q [TY][128].
+template <int TY>
+__device__ __forceinline__ void box_rows(const uint32_t *v_i, const uint32_t *v_q, int wt,
+                                         int vs, uint32_t *s_i, uint32_t *s_q, int tid,
+                                         int nthreads) {
+  constexpr int kRuns = kHalfUnitCols / kCols;
+  for (int u = tid; u < TY * kRuns; u += nthreads) {
+    const int y = u / kRuns, c0 = (u - y * kRuns) * kCols;
+    const uint32_t *ri = v_i + y * vs, *rq = v_q + y * vs;
+    uint32_t s = 0, q = 0;
+#pragma unroll 4
+    for (int j = 0; j < wt; ++j) {
+      const int x = c0 + j, xs = x + (x >> 3);
+      s += ri[xs];
+      q += rq[xs];
+    }
+    uint32_t *oi = s_i + y * kHalfUnitCols + c0, *oq = s_q + y * kHalfUnitCols + c0;
+    oi[0] = s;
+    oq[0] = q;
+#pragma unroll
+    for (int c = 1; c < kCols; ++c) {
+      const int xo = c0 + c - 1, xi = xo + wt;
+      s += ri[xi + (xi >> 3)] - ri[xo + (xo >> 3)];
+      q += rq[xi + (xi >> 3)] - rq[xo + (xo >> 3)];
+      oi[c] = s;
+      oq[c] = q;
+    }
+  }
+}
+
 // Fast path: template width WT words known at compile time, any image
 // alignment (the staging unit VB follows it).
 //
@@ -357,8 +447,19 @@ __global__ void __launch_bounds__(FixedShape<BOX>::kThreadsPerCta,
   constexpr int RB = TileGeom<WT>::kRowBytes;
   constexpr int TY = 2 * R * kWarpsPerCta;
   extern __shared__ uint4 smem_u4[];
-  uint32_t *tmpl_s = reinterpret_cast<uint32_t *>(smem_u4);
-  uint8_t *tile = reinterpret_cast<uint8_t *>(smem_u4) + size_t(a.ht) * WTP * 4;
+  uint8_t *smem = reinterpret_cast<uint8_t *>(smem_u4);
+  constexpr int NS = BOX ? 1 : 3;                     // sums exchanged per column
+  constexpr int E = NS * R * kCols;
+  const size_t tile_bytes = size_t(TY + a.ht - 1) * RB;
+  const size_t part_bytes = size_t(KS - 1) * kWarpsPerCta * E * 32 * 4;
+  const size_t s_bytes = size_t(2) * TY * kHalfUnitCols * 4;
+  // regions as fixed_tile_layout places them
+  uint8_t *tile = BOX ? smem : smem + size_t(a.ht) * WTP * 4;
+  uint32_t *part = reinterpret_cast<uint32_t *>(
+      BOX ? smem + (tile_bytes > s_bytes ? tile_bytes : s_bytes) : tile + tile_bytes);
+  uint32_t *tmpl_s = BOX ? reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(part) +
+                                                        part_bytes)
+                         : reinterpret_cast<uint32_t *>(smem);
   __shared__ uint32_t red[2];
 
   const int tx = blockIdx.x % a.tiles_x, ty = blockIdx.x / a.tiles_x;
@@ -408,6 +509,12 @@ __global__ void __launch_bounds__(FixedShape<BOX>::kThreadsPerCta,
   for (int i = threadIdx.x + kStageBatch * kFixedThreads; i < nchunks; i += kFixedThreads)
     chunk_store(i, chunk_load(i));
   __syncthreads();
+
+  // BOX: column sums over the template, SumI / SumISq over the tile, each
+  // once the region is dead
+  const int vs = BOX ? box_v_stride(a.wt) : 0;
+  uint32_t *v_i = tmpl_s, *v_q = v_i + TY * vs;
+  uint32_t *s_i = reinterpret_cast<uint32_t *>(tile), *s_q = s_i + TY * kHalfUnitCols;
 
   const int warp_id = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int warp = warp_id % kWarpsPerCta;            // row group of the tile
@@ -471,12 +578,11 @@ __global__ void __launch_bounds__(FixedShape<BOX>::kThreadsPerCta,
     if (rel < body_hi) row_fixed<R, WT, true, BOX>(wa, tmpl_s, rel, 0u, sI, sQ, sT, a);
   }
   for (int rel = body_hi; rel < rel_end; ++rel) masked_row(rel);
-  if (KS > 1) {
-    // groups 1.. hand their partial sums to group 0 through shared memory
-    constexpr int NS = BOX ? 1 : 3;          // sums exchanged per column
-    constexpr int E = NS * R * kCols;
-    uint32_t *part = reinterpret_cast<uint32_t *>(tile + size_t(TY + a.ht - 1) * RB);
-    __syncthreads();                        // tile reads done; part may be written
+  if (KS > 1 || BOX) {
+    // groups 1.. hand their partial sums to group 0 through shared memory;
+    // BOX: all threads form the column sums from the tile (into the
+    // template's place), then the last group the box sums (into the tile's)
+    __syncthreads();                        // template and tile reads done
     if (ks > 0) {
       uint32_t *dst = part + ((ks - 1) * kWarpsPerCta + warp) * E * 32 + lane;
 #pragma unroll
@@ -492,6 +598,13 @@ __global__ void __launch_bounds__(FixedShape<BOX>::kThreadsPerCta,
             dst[(e + 2) * 32] = sT[r][c];
           }
         }
+    }
+    if constexpr (BOX) {
+      box_columns<TY, RB>(tile, a.ht, kHalfUnitCols + a.wt - 1, vs, v_i, v_q, threadIdx.x,
+                          kFixedThreads);
+      __syncthreads();                      // column sums done, tile dead
+      if (ks == KS - 1)
+        box_rows<TY>(v_i, v_q, a.wt, vs, s_i, s_q, threadIdx.x - ks * kThreads, kThreads);
     }
     __syncthreads();
     if (ks > 0) return;
@@ -512,8 +625,20 @@ __global__ void __launch_bounds__(FixedShape<BOX>::kThreadsPerCta,
           }
         }
     }
+    if constexpr (BOX) {
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int c = 0; c < kCols; c += 4) {
+          const int o = (yr0 + r) * kHalfUnitCols + hl * kCols + c;
+          const uint4 vi = *reinterpret_cast<const uint4 *>(s_i + o);
+          const uint4 vq = *reinterpret_cast<const uint4 *>(s_q + o);
+          sI[r][c] = vi.x; sI[r][c + 1] = vi.y; sI[r][c + 2] = vi.z; sI[r][c + 3] = vi.w;
+          sQ[r][c] = vq.x; sQ[r][c + 1] = vq.y; sQ[r][c + 2] = vq.z; sQ[r][c + 3] = vq.w;
+        }
+    }
   }
-  epilogue<R, BOX>(a, x0, y0, sI, sQ, sT, sum_t, template_rsqrt(a, sum_t, sum_t_sq));
+  epilogue<R>(a, x0, y0, sI, sQ, sT, sum_t, template_rsqrt(a, sum_t, sum_t_sq));
 }
 
 // General path: any template width (multiple of 4) and any image alignment.
@@ -639,9 +764,9 @@ cudaError_t ncc_u8_launch_fixed_wide(const ncc::NccArgs &a, size_t smem, int vb,
 cudaError_t ncc_u8_launch_fixed_box_wide(const ncc::NccArgs &a, size_t smem, int vb,
                                          cudaStream_t stream);
 
-// Box-sum variant of the fast path (ncc_u8_box.cu): horizontal and vertical
-// box passes for SumI / SumISq (into a.sums planes 0 and 1, or into pool
-// scratch when a.sums is null), then the SumIT-only tiled kernel.
-cudaError_t ncc_u8_launch_box(ncc::NccArgs a, size_t smem, int vb, cudaStream_t stream);
+// Box-sum form of the fast path (ncc_u8_box.cu): SumI / SumISq as box
+// filters of the staged tile, SumIT alone by dp4a.
+cudaError_t ncc_u8_launch_box(const ncc::NccArgs &a, size_t smem, int vb,
+                              cudaStream_t stream);
 
 }  // namespace corr

@@ -42,7 +42,6 @@
 
 #include <stdlib.h>
 
-#include <mutex>
 #include <utility>
 
 #include "internal.cuh"
@@ -1292,56 +1291,5 @@ cudaError_t xcorr_f32_launch_scratch(const float *left, int nl, const float *rig
   return run_plan(pl, scratch, stream);
 }
 
-// ---------------------------------------------------------------------------
-// Per-device cached launch attributes.
-// ---------------------------------------------------------------------------
-namespace {
-constexpr int kAttrDevices = 64;
-std::mutex g_attr_mu;
-int g_sms[kAttrDevices] = {};
-int g_smem_optin[kAttrDevices] = {};
-const void *g_smem_done[kAttrDevices][16] = {};
-}  // namespace
-
-int device_sm_count() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kAttrDevices) return 1;
-  std::lock_guard<std::mutex> lock(g_attr_mu);
-  if (!g_sms[dev]) {
-    int sms = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        sms <= 0)
-      return 1;
-    g_sms[dev] = sms;
-  }
-  return g_sms[dev];
-}
-
-cudaError_t allow_dynamic_smem(const void *kernel) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kAttrDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_attr_mu);
-  int slot = 0;
-  for (; slot < 16 && g_smem_done[dev][slot]; ++slot)
-    if (g_smem_done[dev][slot] == kernel) return cudaSuccess;
-  if (!g_smem_optin[dev]) {
-    int v = 0;
-    if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
-        cudaSuccess)
-      return e;
-    g_smem_optin[dev] = v;
-  }
-  // dynamic + the kernel's static shared memory may not exceed the opt-in limit
-  cudaFuncAttributes fa;
-  if ((e = cudaFuncGetAttributes(&fa, kernel)) != cudaSuccess) return e;
-  const int dyn = g_smem_optin[dev] - int(fa.sharedSizeBytes);
-  if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn)) !=
-      cudaSuccess)
-    return e;
-  if (slot < 16) g_smem_done[dev][slot] = kernel;
-  return cudaSuccess;
-}
 
 }  // namespace corr

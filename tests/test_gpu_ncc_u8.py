@@ -153,12 +153,12 @@ def test_single_offset_and_thin_shapes():
         assert_parity(image, tmpl, s, c)
 
 
-@pytest.mark.parametrize("h,w,wt,ht", [(260, 264, 256, 258), (560, 300, 128, 500)])
+@pytest.mark.parametrize("h,w,wt,ht", [(260, 264, 256, 258), (440, 300, 128, 430)])
 def test_largest_template(h, w, wt, ht):
     """wt*ht close to 66052: SumISq near the uint32 limit, on the general
-    path (256 x 258) and on the fast path (128 x 500, the tallest 128-wide
-    template whose tile fits) with both methods (the box passes' slides wrap
-    modulo 2^32 and must still land on the exact sums)."""
+    path (256 x 258) and on the fast path (128 x 430, a tile that fits the
+    shared memory of both forms) with both methods (the box sums' slides
+    wrap modulo 2^32 and must still land on the exact sums)."""
     image, tmpl = rand_u8(h, w, 200, 256), rand_u8(ht, wt, 200, 256)
     for method in ("box", "dp4a"):
         s, c = run_gpu(image, tmpl, method=method)
