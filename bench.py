@@ -4,16 +4,19 @@
 
 One step = one corr_ncc_u8 call over the 1920x1080 uint8 image with a 32x32
 template (every valid offset: SumI, SumISq, SumIT and the coefficient), i.e.
-template prep, tile loads, window packing, dp4a accumulation and the
-epilogue, all in one launch.  Inputs are resident in HBM when the timed
+template prep, tile loads, window packing, dp4a accumulation, the box sums
+and the epilogue, all in one launch, with the library's default method (the
+box form: SumI / SumISq as box filters of the staged tile, SumIT by one
+unsigned dp4a per 4 pixels).  Inputs are resident in HBM when the timed
 region starts; a 256 MB buffer is written between steps so every step starts
 with a cold L2 (the workload's inputs and outputs would otherwise fit in the
 129 MB L2).  Prints one JSON line.
 
-The line also carries, per workload, the kernel-only throughput and its
-roofline fraction for the other five workloads (u8 256x256 / 4096x4096 and
-the three f32 cross-correlation batches), an end-to-end number through host
-buffers, and the CPU oracle's throughput on a bounded sample.
+The line also carries the same step with the pages' method (all three sums
+by dp4a, "method_dp4a"), per workload the kernel-only throughput of both
+methods and its roofline fraction for the other five workloads (u8 256x256 /
+4096x4096 and the three f32 cross-correlation batches), an end-to-end number
+through host buffers, and the CPU oracle's throughput on a bounded sample.
 
 --impl reference times the CPU oracle (the only reference implementation:
 the pages ship no code) on the same workload and metric.
@@ -230,14 +233,14 @@ def traffic_for(kernel_key, src_paths):
 # our arm
 # --------------------------------------------------------------------------
 
-def ncc_buffers(torch, corr, w, dev):
+def ncc_buffers(torch, corr, w, dev, method=None):
     img = torch.from_numpy(w.image).to(dev)
     tm = torch.from_numpy(w.tmpl).to(dev)
     h, ww = w.image.shape
     ht, wt = w.tmpl.shape
     s = torch.empty((3, h - ht + 1, ww - wt + 1), dtype=torch.int32, device=dev)
     c = torch.empty((h - ht + 1, ww - wt + 1), dtype=torch.float32, device=dev)
-    return img, tm, s, c, (lambda: corr.ncc_u8_into(img, tm, s, c))
+    return img, tm, s, c, (lambda: corr.ncc_u8_into(img, tm, s, c, method=method))
 
 
 def xcorr_buffers(torch, corr, w, dev):
@@ -249,9 +252,12 @@ def xcorr_buffers(torch, corr, w, dev):
     return L, R, out, (lambda: corr.xcorr_f32_into(L, R, out))
 
 
-def dp4a_per_offset(w):
+def dp4a_per_offset(w, method="box"):
+    """Unsigned dp4a per offset: one per 4-pixel template word for SumIT
+    (box form), three for the pages' method."""
     ht, wt = w.tmpl.shape
-    return 3 * (wt * ht) // 4
+    words = (wt + 3) // 4 * ht
+    return words if method == "box" else 3 * words
 
 
 def run_ours(args, world, rank, local):
@@ -297,16 +303,20 @@ def run_ours(args, world, rank, local):
     dp4a_peak = sms * DP4A_PER_SM_CLK * SM_MAX_MHZ_NOMINAL * 1e6
     achieved = w.offsets * dp4a_per_offset(w) / avg_launch_s
     ncc_src = [os.path.join(ROOT, "normalized_cross_correlation_u8_gb300", "csrc", f)
-               for f in ("ncc_u8.cu", "ncc_u8_kernels.cuh")]
+               for f in ("ncc_u8.cu", "ncc_u8_box.cu", "ncc_u8_kernels.cuh")]
     roofline = {
-        "bound": "alu", "kernel": "ncc_u8_fixed_kernel (unsigned dp4a issue)",
+        "bound": "alu",
+        "kernel": "ncc_u8_fixed_kernel, box form (unsigned dp4a issue; SumIT only)",
         "achieved": achieved / 1e12, "peak": dp4a_peak / 1e12, "unit": "Tdp4a/s",
         "frac": achieved / dp4a_peak,
         "peak_basis": f"{sms} SMs x {DP4A_PER_SM_CLK} dp4a/clk x {SM_MAX_MHZ_NOMINAL:.0f} MHz max clock",
         "frac_at_live_clock": achieved / (sms * DP4A_PER_SM_CLK * sm_mhz * 1e6),
         "probe_dp4a_per_s": dp4a_probe / 1e12,
-        "algorithmic_per_unit": f"{dp4a_per_offset(w)} dp4a per offset (3 per 4 template pixels)",
-        "traffic": traffic_for("ncc_u8_1080p", ncc_src),
+        "algorithmic_per_unit": (f"{dp4a_per_offset(w)} dp4a per offset (1 per 4 template "
+                                 "pixels, SumIT; SumI / SumISq are box sums: "
+                                 f"{w.tmpl.shape[0] + w.tmpl.shape[1]} adds per offset "
+                                 "amortised, not counted)"),
+        "traffic": traffic_for("ncc_u8_1080p_box", ncc_src),
         "hbm_bytes_algorithmic": int(w.image.size + w.tmpl.size + 16 * w.offsets),
     }
 
@@ -326,6 +336,7 @@ def run_ours(args, world, rank, local):
     }
 
     if args.extras and rank == 0:
+        line["method_dp4a"] = method_dp4a_headline(torch, corr, w, dev, flush, sms, args)
         line["per_workload"] = extras_workloads(torch, corr, wl, dev, flush, sms,
                                                 dp4a_probe, ffma_probe)
         line["e2e"] = e2e_headline(torch, corr, w, dev, args)
@@ -333,6 +344,28 @@ def run_ours(args, world, rank, local):
     elif args.extras:
         line["e2e"] = None
     return line
+
+
+def method_dp4a_headline(torch, corr, w, dev, flush, sms, args):
+    """The headline step with the pages' method (SumI, SumISq and SumIT all
+    by dp4a in the tiled kernel), event-timed the same way, for comparison."""
+    *_, fn = ncc_buffers(torch, corr, w, dev, method="dp4a")
+    for _ in range(3):
+        flush()
+        fn()
+    steps = max(50, min(args.steps // 5, 2000))
+    t = event_time_steps(torch, fn, steps, flush)
+    avg_s = (sum(t) / steps) * 1e-3
+    dp4a_peak = sms * DP4A_PER_SM_CLK * SM_MAX_MHZ_NOMINAL * 1e6
+    achieved = w.offsets * dp4a_per_offset(w, "dp4a") / avg_s
+    return {"value": w.offsets / avg_s, "unit": UNIT, "steps": steps,
+            "ms_per_step": avg_s * 1e3,
+            "roofline": {"bound": "alu",
+                         "kernel": "ncc_u8_fixed_kernel (unsigned dp4a issue; 3 sums)",
+                         "achieved": achieved / 1e12, "peak": dp4a_peak / 1e12,
+                         "unit": "Tdp4a/s", "frac": achieved / dp4a_peak,
+                         "algorithmic_per_unit": f"{dp4a_per_offset(w, 'dp4a')} dp4a per "
+                                                 "offset (3 per 4 template pixels)"}}
 
 
 # Per-workload kernel durations: device time per launch from replaying a
@@ -348,21 +381,27 @@ def extras_workloads(torch, corr, wl, dev, flush, sms, dp4a_probe, ffma_probe):
     ffma_peak = sms * FFMA_PER_SM_CLK * SM_MAX_MHZ_NOMINAL * 1e6
     for key, make in wl.NCC_WORKLOADS.items():
         w = make()
-        *_, fn = ncc_buffers(torch, corr, w, dev)
-        reps = 30 if w.offsets > 1e7 else 200
-        for _ in range(3):
-            fn()
-        t = event_time_steps(torch, fn, reps, flush)
-        ms = statistics.median(t)
-        rate = w.offsets * dp4a_per_offset(w) / (ms * 1e-3)
-        gms = graph_time_per_call(torch, fn)
-        grate = w.offsets * dp4a_per_offset(w) / (gms * 1e-3)
-        out[key] = {"workload": w.name, "offsets_per_s": w.offsets / (ms * 1e-3),
-                    "us_per_launch": ms * 1e3, "us_per_launch_graph_warm_l2": gms * 1e3,
-                    "roofline": {"bound": "alu", "achieved": grate / 1e12,
-                                 "peak": dp4a_peak / 1e12, "unit": "Tdp4a/s",
-                                 "frac": grate / dp4a_peak, "timing": ROOFLINE_TIMING,
-                                 "frac_single_launch": rate / dp4a_peak}}
+        for method in ("box", "dp4a"):
+            *_, fn = ncc_buffers(torch, corr, w, dev, method=method)
+            reps = 30 if w.offsets > 1e7 else 200
+            for _ in range(3):
+                fn()
+            t = event_time_steps(torch, fn, reps, flush)
+            ms = statistics.median(t)
+            per = dp4a_per_offset(w, method)
+            rate = w.offsets * per / (ms * 1e-3)
+            gms = graph_time_per_call(torch, fn)
+            grate = w.offsets * per / (gms * 1e-3)
+            out[key if method == "box" else key + "_dp4a"] = {
+                "workload": w.name, "method": method,
+                "offsets_per_s": w.offsets / (ms * 1e-3),
+                "offsets_per_s_graph_warm_l2": w.offsets / (gms * 1e-3),
+                "us_per_launch": ms * 1e3, "us_per_launch_graph_warm_l2": gms * 1e3,
+                "roofline": {"bound": "alu", "achieved": grate / 1e12,
+                             "peak": dp4a_peak / 1e12, "unit": "Tdp4a/s",
+                             "frac": grate / dp4a_peak, "timing": ROOFLINE_TIMING,
+                             "frac_single_launch": rate / dp4a_peak,
+                             "algorithmic_per_unit": f"{per} dp4a per offset"}}
     for key, make in wl.XCORR_WORKLOADS.items():
         w = make()
         *_, fn = xcorr_buffers(torch, corr, w, dev)

@@ -29,13 +29,22 @@ cudaError_t ncc_u8_launch(const uint8_t *image, int w, int h,
   a.ow = w - wt + 1;
   a.oh = h - ht + 1;
   a.plane = size_t(a.ow) * a.oh;
+  a.rows = R;
   const size_t smem = size_t(ht) * a.wtp * 4;   // general path: the template
 
   const bool aligned8 = (reinterpret_cast<uintptr_t>(image) & 7) == 0 && (w & 7) == 0;
   const bool aligned16 = (reinterpret_cast<uintptr_t>(image) & 15) == 0 && (w & 15) == 0;
   if (a.wtw >= 1 && a.wtw <= kMaxFixedWords) {
     const bool box = method == kMethodBox;
-    const int rows = box ? kBoxRows : R;
+    auto tiles_for = [&](int rows) {
+      return (long long)((a.ow + kHalfUnitCols - 1) / kHalfUnitCols) *
+             ((a.oh + 2 * rows * kWarpsPerCta - 1) / (2 * rows * kWarpsPerCta));
+    };
+    int rows = box ? kBoxRows : R;
+    if (box && kBoxRows != 1 && a.wtw <= kBoxNarrowWords &&
+        tiles_for(kBoxRows) < (long long)CORR_NCC_BOX_NARROW_TILES_PER_SM * device_sm_count())
+      rows = 1;
+    a.rows = rows;
     const int ty = 2 * rows * kWarpsPerCta;
     const size_t ts = fixed_tile_layout(ht, a.wtw, a.wtp, rows, box ? kBoxSplit : kSplit,
                                         box ? 1 : 3, box, wt).total;

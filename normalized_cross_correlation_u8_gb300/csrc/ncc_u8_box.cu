@@ -13,17 +13,26 @@
 // reformulation is not on the pages.
 #include "ncc_u8_kernels.cuh"
 
+static_assert(corr::ncc::kBoxNarrowWords >= 0 &&
+                  corr::ncc::kBoxNarrowWords < corr::ncc::kNarrowWords,
+              "narrow box widths must be a strict subset of ncc_u8_box.cu's table");
+
 namespace corr {
 
 cudaError_t ncc_u8_launch_box(const ncc::NccArgs &a, size_t smem, int vb,
                               cudaStream_t stream) {
   using namespace ncc;
-  constexpr int R = kBoxRows;
   if (a.wtw < 1 || a.wtw > kMaxFixedWords) return cudaErrorInvalidValue;
   if (a.wtw > kNarrowWords) return ncc_u8_launch_fixed_box_wide(a, smem, vb, stream);
-  static constexpr auto table =
-      fixed_launchers<R, true, 1>(std::make_integer_sequence<int, kNarrowWords>{});
-  return table[a.wtw - 1](a, smem, vb, stream);
+  // a.rows output rows per half-warp: kBoxRows, or 1 for narrow templates
+  // (the launch geometry in a.units was computed for it)
+  static constexpr auto narrow = fixed_launchers<1, true, 1>(
+      std::make_integer_sequence<int, kBoxNarrowWords>{});
+  static constexpr auto table = fixed_launchers<kBoxRows, true, 1>(
+      std::make_integer_sequence<int, kNarrowWords>{});
+  if (a.rows == kBoxRows) return table[a.wtw - 1](a, smem, vb, stream);
+  if (a.rows == 1 && a.wtw <= kBoxNarrowWords) return narrow[a.wtw - 1](a, smem, vb, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace corr

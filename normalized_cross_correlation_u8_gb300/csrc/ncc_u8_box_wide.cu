@@ -12,7 +12,8 @@ cudaError_t ncc_u8_launch_fixed_box_wide(const ncc::NccArgs &a, size_t smem, int
   constexpr int kWide = kMaxFixedWords - kNarrowWords;
   static constexpr auto table =
       fixed_launchers<R, true, kNarrowWords + 1>(std::make_integer_sequence<int, kWide>{});
-  if (a.wtw <= kNarrowWords || a.wtw > kMaxFixedWords) return cudaErrorInvalidValue;
+  if (a.wtw <= kNarrowWords || a.wtw > kMaxFixedWords || a.rows != R)
+    return cudaErrorInvalidValue;
   return table[a.wtw - kNarrowWords - 1](a, smem, vb, stream);
 }
 

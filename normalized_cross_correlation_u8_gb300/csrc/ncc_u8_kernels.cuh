@@ -63,12 +63,26 @@ constexpr int kHalfUnitCols = 16 * kCols;  // output columns per warp unit (fast
 #ifndef CORR_NCC_KSPLIT
 #define CORR_NCC_KSPLIT 2
 #endif
-// Output rows per half-warp of the SumIT-only kernel (box-sum variant).
+// Output rows per half-warp of the box-sum form: CORR_NCC_BOX_ROWS, or 1
+// for templates of up to CORR_NCC_BOX_NARROW_WORDS words on images whose
+// tiles would fill fewer than CORR_NCC_BOX_NARROW_TILES_PER_SM tiles per SM
+// (smaller tiles then fill the SMs more evenly).
 #ifndef CORR_NCC_BOX_ROWS
 #define CORR_NCC_BOX_ROWS 2
 #endif
+#ifndef CORR_NCC_BOX_NARROW_WORDS
+#define CORR_NCC_BOX_NARROW_WORDS 4
+#endif
+#ifndef CORR_NCC_BOX_NARROW_TILES_PER_SM
+#define CORR_NCC_BOX_NARROW_TILES_PER_SM 16
+#endif
+// Minimum resident CTAs per SM asked of the compiler for the box form:
+// templates of up to 16 words, and wider ones.
 #ifndef CORR_NCC_BOX_MINB
-#define CORR_NCC_BOX_MINB 1
+#define CORR_NCC_BOX_MINB 8
+#endif
+#ifndef CORR_NCC_BOX_MINB_WIDE
+#define CORR_NCC_BOX_MINB_WIDE 1
 #endif
 // Template-row ranges (warp groups) per tile of the SumIT-only kernel.
 #ifndef CORR_NCC_BOX_KSPLIT
@@ -81,6 +95,7 @@ constexpr int kThreads = 32 * kWarpsPerCta;
 // shared memory (integer sums: exact in any order).
 constexpr int kSplit = CORR_NCC_KSPLIT;
 constexpr int kBoxRows = CORR_NCC_BOX_ROWS;
+constexpr int kBoxNarrowWords = CORR_NCC_BOX_NARROW_WORDS;
 constexpr int kBoxSplit = CORR_NCC_BOX_KSPLIT;
 // Warp groups and threads of the fast kernel (BOX: the SumIT-only form).
 template <bool BOX>
@@ -148,6 +163,7 @@ struct NccArgs {
   uint32_t tail_mask;  // SumISq mask of the last word (0xff in its template bytes)
   int wtp;           // shared-memory template row stride in words (multiple of 4)
   int ow, oh;
+  int rows;          // fast path: output rows per half-warp (the kernel's R)
   int tiles_x;       // units across a row of outputs
   int units;         // warp units (fast path: 128 cols x 2R rows)
 };
@@ -379,7 +395,8 @@ __device__ __forceinline__ void box_columns(const uint8_t *tile, int ht, int nv,
 
 // Box-sum form, row step: SumI[y][c] = sum_{j<wt} v[y][c+j] (and SumISq)
 // for the tile's TY x 128 outputs, a thread per run of 8 columns (the first
-// sum direct, the next 7 sliding by one column), into s_i / s_q [TY][128].
+// sum direct, the next 7 sliding by one column), into s_i / s_q [TY][128]
+// (written as 16-byte vectors).
 template <int TY>
 __device__ __forceinline__ void box_rows(const uint32_t *v_i, const uint32_t *v_q, int wt,
                                          int vs, uint32_t *s_i, uint32_t *s_q, int tid,
@@ -395,7 +412,7 @@ __device__ __forceinline__ void box_rows(const uint32_t *v_i, const uint32_t *v_
       s += ri[xs];
       q += rq[xs];
     }
-    uint32_t *oi = s_i + y * kHalfUnitCols + c0, *oq = s_q + y * kHalfUnitCols + c0;
+    uint32_t oi[kCols], oq[kCols];
     oi[0] = s;
     oq[0] = q;
 #pragma unroll
@@ -405,6 +422,13 @@ __device__ __forceinline__ void box_rows(const uint32_t *v_i, const uint32_t *v_
       q += rq[xi + (xi >> 3)] - rq[xo + (xo >> 3)];
       oi[c] = s;
       oq[c] = q;
+    }
+    uint4 *di = reinterpret_cast<uint4 *>(s_i + y * kHalfUnitCols + c0);
+    uint4 *dq = reinterpret_cast<uint4 *>(s_q + y * kHalfUnitCols + c0);
+#pragma unroll
+    for (int c = 0; c < kCols; c += 4) {
+      di[c / 4] = make_uint4(oi[c], oi[c + 1], oi[c + 2], oi[c + 3]);
+      dq[c / 4] = make_uint4(oq[c], oq[c + 1], oq[c + 2], oq[c + 3]);
     }
   }
 }
@@ -439,7 +463,8 @@ struct StageChunk {
 
 template <int R, int WT, int VB, bool BOX>
 __global__ void __launch_bounds__(FixedShape<BOX>::kThreadsPerCta,
-                                  BOX ? CORR_NCC_BOX_MINB : CORR_NCC_MINB)
+                                  !BOX ? CORR_NCC_MINB
+                                  : WT <= 16 ? CORR_NCC_BOX_MINB : CORR_NCC_BOX_MINB_WIDE)
     ncc_u8_fixed_kernel(const NccArgs a) {
   constexpr int KS = FixedShape<BOX>::kGroups;
   constexpr int kFixedThreads = FixedShape<BOX>::kThreadsPerCta;
@@ -581,7 +606,7 @@ __global__ void __launch_bounds__(FixedShape<BOX>::kThreadsPerCta,
   if (KS > 1 || BOX) {
     // groups 1.. hand their partial sums to group 0 through shared memory;
     // BOX: all threads form the column sums from the tile (into the
-    // template's place), then the last group the box sums (into the tile's)
+    // template's place), then the box sums (into the tile's)
     __syncthreads();                        // template and tile reads done
     if (ks > 0) {
       uint32_t *dst = part + ((ks - 1) * kWarpsPerCta + warp) * E * 32 + lane;
@@ -603,8 +628,7 @@ __global__ void __launch_bounds__(FixedShape<BOX>::kThreadsPerCta,
       box_columns<TY, RB>(tile, a.ht, kHalfUnitCols + a.wt - 1, vs, v_i, v_q, threadIdx.x,
                           kFixedThreads);
       __syncthreads();                      // column sums done, tile dead
-      if (ks == KS - 1)
-        box_rows<TY>(v_i, v_q, a.wt, vs, s_i, s_q, threadIdx.x - ks * kThreads, kThreads);
+      box_rows<TY>(v_i, v_q, a.wt, vs, s_i, s_q, threadIdx.x, kFixedThreads);
     }
     __syncthreads();
     if (ks > 0) return;

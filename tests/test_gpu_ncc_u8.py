@@ -109,6 +109,28 @@ def test_methods_agree_bit_for_bit():
     assert_parity(image, tmpl, sb, cb)
 
 
+@pytest.mark.parametrize("h,w,wt,ht", [(2048, 2048, 32, 32), (2000, 2064, 13, 7),
+                                        (1100, 1936, 64, 20)])
+def test_large_image_both_forms(h, w, wt, ht):
+    """Images large enough that the box form uses 2 output rows per
+    half-warp for narrow templates too: both forms bit-identical, and a band
+    of rows at each edge and sampled interior offsets against the oracle."""
+    image, tmpl = rand_u8(h, w), rand_u8(ht, wt)
+    sb, cb = run_gpu(image, tmpl, method="box")
+    sd, cd = run_gpu(image, tmpl, method="dp4a")
+    np.testing.assert_array_equal(sb, sd)
+    np.testing.assert_array_equal(cb.view(np.uint32), cd.view(np.uint32))
+    oh, ow = cb.shape
+    for y0, y1 in ((0, 9), (oh - 9, oh)):
+        rb, rcb, _ = oracle.ncc_u8(image[y0:y1 + ht - 1], tmpl, nthreads=NT)
+        np.testing.assert_array_equal(sb[:, y0:y1, :], rb)
+        assert np.abs(cb[y0:y1, :] - rcb).max() <= COEF_TOL
+    ys, xs = RNG.integers(0, oh, 300), RNG.integers(0, ow, 300)
+    rs, rc = oracle.ncc_u8_at(image, tmpl, xs, ys)
+    np.testing.assert_array_equal(sb[:, ys, xs], rs)
+    assert np.abs(cb[ys, xs] - rc).max() <= COEF_TOL
+
+
 def test_method_setting_is_per_thread_and_restored():
     assert corr.ncc_get_method() == "box"
     corr.ncc_set_method("dp4a")
