@@ -4,8 +4,12 @@
  *
  * Plain C types only.  Every buffer pointer is a DEVICE pointer (memory the
  * caller allocated on the current CUDA device, e.g. a torch tensor's
- * data_ptr()); the library never frees, keeps or reallocates a caller
- * buffer.  Calls are asynchronous on the calling thread's stream (see
+ * data_ptr(), or managed memory); page-locked host memory mapped into the
+ * device's address space is also accepted (through its device alias; the
+ * kernels then read and write across the host link, which is far slower
+ * than copying).  Pageable host memory and other devices' memory are
+ * refused with CORR_EINVAL.  The library never frees, keeps or reallocates
+ * a caller buffer.  Calls are asynchronous on the calling thread's stream (see
  * corr_set_stream) and run on the calling thread's current CUDA device.
  * Every argument is checked before anything is launched: a call that returns
  * an error has written nothing.

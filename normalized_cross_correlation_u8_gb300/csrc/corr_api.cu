@@ -18,6 +18,53 @@ int cuda_status(cudaError_t e) {
   return CORR_ECUDA;
 }
 
+// The address at which the current device's kernels reach a caller buffer:
+// device or managed memory of this device as is; page-locked host memory
+// mapped into the device's address space by its device alias.  Anything
+// else (pageable host memory, another device's memory, an unknown address)
+// is refused with CORR_EINVAL before any launch.
+template <typename T>
+int device_view(T *p, T **out) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();   // clear the sticky-free error of an unknown pointer
+    return CORR_EINVAL;
+  }
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return CORR_EINVAL;
+  }
+  switch (at.type) {
+    case cudaMemoryTypeDevice:
+      if (at.device != dev) return CORR_EINVAL;
+      *out = p;
+      return CORR_OK;
+    case cudaMemoryTypeManaged:
+      *out = p;
+      return CORR_OK;
+    case cudaMemoryTypeHost:
+      if (!at.devicePointer) return CORR_EINVAL;
+      *out = static_cast<T *>(at.devicePointer);
+      return CORR_OK;
+    default:
+      return CORR_EINVAL;
+  }
+}
+
+// device_view of the three f32 buffers, each still 4-byte aligned.
+int device_views(const float **left, const float **right, float **out) {
+  int rc;
+  if ((rc = device_view(*left, left)) != CORR_OK ||
+      (rc = device_view(*right, right)) != CORR_OK ||
+      (rc = device_view(*out, out)) != CORR_OK)
+    return rc;
+  if ((reinterpret_cast<uintptr_t>(*left) | reinterpret_cast<uintptr_t>(*right) |
+       reinterpret_cast<uintptr_t>(*out)) & 3)
+    return CORR_EINVAL;
+  return CORR_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -28,6 +75,12 @@ int corr_ncc_u8(const uint8_t *image, int w, int h, const uint8_t *tmpl,
   if (w <= 0 || h <= 0 || wt <= 0 || ht <= 0) return CORR_EINVAL;
   if (wt > w || ht > h) return CORR_EINVAL;
   if (int64_t(wt) * ht > CORR_NCC_MAX_TEMPLATE_PIXELS) return CORR_EUNSUPPORTED;
+  int rc;
+  if ((rc = device_view(image, &image)) != CORR_OK ||
+      (rc = device_view(tmpl, &tmpl)) != CORR_OK ||
+      (sums_out && (rc = device_view(sums_out, &sums_out)) != CORR_OK) ||
+      (coef_out && (rc = device_view(coef_out, &coef_out)) != CORR_OK))
+    return rc;
   // output planes are addressed with size_t, coordinates with int
   const int method = tls_ncc_method == CORR_NCC_METHOD_BOX ? corr::kMethodBox
                                                             : corr::kMethodDp4a;
@@ -54,6 +107,8 @@ int corr_xcorr_f32(const float *left, int nl, const float *right, int nr,
   if (int64_t(nl) * nr > 0x7fffffffLL) return CORR_EUNSUPPORTED;
   if (int64_t(2) * H - 1 > 0x7fffffffLL || int64_t(2) * W - 1 > 0x7fffffffLL)
     return CORR_EUNSUPPORTED;
+  int rc;
+  if ((rc = device_views(&left, &right, &out)) != CORR_OK) return rc;
   return cuda_status(
       corr::xcorr_f32_launch(left, nl, right, nr, H, W, out, tls_stream));
 }
@@ -71,6 +126,8 @@ int corr_xcorr_f32_noalloc(const float *left, int nl, const float *right, int nr
   if (corr::xcorr_f32_scratch_bytes(left, nl, right, nr, H, W) >
       CORR_XCORR_NOALLOC_SCRATCH_BYTES)
     return CORR_EUNSUPPORTED;
+  int rc;
+  if ((rc = device_views(&left, &right, &out)) != CORR_OK) return rc;
   return cuda_status(
       corr::xcorr_f32_noalloc_launch(left, nl, right, nr, H, W, out, tls_stream));
 }

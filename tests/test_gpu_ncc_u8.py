@@ -237,6 +237,30 @@ def test_argument_errors_raise():
     assert e.value.code == -2
 
 
+def test_buffer_kinds_through_the_abi():
+    """Pageable host memory is refused before any launch; page-locked host
+    outputs are written through their device alias and match."""
+    import ctypes
+    image, tmpl = rand_u8(40, 160), rand_u8(6, 10)
+    dev = torch.device("cuda", 0)
+    img, tm = torch.from_numpy(image).to(dev), torch.from_numpy(tmpl).to(dev)
+    oh, ow = 40 - 6 + 1, 160 - 10 + 1
+    lib = corr.load()
+    lib.corr_set_stream(ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    vp = ctypes.c_void_p
+    pageable = np.zeros((oh, ow), np.float32)
+    rc = lib.corr_ncc_u8(vp(img.data_ptr()), 160, 40, vp(tm.data_ptr()), 10, 6, None,
+                         vp(pageable.ctypes.data))
+    assert rc == -1
+    hs = torch.zeros((3, oh, ow), dtype=torch.int32).pin_memory()
+    hc = torch.zeros((oh, ow), dtype=torch.float32).pin_memory()
+    rc = lib.corr_ncc_u8(vp(img.data_ptr()), 160, 40, vp(tm.data_ptr()), 10, 6,
+                         vp(hs.data_ptr()), vp(hc.data_ptr()))
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert_parity(image, tmpl, hs.numpy().view(np.uint32), hc.numpy())
+
+
 def test_host_tensors_round_trip():
     image, tmpl = rand_u8(50, 200), rand_u8(8, 12)
     s, c = corr.ncc_u8(torch.from_numpy(image).pin_memory(), torch.from_numpy(tmpl))
