@@ -30,6 +30,7 @@ cudaError_t ncc_u8_launch(const uint8_t *image, int w, int h,
   a.oh = h - ht + 1;
   a.plane = size_t(a.ow) * a.oh;
   a.rows = R;
+  a.staged = 0;
   const size_t smem = size_t(ht) * a.wtp * 4;   // general path: the template
 
   const bool aligned8 = (reinterpret_cast<uintptr_t>(image) & 7) == 0 && (w & 7) == 0;
@@ -45,6 +46,7 @@ cudaError_t ncc_u8_launch(const uint8_t *image, int w, int h,
         tiles_for(kBoxRows) < (long long)CORR_NCC_BOX_NARROW_TILES_PER_SM * device_sm_count())
       rows = 1;
     a.rows = rows;
+    a.staged = !box || (long long)a.wtw * ht <= CORR_NCC_STAGED_BOX_WORDS;
     const int ty = 2 * rows * kWarpsPerCta;
     const size_t ts = fixed_tile_layout(ht, a.wtw, a.wtp, rows, box ? kBoxSplit : kSplit,
                                         box ? 1 : 3, box, wt).total;

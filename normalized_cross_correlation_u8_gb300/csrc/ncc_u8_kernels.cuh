@@ -85,6 +85,17 @@ constexpr int kHalfUnitCols = 16 * kCols;  // output columns per warp unit (fast
 #define CORR_NCC_BOX_MINB_WIDE 1
 #endif
 // Template-row ranges (warp groups) per tile of the SumIT-only kernel.
+// Fast kernel: write outputs through a warp-private staging area
+// (coalesced stores) rather than each lane's own 8 columns -- always for the
+// three-dp4a method, and for the box form while the template has at most
+// CORR_NCC_STAGED_BOX_WORDS words (wtw * ht): beyond that the staging's
+// instructions cost more than the scattered stores.
+#ifndef CORR_NCC_STAGED_STORES
+#define CORR_NCC_STAGED_STORES 1
+#endif
+#ifndef CORR_NCC_STAGED_BOX_WORDS
+#define CORR_NCC_STAGED_BOX_WORDS 200
+#endif
 #ifndef CORR_NCC_BOX_KSPLIT
 #define CORR_NCC_BOX_KSPLIT 2
 #endif
@@ -164,6 +175,7 @@ struct NccArgs {
   int wtp;           // shared-memory template row stride in words (multiple of 4)
   int ow, oh;
   int rows;          // fast path: output rows per half-warp (the kernel's R)
+  int staged;        // fast path: coalesced stores through shared memory
   int tiles_x;       // units across a row of outputs
   int units;         // warp units (fast path: 128 cols x 2R rows)
 };
@@ -293,6 +305,62 @@ __device__ __forceinline__ void epilogue(const NccArgs &a, int x0, int y0,
         a.coef[o] = d_i > 0 ? i64_to_f32(num) * rsqrtf(i64_to_f32(d_i)) * rs_t : 0.f;
       }
     }
+  }
+}
+
+// The same outputs for a whole warp of the tiled kernel, written through a
+// warp-private staging area so that the global stores are coalesced.  A
+// lane owns 8 adjacent columns, so storing its own values makes every store
+// instruction touch 16 sectors for 64 bytes; staging one plane at a time
+// ([2 halves][R][128] words, half h's row r at (h*R + r)*128) lets each
+// store instruction write 32 consecutive outputs of one row instead.  The
+// warp's rows are yw .. yw+2R-1 and its columns xt .. xt+127.
+template <int R>
+__device__ __forceinline__ void epilogue_staged(const NccArgs &a, int xt, int yw, int lane,
+                                                const uint32_t (&sI)[R][kCols],
+                                                const uint32_t (&sQ)[R][kCols],
+                                                const uint32_t (&sT)[R][kCols],
+                                                uint32_t sum_t, float rs_t,
+                                                uint32_t *stage) {
+  const int64_t n = int64_t(a.wt) * a.ht;
+  const int half = lane >> 4, hl = lane & 15;
+  // value(r, c) of one plane -> staging area -> coalesced rows of dst
+  auto put = [&](auto value, uint32_t *dst) {
+    __syncwarp();                           // the area's previous reads are done
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      uint4 *row = reinterpret_cast<uint4 *>(stage + (half * R + r) * kHalfUnitCols +
+                                             hl * kCols);
+      row[0] = make_uint4(value(r, 0), value(r, 1), value(r, 2), value(r, 3));
+      row[1] = make_uint4(value(r, 4), value(r, 5), value(r, 6), value(r, 7));
+    }
+    __syncwarp();
+#pragma unroll
+    for (int rr = 0; rr < 2 * R; ++rr) {
+      const int y = yw + rr;
+      if (y >= a.oh) break;
+      uint32_t *out = dst + size_t(y) * a.ow + xt;
+#pragma unroll
+      for (int k = 0; k < kHalfUnitCols / 32; ++k) {
+        const int col = 32 * k + lane;
+        if (xt + col < a.ow) out[col] = stage[rr * kHalfUnitCols + col];
+      }
+    }
+  };
+  if (a.sums) {
+    put([&](int r, int c) { return sI[r][c]; }, a.sums);
+    put([&](int r, int c) { return sQ[r][c]; }, a.sums + a.plane);
+    put([&](int r, int c) { return sT[r][c]; }, a.sums + 2 * a.plane);
+  }
+  if (a.coef) {
+    put([&](int r, int c) {
+          const int64_t si = sI[r][c];
+          const int64_t num = n * int64_t(sT[r][c]) - si * int64_t(sum_t);
+          const int64_t d_i = n * int64_t(sQ[r][c]) - si * si;
+          return __float_as_uint(
+              d_i > 0 ? i64_to_f32(num) * rsqrtf(i64_to_f32(d_i)) * rs_t : 0.f);
+        },
+        reinterpret_cast<uint32_t *>(a.coef));
   }
 }
 
@@ -660,6 +728,15 @@ __global__ void __launch_bounds__(FixedShape<BOX>::kThreadsPerCta,
           sI[r][c] = vi.x; sI[r][c + 1] = vi.y; sI[r][c + 2] = vi.z; sI[r][c + 3] = vi.w;
           sQ[r][c] = vq.x; sQ[r][c + 1] = vq.y; sQ[r][c + 2] = vq.z; sQ[r][c + 3] = vq.w;
         }
+    }
+  }
+  if constexpr (KS > 1 && CORR_NCC_STAGED_STORES) {
+    if (a.staged) {                         // warp-uniform
+      // this warp's partial-sum area (read above) holds 2R x 128 words
+      static_assert(NS * R * kCols * 32 >= 2 * R * kHalfUnitCols, "staging area too small");
+      epilogue_staged<R>(a, xt, yt + warp * 2 * R, lane, sI, sQ, sT, sum_t,
+                         template_rsqrt(a, sum_t, sum_t_sq), part + warp * E * 32);
+      return;
     }
   }
   epilogue<R>(a, x0, y0, sI, sQ, sT, sum_t, template_rsqrt(a, sum_t, sum_t_sq));
