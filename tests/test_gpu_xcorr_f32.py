@@ -66,6 +66,9 @@ def test_fixture(path):
     (1, 5, 31, 29), (1, 37, 64, 64), (3, 4, 7, 11), (5, 9, 16, 16),
     # small matrices in batches: block shapes 16 x 32, 8 x 64 and 64 x 8
     (16, 40, 10, 10), (8, 64, 12, 12), (70, 5, 6, 7),
+    # small batches, pairs of shifts per lane: W = 1, 2, 3 and odd / even W
+    (20, 10, 4, 1), (10, 10, 3, 2), (12, 8, 5, 3), (64, 1, 1, 16), (9, 9, 16, 16),
+    (40, 33, 13, 15),
     (2, 3, 50, 8), (33, 3, 5, 5), (1, 1, 1, 300), (1, 1, 300, 1),
     # rights in lanes: ragged right block, W % 4 != 0, short H, several lefts
     (2, 40, 20, 12), (1, 33, 30, 10), (3, 64, 9, 40), (1, 96, 33, 8),
