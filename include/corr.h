@@ -21,6 +21,7 @@
 #ifndef CORR_H_
 #define CORR_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -71,6 +72,18 @@ extern "C" {
  */
 int corr_ncc_u8(const uint8_t *image, int w, int h, const uint8_t *tmpl,
                 int wt, int ht, uint32_t *sums_out, float *coef_out);
+
+/*
+ * corr_ncc_u8_pitched -- corr_ncc_u8 on an image whose rows are `pitch`
+ * bytes apart (pitch >= w, else CORR_EINVAL): a pitched allocation or a
+ * crop of a larger image.  Only the w bytes of each row are read; the
+ * outputs stay dense.  corr_ncc_u8 is this call with pitch = w.  Vector
+ * staging of the tile needs the image pointer, w and pitch all 16- (or 8-)
+ * byte multiples; other images are staged with byte loads, same results.
+ */
+int corr_ncc_u8_pitched(const uint8_t *image, int w, int h, size_t pitch,
+                        const uint8_t *tmpl, int wt, int ht, uint32_t *sums_out,
+                        float *coef_out);
 
 /*
  * corr_ncc_set_method / corr_ncc_get_method -- how corr_ncc_u8 forms SumI

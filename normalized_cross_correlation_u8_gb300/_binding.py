@@ -27,7 +27,7 @@ NCC_METHOD_DP4A = 0
 NCC_METHOD_BOX = 1
 _NCC_METHODS = {"dp4a": NCC_METHOD_DP4A, "box": NCC_METHOD_BOX}
 
-EXPORTS = ["corr_ncc_u8", "corr_ncc_set_method", "corr_ncc_get_method", "corr_xcorr_f32", "corr_xcorr_f32_noalloc", "corr_set_stream",
+EXPORTS = ["corr_ncc_u8", "corr_ncc_u8_pitched", "corr_ncc_set_method", "corr_ncc_get_method", "corr_xcorr_f32", "corr_xcorr_f32_noalloc", "corr_set_stream",
            "corr_get_stream", "corr_strerror", "corr_last_cuda_error",
            "corr_version", "corr_peak_dp4a", "corr_peak_ffma"]
 
@@ -67,6 +67,8 @@ def load(build_if_missing=True):
         lib = ctypes.CDLL(path)
         c_int, vp, c_dbl_p = ctypes.c_int, ctypes.c_void_p, ctypes.POINTER(ctypes.c_double)
         lib.corr_ncc_u8.argtypes = [vp, c_int, c_int, vp, c_int, c_int, vp, vp]
+        lib.corr_ncc_u8_pitched.argtypes = [vp, c_int, c_int, ctypes.c_size_t, vp, c_int,
+                                            c_int, vp, vp]
         lib.corr_ncc_set_method.argtypes = [c_int]
         lib.corr_ncc_get_method.argtypes = []
         lib.corr_xcorr_f32.argtypes = [vp, c_int, vp, c_int, c_int, c_int, vp]
@@ -80,7 +82,8 @@ def load(build_if_missing=True):
         lib.corr_version.argtypes = []
         lib.corr_peak_dp4a.argtypes = [c_int, c_dbl_p, c_dbl_p]
         lib.corr_peak_ffma.argtypes = [c_dbl_p, c_dbl_p]
-        for f in (lib.corr_ncc_u8, lib.corr_ncc_set_method, lib.corr_ncc_get_method,
+        for f in (lib.corr_ncc_u8, lib.corr_ncc_u8_pitched, lib.corr_ncc_set_method,
+                  lib.corr_ncc_get_method,
                   lib.corr_xcorr_f32, lib.corr_xcorr_f32_noalloc,
                   lib.corr_set_stream,
                   lib.corr_last_cuda_error, lib.corr_version,
@@ -134,9 +137,10 @@ def ncc_get_method():
 
 
 def ncc_u8_into(image, tmpl, sums_out, coef_out, method=None):
-    """Device call: image [h,w] uint8, tmpl [ht,wt] uint8, sums_out
+    """Device call: image [h,w] uint8 (rows may be strided, e.g. a crop of a
+    larger image: passed as the row pitch), tmpl [ht,wt] uint8, sums_out
     [3,oh,ow] 32-bit (or None), coef_out [oh,ow] float32 (or None), all on
-    the same CUDA device and contiguous.  Runs on the current stream.
+    the same CUDA device, outputs contiguous.  Runs on the current stream.
     `method` ("dp4a" / "box") overrides this thread's method for the call."""
     if image.dtype != torch.uint8 or tmpl.dtype != torch.uint8:
         raise TypeError("image and template must be uint8")
@@ -156,7 +160,10 @@ def ncc_u8_into(image, tmpl, sums_out, coef_out, method=None):
                 raise TypeError("outputs are 32-bit")
     if coef_out is not None and coef_out.dtype != torch.float32:
         raise TypeError("coef_out must be float32")
-    image, tmpl = image.contiguous(), tmpl.contiguous()
+    if image.stride(1) != 1 or image.stride(0) < w:
+        image = image.contiguous()
+    pitch = image.stride(0)
+    tmpl = tmpl.contiguous()
     if method is not None and method not in _NCC_METHODS:
         raise ValueError(f"method must be one of {sorted(_NCC_METHODS)}")
     with torch.cuda.device(dev):
@@ -165,8 +172,8 @@ def ncc_u8_into(image, tmpl, sums_out, coef_out, method=None):
         if method is not None:
             _check(lib.corr_ncc_set_method(_NCC_METHODS[method]))
         try:
-            _check(lib.corr_ncc_u8(
-                ctypes.c_void_p(image.data_ptr()), w, h,
+            _check(lib.corr_ncc_u8_pitched(
+                ctypes.c_void_p(image.data_ptr()), w, h, pitch,
                 ctypes.c_void_p(tmpl.data_ptr()), wt, ht,
                 ctypes.c_void_p(sums_out.data_ptr() if sums_out is not None else 0),
                 ctypes.c_void_p(coef_out.data_ptr() if coef_out is not None else 0)))

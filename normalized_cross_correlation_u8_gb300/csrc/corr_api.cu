@@ -71,8 +71,16 @@ extern "C" {
 
 int corr_ncc_u8(const uint8_t *image, int w, int h, const uint8_t *tmpl,
                 int wt, int ht, uint32_t *sums_out, float *coef_out) {
+  if (w <= 0) return CORR_EINVAL;
+  return corr_ncc_u8_pitched(image, w, h, size_t(w), tmpl, wt, ht, sums_out, coef_out);
+}
+
+int corr_ncc_u8_pitched(const uint8_t *image, int w, int h, size_t pitch,
+                        const uint8_t *tmpl, int wt, int ht, uint32_t *sums_out,
+                        float *coef_out) {
   if (!image || !tmpl || (!sums_out && !coef_out)) return CORR_EINVAL;
   if (w <= 0 || h <= 0 || wt <= 0 || ht <= 0) return CORR_EINVAL;
+  if (pitch < size_t(w)) return CORR_EINVAL;
   if (wt > w || ht > h) return CORR_EINVAL;
   if (int64_t(wt) * ht > CORR_NCC_MAX_TEMPLATE_PIXELS) return CORR_EUNSUPPORTED;
   int rc;
@@ -84,7 +92,7 @@ int corr_ncc_u8(const uint8_t *image, int w, int h, const uint8_t *tmpl,
   // output planes are addressed with size_t, coordinates with int
   const int method = tls_ncc_method == CORR_NCC_METHOD_BOX ? corr::kMethodBox
                                                             : corr::kMethodDp4a;
-  return cuda_status(corr::ncc_u8_launch(image, w, h, tmpl, wt, ht, sums_out,
+  return cuda_status(corr::ncc_u8_launch(image, w, h, pitch, tmpl, wt, ht, sums_out,
                                          coef_out, method, tls_stream));
 }
 

@@ -27,7 +27,7 @@ constexpr int kMethodBox = 1;    // SumI, SumISq by box passes; SumIT by dp4a
 
 // Launches the u8 normalized cross-correlation on `stream`.  Arguments are
 // already validated by the C ABI layer (corr_api.cu).
-cudaError_t ncc_u8_launch(const uint8_t *image, int w, int h,
+cudaError_t ncc_u8_launch(const uint8_t *image, int w, int h, size_t pitch,
                           const uint8_t *tmpl, int wt, int ht,
                           uint32_t *sums_out, float *coef_out, int method,
                           cudaStream_t stream);

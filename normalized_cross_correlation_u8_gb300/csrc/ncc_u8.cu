@@ -7,7 +7,7 @@ namespace corr {
 
 using namespace ncc;
 
-cudaError_t ncc_u8_launch(const uint8_t *image, int w, int h,
+cudaError_t ncc_u8_launch(const uint8_t *image, int w, int h, size_t pitch,
                           const uint8_t *tmpl, int wt, int ht,
                           uint32_t *sums_out, float *coef_out, int method,
                           cudaStream_t stream) {
@@ -18,6 +18,7 @@ cudaError_t ncc_u8_launch(const uint8_t *image, int w, int h,
   a.sums = sums_out;
   a.coef = coef_out;
   a.w = w;
+  a.pitch = pitch;
   a.h = h;
   a.wt = wt;
   a.ht = ht;
@@ -33,8 +34,11 @@ cudaError_t ncc_u8_launch(const uint8_t *image, int w, int h,
   a.staged = 0;
   const size_t smem = size_t(ht) * a.wtp * 4;   // general path: the template
 
-  const bool aligned8 = (reinterpret_cast<uintptr_t>(image) & 7) == 0 && (w & 7) == 0;
-  const bool aligned16 = (reinterpret_cast<uintptr_t>(image) & 15) == 0 && (w & 15) == 0;
+  // whole-vector staging needs every row start and width on the vector size
+  const bool aligned8 =
+      (reinterpret_cast<uintptr_t>(image) & 7) == 0 && (w & 7) == 0 && (pitch & 7) == 0;
+  const bool aligned16 =
+      (reinterpret_cast<uintptr_t>(image) & 15) == 0 && (w & 15) == 0 && (pitch & 15) == 0;
   if (a.wtw >= 1 && a.wtw <= kMaxFixedWords) {
     const bool box = method == kMethodBox;
     auto tiles_for = [&](int rows) {

@@ -168,6 +168,7 @@ struct NccArgs {
   float *coef;
   size_t plane;      // ow * oh
   int w, h, wt, ht;
+  size_t pitch;      // bytes from one image row to the next (>= w)
   int wtw;           // template words per row (ceil(wt / 4))
   int tail;          // wt % 4: bytes of the last word that are template pixels (0: all)
   uint32_t tail_ones;  // SumI multiplier of the last word (0x01 in its template bytes)
@@ -572,13 +573,13 @@ __global__ void __launch_bounds__(FixedShape<BOX>::kThreadsPerCta,
     memset(&v, 0, sizeof(v));
     const int r = i / C, c = i - r * C;
     const int x = xt + CB * c;
-    const uint8_t *row = a.image + size_t(yt + r) * a.w;
+    const uint8_t *row = a.image + size_t(yt + r) * a.pitch;
     if constexpr (VB == 1) {
 #pragma unroll
       for (int b = 0; b < 4; ++b)
         if (x + b < a.w) v |= uint32_t(__ldg(row + x + b)) << (8 * b);
     } else {
-      if (x < a.w) v = __ldg(reinterpret_cast<const Chunk *>(row + x));   // w % CB == 0
+      if (x < a.w) v = __ldg(reinterpret_cast<const Chunk *>(row + x));   // w, pitch % CB == 0
     }
     return v;
   };
@@ -769,7 +770,7 @@ __global__ void __launch_bounds__(kThreads)
 
   const int nrows = min(R + a.ht - 1, a.h - y0);
   for (int rel = 0; rel < nrows; ++rel) {
-    const uint8_t *row = a.image + size_t(y0 + rel) * a.w;
+    const uint8_t *row = a.image + size_t(y0 + rel) * a.pitch;
     unsigned mask = 0;
 #pragma unroll
     for (int r = 0; r < R; ++r)

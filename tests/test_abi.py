@@ -80,6 +80,17 @@ def test_ncc_argument_errors(args, code):
 
 
 @pytest.mark.parametrize("args,code", [
+    ((FAKE, 16, 16, 15, FAKE, 4, 4, FAKE, FAKE), -1),        # pitch < w
+    ((FAKE, 16, 16, 0, FAKE, 4, 4, FAKE, FAKE), -1),
+    ((None, 16, 16, 32, FAKE, 4, 4, FAKE, FAKE), -1),        # null image
+    ((FAKE, 16, 16, 32, FAKE, 20, 4, FAKE, FAKE), -1),       # template wider
+    ((FAKE, 300, 300, 512, FAKE, 257, 258, FAKE, FAKE), -2), # > 66052 pixels
+])
+def test_ncc_pitched_argument_errors(args, code):
+    assert corr.load().corr_ncc_u8_pitched(*args) == code
+
+
+@pytest.mark.parametrize("args,code", [
     ((None, 1, FAKE, 1, 4, 4, FAKE), -1),
     ((FAKE, 1, FAKE, 1, 4, 4, None), -1),
     ((FAKE, 0, FAKE, 1, 4, 4, FAKE), -1),

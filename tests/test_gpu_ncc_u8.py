@@ -237,6 +237,28 @@ def test_argument_errors_raise():
     assert e.value.code == -2
 
 
+@pytest.mark.parametrize("method", ["box", "dp4a"])
+@pytest.mark.parametrize("off,pitch,h,w,wt,ht", [
+    (0, 512, 70, 300, 32, 32),      # 16-byte aligned rows: vector staging
+    (8, 520, 45, 264, 20, 9),       # 8-byte aligned rows
+    (3, 401, 60, 333, 17, 11),      # odd pitch: byte staging
+    (5, 300, 40, 290, 160, 5),      # general kernel (wt > 128)
+])
+def test_pitched_image(method, off, pitch, h, w, wt, ht):
+    """An image whose rows are `pitch` bytes apart (a crop of a larger
+    buffer, passed through corr_ncc_u8_pitched): the same results as the
+    dense copy."""
+    dev = torch.device("cuda", 0)
+    big = rand_u8(h + 2, pitch + 16)
+    flat = torch.from_numpy(big.ravel().copy()).to(dev)
+    view = flat[off:off + (h - 1) * pitch + w].as_strided((h, w), (pitch, 1))
+    image = np.lib.stride_tricks.as_strided(big.ravel()[off:], (h, w), (pitch, 1)).copy()
+    tmpl = rand_u8(ht, wt)
+    s, c = corr.ncc_u8(view, torch.from_numpy(tmpl).to(dev), method=method)
+    torch.cuda.synchronize()
+    assert_parity(image, tmpl, s.cpu().numpy().view(np.uint32), c.cpu().numpy())
+
+
 def test_buffer_kinds_through_the_abi():
     """Pageable host memory is refused before any launch; page-locked host
     outputs are written through their device alias and match."""
