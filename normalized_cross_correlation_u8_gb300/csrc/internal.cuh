@@ -23,7 +23,7 @@ cudaError_t scratch_alloc(void **ptr, size_t bytes, cudaStream_t stream);
 
 // Methods of the u8 fast path (corr.h: CORR_NCC_METHOD_*).
 constexpr int kMethodDp4a = 0;   // SumI, SumISq, SumIT all by dp4a in the tiled kernel
-constexpr int kMethodBox = 1;    // SumI, SumISq by box passes; SumIT by dp4a
+constexpr int kMethodBox = 1;    // SumI, SumISq as box sums of the tile; SumIT by dp4a
 
 // Launches the u8 normalized cross-correlation on `stream`.  Arguments are
 // already validated by the C ABI layer (corr_api.cu).

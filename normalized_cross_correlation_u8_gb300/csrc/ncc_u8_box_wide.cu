@@ -1,6 +1,6 @@
-// ncc_u8_box_wide.cu -- the SumIT-only fast kernel (box-sum variant,
-// ncc_u8_box.cu) for templates of 17 .. 32 words, in a translation unit of
-// its own so that it compiles beside the others (kernels: ncc_u8_kernels.cuh).
+// ncc_u8_box_wide.cu -- the box form of the fast kernel (ncc_u8_box.cu) for
+// templates of 17 .. 32 words, in a translation unit of its own so that it
+// compiles beside the others (kernels: ncc_u8_kernels.cuh).
 #include "ncc_u8_kernels.cuh"
 
 namespace corr {
