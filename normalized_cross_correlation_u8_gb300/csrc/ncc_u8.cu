@@ -41,9 +41,10 @@ cudaError_t ncc_u8_launch(const uint8_t *image, int w, int h, size_t pitch,
       (reinterpret_cast<uintptr_t>(image) & 15) == 0 && (w & 15) == 0 && (pitch & 15) == 0;
   if (a.wtw >= 1 && a.wtw <= kMaxFixedWords) {
     const bool box = method == kMethodBox;
+    const int warps = box ? kBoxWarps : kWarpsPerCta;   // row groups per tile
     auto tiles_for = [&](int rows) {
       return (long long)((a.ow + kHalfUnitCols - 1) / kHalfUnitCols) *
-             ((a.oh + 2 * rows * kWarpsPerCta - 1) / (2 * rows * kWarpsPerCta));
+             ((a.oh + 2 * rows * warps - 1) / (2 * rows * warps));
     };
     int rows = box ? kBoxRows : R;
     if (box && kBoxRows != 1 && a.wtw <= kBoxNarrowWords &&
@@ -51,9 +52,9 @@ cudaError_t ncc_u8_launch(const uint8_t *image, int w, int h, size_t pitch,
       rows = 1;
     a.rows = rows;
     a.staged = !box || (long long)a.wtw * ht <= CORR_NCC_STAGED_BOX_WORDS;
-    const int ty = 2 * rows * kWarpsPerCta;
-    const size_t ts = fixed_tile_layout(ht, a.wtw, a.wtp, rows, box ? kBoxSplit : kSplit,
-                                        box ? 1 : 3, box, wt).total;
+    const int ty = 2 * rows * warps;
+    const size_t ts = fixed_tile_layout(ht, a.wtw, a.wtp, rows, warps,
+                                        box ? kBoxSplit : kSplit, box ? 1 : 3, box, wt).total;
     if (ts > 200 * 1024) goto general;   // very tall template: general path
     a.tiles_x = (a.ow + kHalfUnitCols - 1) / kHalfUnitCols;
     const long long tiles = (long long)a.tiles_x * ((a.oh + ty - 1) / ty);

@@ -105,6 +105,10 @@ constexpr int kHalfUnitCols = 16 * kCols;  // output columns per warp unit (fast
 #ifndef CORR_NCC_STAGED_BOX_WORDS
 #define CORR_NCC_STAGED_BOX_WORDS 200
 #endif
+// Warps per template-row group (row groups of the tile) of the box form.
+#ifndef CORR_NCC_BOX_WARPS
+#define CORR_NCC_BOX_WARPS 2
+#endif
 #ifndef CORR_NCC_BOX_KSPLIT
 #define CORR_NCC_BOX_KSPLIT 2
 #endif
@@ -117,11 +121,13 @@ constexpr int kSplit = CORR_NCC_KSPLIT;
 constexpr int kBoxRows = CORR_NCC_BOX_ROWS;
 constexpr int kBoxNarrowWords = CORR_NCC_BOX_NARROW_WORDS;
 constexpr int kBoxSplit = CORR_NCC_BOX_KSPLIT;
+constexpr int kBoxWarps = CORR_NCC_BOX_WARPS;
 // Warp groups and threads of the fast kernel (BOX: the SumIT-only form).
 template <bool BOX>
 struct FixedShape {
+  static constexpr int kWarps = BOX ? kBoxWarps : kWarpsPerCta;   // per group
   static constexpr int kGroups = BOX ? kBoxSplit : kSplit;
-  static constexpr int kThreadsPerCta = kThreads * kGroups;
+  static constexpr int kThreadsPerCta = 32 * kWarps * kGroups;
 };
 
 
@@ -144,12 +150,12 @@ __host__ __device__ inline int box_v_stride(int wt) {
 struct TileLayout {
   size_t tile, part, tmpl, total;   // byte offsets of the regions, total size
 };
-inline TileLayout fixed_tile_layout(int ht, int wtw, int wtp, int rows, int groups, int ns,
-                                    bool box, int wt) {
-  const int ty = 2 * rows * kWarpsPerCta;
+inline TileLayout fixed_tile_layout(int ht, int wtw, int wtp, int rows, int warps,
+                                    int groups, int ns, bool box, int wt) {
+  const int ty = 2 * rows * warps;
   const size_t rb = (kHalfUnitCols + 4 * wtw + 8 + 15) & ~15;
   const size_t tile = size_t(ty + ht - 1) * rb;
-  const size_t part = size_t(groups - 1) * kWarpsPerCta * 32 * ns * rows * kCols * 4;
+  const size_t part = size_t(groups - 1) * warps * 32 * ns * rows * kCols * 4;
   const size_t tmpl = size_t(ht) * wtp * 4;
   TileLayout l;
   if (!box) {
@@ -514,7 +520,7 @@ __device__ __forceinline__ void box_rows(const uint32_t *v_i, const uint32_t *v_
 // Fast path: template width WT words known at compile time, any image
 // alignment (the staging unit VB follows it).
 //
-// A CTA owns a tile of 128 output columns x TY = 2*R*kWarpsPerCta output
+// A CTA owns a tile of 128 output columns x TY = 2*R*kWarps output
 // rows.  It first copies the image tile plus halo -- TY+ht-1 rows of
 // 128+4*WT+8 bytes (rounded to 16) -- into shared memory with 16-byte (or
 // 8-byte) vector loads that are all independent, so the tile costs one
@@ -545,16 +551,17 @@ __global__ void __launch_bounds__(FixedShape<BOX>::kThreadsPerCta,
                                   : WT <= 16 ? CORR_NCC_BOX_MINB : CORR_NCC_BOX_MINB_WIDE)
     ncc_u8_fixed_kernel(const NccArgs a) {
   constexpr int KS = FixedShape<BOX>::kGroups;
+  constexpr int WPC = FixedShape<BOX>::kWarps;
   constexpr int kFixedThreads = FixedShape<BOX>::kThreadsPerCta;
   constexpr int WTP = (WT + 3) & ~3;
   constexpr int RB = TileGeom<WT>::kRowBytes;
-  constexpr int TY = 2 * R * kWarpsPerCta;
+  constexpr int TY = 2 * R * WPC;
   extern __shared__ uint4 smem_u4[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(smem_u4);
   constexpr int NS = BOX ? 1 : 3;                     // sums exchanged per column
   constexpr int E = NS * R * kCols;
   const size_t tile_bytes = size_t(TY + a.ht - 1) * RB;
-  const size_t part_bytes = size_t(KS - 1) * kWarpsPerCta * E * 32 * 4;
+  const size_t part_bytes = size_t(KS - 1) * WPC * E * 32 * 4;
   const size_t s_bytes = size_t(2) * TY * kHalfUnitCols * 4;
   // regions as fixed_tile_layout places them
   uint8_t *tile = BOX ? smem : smem + size_t(a.ht) * WTP * 4;
@@ -620,8 +627,8 @@ __global__ void __launch_bounds__(FixedShape<BOX>::kThreadsPerCta,
   uint32_t *s_i = reinterpret_cast<uint32_t *>(tile), *s_q = s_i + TY * kHalfUnitCols;
 
   const int warp_id = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int warp = warp_id % kWarpsPerCta;            // row group of the tile
-  const int ks = warp_id / kWarpsPerCta;              // template-row range
+  const int warp = warp_id % WPC;            // row group of the tile
+  const int ks = warp_id / WPC;              // template-row range
   const int j_lo = ks * a.ht / KS, j_hi = (ks + 1) * a.ht / KS;
   const int half = lane >> 4, hl = lane & 15;
   const int yr0 = warp * 2 * R + half * R;           // tile-relative first row
@@ -687,7 +694,7 @@ __global__ void __launch_bounds__(FixedShape<BOX>::kThreadsPerCta,
     // template's place), then the box sums (into the tile's)
     __syncthreads();                        // template and tile reads done
     if (ks > 0) {
-      uint32_t *dst = part + ((ks - 1) * kWarpsPerCta + warp) * E * 32 + lane;
+      uint32_t *dst = part + ((ks - 1) * WPC + warp) * E * 32 + lane;
 #pragma unroll
       for (int r = 0; r < R; ++r)
 #pragma unroll
@@ -712,7 +719,7 @@ __global__ void __launch_bounds__(FixedShape<BOX>::kThreadsPerCta,
     if (ks > 0) return;
 #pragma unroll 1
     for (int g = 1; g < KS; ++g) {
-      const uint32_t *src = part + ((g - 1) * kWarpsPerCta + warp) * E * 32 + lane;
+      const uint32_t *src = part + ((g - 1) * WPC + warp) * E * 32 + lane;
 #pragma unroll
       for (int r = 0; r < R; ++r)
 #pragma unroll
