@@ -33,9 +33,16 @@ extern "C" {
 #define CORR_EUNSUPPORTED (-2)  /* a size the kernels do not handle (see each call) */
 #define CORR_ECUDA (-3)         /* CUDA runtime error (no device, launch failure, ...) */
 
-/* Largest template (pixels) whose SumISq = sum of 255^2 still fits the
- * unsigned 32-bit accumulators: 66052 * 65025 < 2^32. */
-#define CORR_NCC_MAX_TEMPLATE_PIXELS 66052
+/* Largest template (pixels) whose SumISq and SumIT (at most N * 255^2)
+ * still fit the unsigned 32-bit accumulators: 66051 * 65025 < 2^32 <=
+ * 66052 * 65025. */
+#define CORR_NCC_MAX_TEMPLATE_PIXELS 66051
+
+/* Templates wider than 128 pixels, or too tall for the tiled kernel's
+ * shared memory, take a general kernel that holds the template as packed
+ * 32-bit words, ceil(wt/4) per row: ht * ceil(wt/4) may not exceed this
+ * (only 1-pixel-wide templates taller than it are affected). */
+#define CORR_NCC_MAX_GENERAL_TEMPLATE_WORDS 58000
 
 /*
  * corr_ncc_u8 -- 8-bit normalized cross-correlation (template matching).
@@ -61,7 +68,9 @@ extern "C" {
  *   w, h      image width and height in pixels, > 0.
  *   tmpl      device, wt*ht bytes, row-major, pitch wt.
  *   wt, ht    template size, 0 < wt <= w, 0 < ht <= h, and
- *             wt*ht <= CORR_NCC_MAX_TEMPLATE_PIXELS, else CORR_EUNSUPPORTED.
+ *             wt*ht <= CORR_NCC_MAX_TEMPLATE_PIXELS and
+ *             ht*ceil(wt/4) <= CORR_NCC_MAX_GENERAL_TEMPLATE_WORDS, else
+ *             CORR_EUNSUPPORTED.
  *             Any width: the template packs into 32-bit words with the last
  *             word of a row zero-padded, and that word's SumI / SumISq take
  *             only its template bytes.
@@ -130,9 +139,14 @@ int corr_ncc_get_method(void);
  *   H, W      matrix height and width, > 0.
  *   out       device, [nl][nr][2H-1][2W-1] float32, dense; pair li*nr+ri.
  *
- * May allocate and free temporary device memory on the current stream
- * (stream-ordered) for shapes it splits across blocks; returns CORR_ECUDA if
- * that allocation fails.
+ * Shapes it splits across blocks (row bands of more than 128 overlap rows
+ * in a small batch, or x segments of rows wider than about 770 floats) take
+ * temporary device memory for the partial sums, stream-ordered on the
+ * current stream from a pool the library keeps per device; CORR_ECUDA if
+ * that allocation fails.  The library holds none of it between calls: a
+ * block freed by one call is reused by calls queued before the next
+ * synchronisation of the stream or device, which hands it back to the
+ * driver (see corr_scratch_reserved).
  */
 int corr_xcorr_f32(const float *left, int nl, const float *right, int nr,
                    int H, int W, float *out);
@@ -159,9 +173,15 @@ int corr_xcorr_f32(const float *left, int nl, const float *right, int nr,
  *     or the rows into x segments (rows wider than about 770 floats: about
  *     48 bytes per matrix element, so one 1024x1024 pair needs 48 MiB and
  *     is rejected).
- *   * The first call on a device that needs scratch looks the array's device
- *     address up on that device; make that first call before any stream
- *     capture begins on it.
+ *   * The array's device memory is committed when the driver loads the
+ *     library's module that holds it.  Under CUDA's lazy module loading (the
+ *     default) that happens during the first call on a device that needs
+ *     scratch, which also looks the array's device address up on that
+ *     device: that call can fail with CORR_ECUDA if the caller has already
+ *     reserved all device memory.  So make one warm-up call on each device
+ *     with a shape that uses scratch (one 256x256 pair does) before
+ *     reserving memory or beginning a stream capture, or load modules
+ *     eagerly (environment CUDA_MODULE_LOADING=EAGER).
  *   * Every call, on every stream and thread, shares the one array: calls
  *     that overlap on the GPU race and corrupt each other's results, so
  *     order them (one stream, or events between streams).
@@ -169,6 +189,11 @@ int corr_xcorr_f32(const float *left, int nl, const float *right, int nr,
 #define CORR_XCORR_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 int corr_xcorr_f32_noalloc(const float *left, int nl, const float *right, int nr,
                            int H, int W, float *out);
+
+/* Bytes of device memory the library's scratch pool holds on the current
+ * device right now: nonzero only while calls that use scratch are queued or
+ * running (none after the stream or device has been synchronised). */
+int corr_scratch_reserved(size_t *bytes);
 
 /* Stream for this thread's following calls (a cudaStream_t; NULL = the
  * legacy default stream).  Thread-local; never fails. */

@@ -22,12 +22,12 @@ CORR_OK = 0
 CORR_EINVAL = -1
 CORR_EUNSUPPORTED = -2
 CORR_ECUDA = -3
-NCC_MAX_TEMPLATE_PIXELS = 66052
+NCC_MAX_TEMPLATE_PIXELS = 66051
 NCC_METHOD_DP4A = 0
 NCC_METHOD_BOX = 1
 _NCC_METHODS = {"dp4a": NCC_METHOD_DP4A, "box": NCC_METHOD_BOX}
 
-EXPORTS = ["corr_ncc_u8", "corr_ncc_u8_pitched", "corr_ncc_set_method", "corr_ncc_get_method", "corr_xcorr_f32", "corr_xcorr_f32_noalloc", "corr_set_stream",
+EXPORTS = ["corr_ncc_u8", "corr_ncc_u8_pitched", "corr_ncc_set_method", "corr_ncc_get_method", "corr_xcorr_f32", "corr_xcorr_f32_noalloc", "corr_scratch_reserved", "corr_set_stream",
            "corr_get_stream", "corr_strerror", "corr_last_cuda_error",
            "corr_version", "corr_peak_dp4a", "corr_peak_ffma"]
 
@@ -73,6 +73,7 @@ def load(build_if_missing=True):
         lib.corr_ncc_get_method.argtypes = []
         lib.corr_xcorr_f32.argtypes = [vp, c_int, vp, c_int, c_int, c_int, vp]
         lib.corr_xcorr_f32_noalloc.argtypes = [vp, c_int, vp, c_int, c_int, c_int, vp]
+        lib.corr_scratch_reserved.argtypes = [ctypes.POINTER(ctypes.c_size_t)]
         lib.corr_set_stream.argtypes = [vp]
         lib.corr_get_stream.argtypes = []
         lib.corr_get_stream.restype = vp
@@ -84,7 +85,7 @@ def load(build_if_missing=True):
         lib.corr_peak_ffma.argtypes = [c_dbl_p, c_dbl_p]
         for f in (lib.corr_ncc_u8, lib.corr_ncc_u8_pitched, lib.corr_ncc_set_method,
                   lib.corr_ncc_get_method,
-                  lib.corr_xcorr_f32, lib.corr_xcorr_f32_noalloc,
+                  lib.corr_xcorr_f32, lib.corr_xcorr_f32_noalloc, lib.corr_scratch_reserved,
                   lib.corr_set_stream,
                   lib.corr_last_cuda_error, lib.corr_version,
                   lib.corr_peak_dp4a, lib.corr_peak_ffma):
@@ -102,8 +103,27 @@ def _check(rc):
 
 def _bind_stream(device):
     lib = load()
-    lib.corr_set_stream(ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream))
+    lib.corr_set_stream(torch.cuda.current_stream(device).cuda_stream)
     return lib
+
+
+class _Nothing:
+    def __enter__(self):
+        return None
+
+    def __exit__(self, *exc):
+        return False
+
+
+_NOTHING = _Nothing()
+
+
+def _on_device(dev):
+    """torch.cuda.device(dev) unless dev is already current (the common
+    case, where switching costs two runtime calls for nothing)."""
+    if dev.index is None or dev.index == torch.cuda.current_device():
+        return _NOTHING
+    return torch.cuda.device(dev)
 
 
 def _require_cuda():
@@ -166,19 +186,20 @@ def ncc_u8_into(image, tmpl, sums_out, coef_out, method=None):
     tmpl = tmpl.contiguous()
     if method is not None and method not in _NCC_METHODS:
         raise ValueError(f"method must be one of {sorted(_NCC_METHODS)}")
-    with torch.cuda.device(dev):
+    args = (image.data_ptr(), w, h, pitch, tmpl.data_ptr(), wt, ht,
+            sums_out.data_ptr() if sums_out is not None else None,
+            coef_out.data_ptr() if coef_out is not None else None)
+    with _on_device(dev):
         lib = _bind_stream(dev)
-        prev = lib.corr_ncc_get_method()
-        if method is not None:
+        if method is None:
+            _check(lib.corr_ncc_u8_pitched(*args))
+        else:
+            prev = lib.corr_ncc_get_method()
             _check(lib.corr_ncc_set_method(_NCC_METHODS[method]))
-        try:
-            _check(lib.corr_ncc_u8_pitched(
-                ctypes.c_void_p(image.data_ptr()), w, h, pitch,
-                ctypes.c_void_p(tmpl.data_ptr()), wt, ht,
-                ctypes.c_void_p(sums_out.data_ptr() if sums_out is not None else 0),
-                ctypes.c_void_p(coef_out.data_ptr() if coef_out is not None else 0)))
-        finally:
-            lib.corr_ncc_set_method(prev)
+            try:
+                _check(lib.corr_ncc_u8_pitched(*args))
+            finally:
+                lib.corr_ncc_set_method(prev)
     return sums_out, coef_out
 
 
@@ -227,11 +248,10 @@ def xcorr_f32_into(left, right, out):
     if tuple(out.shape) != (nl, nr, 2 * H - 1, 2 * W - 1) or not out.is_contiguous():
         raise ValueError("out must be a contiguous [nl, nr, 2H-1, 2W-1] tensor")
     left, right = left.contiguous(), right.contiguous()
-    with torch.cuda.device(dev):
+    with _on_device(dev):
         lib = _bind_stream(dev)
-        _check(lib.corr_xcorr_f32(ctypes.c_void_p(left.data_ptr()), nl,
-                                  ctypes.c_void_p(right.data_ptr()), nr, H, W,
-                                  ctypes.c_void_p(out.data_ptr())))
+        _check(lib.corr_xcorr_f32(left.data_ptr(), nl, right.data_ptr(), nr, H, W,
+                                  out.data_ptr()))
     return out
 
 
@@ -253,11 +273,10 @@ def xcorr_f32_noalloc_into(left, right, out):
     if tuple(out.shape) != (nl, nr, 2 * H - 1, 2 * W - 1) or not out.is_contiguous():
         raise ValueError("out must be a contiguous [nl, nr, 2H-1, 2W-1] tensor")
     left, right = left.contiguous(), right.contiguous()
-    with torch.cuda.device(dev):
+    with _on_device(dev):
         lib = _bind_stream(dev)
-        _check(lib.corr_xcorr_f32_noalloc(ctypes.c_void_p(left.data_ptr()), nl,
-                                          ctypes.c_void_p(right.data_ptr()), nr, H, W,
-                                          ctypes.c_void_p(out.data_ptr())))
+        _check(lib.corr_xcorr_f32_noalloc(left.data_ptr(), nl, right.data_ptr(), nr, H, W,
+                                          out.data_ptr()))
     return out
 
 
@@ -284,6 +303,19 @@ def xcorr_f32(left, right, device=None):
                       device=left.device)
     xcorr_f32_into(left, right, out)
     return out.cpu() if host else out
+
+
+def scratch_reserved(device=None):
+    """Bytes of device memory the library's scratch pool holds on the
+    device right now (0 once the calls that used scratch have been
+    synchronised)."""
+    _require_cuda()
+    dev = torch.device(device) if device is not None else torch.device(
+        "cuda", torch.cuda.current_device())
+    n = ctypes.c_size_t()
+    with torch.cuda.device(dev):
+        _check(load().corr_scratch_reserved(ctypes.byref(n)))
+    return n.value
 
 
 def peak_dp4a(shf_per_8=0, device=None):

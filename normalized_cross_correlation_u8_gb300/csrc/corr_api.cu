@@ -18,21 +18,28 @@ int cuda_status(cudaError_t e) {
   return CORR_ECUDA;
 }
 
-// The address at which the current device's kernels reach a caller buffer:
+// The calling thread's current device, or -1 (error cleared) if there is
+// none.
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  return dev;
+}
+
+// The address at which device `dev`'s kernels reach a caller buffer:
 // device or managed memory of this device as is; page-locked host memory
 // mapped into the device's address space by its device alias.  Anything
 // else (pageable host memory, another device's memory, an unknown address)
 // is refused with CORR_EINVAL before any launch.
 template <typename T>
-int device_view(T *p, T **out) {
+int device_view(int dev, T *p, T **out) {
+  if (dev < 0) return CORR_EINVAL;
   cudaPointerAttributes at;
   if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
     cudaGetLastError();   // clear the sticky-free error of an unknown pointer
-    return CORR_EINVAL;
-  }
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) {
-    cudaGetLastError();
     return CORR_EINVAL;
   }
   switch (at.type) {
@@ -54,10 +61,11 @@ int device_view(T *p, T **out) {
 
 // device_view of the three f32 buffers, each still 4-byte aligned.
 int device_views(const float **left, const float **right, float **out) {
+  const int dev = current_device();
   int rc;
-  if ((rc = device_view(*left, left)) != CORR_OK ||
-      (rc = device_view(*right, right)) != CORR_OK ||
-      (rc = device_view(*out, out)) != CORR_OK)
+  if ((rc = device_view(dev, *left, left)) != CORR_OK ||
+      (rc = device_view(dev, *right, right)) != CORR_OK ||
+      (rc = device_view(dev, *out, out)) != CORR_OK)
     return rc;
   if ((reinterpret_cast<uintptr_t>(*left) | reinterpret_cast<uintptr_t>(*right) |
        reinterpret_cast<uintptr_t>(*out)) & 3)
@@ -83,11 +91,14 @@ int corr_ncc_u8_pitched(const uint8_t *image, int w, int h, size_t pitch,
   if (pitch < size_t(w)) return CORR_EINVAL;
   if (wt > w || ht > h) return CORR_EINVAL;
   if (int64_t(wt) * ht > CORR_NCC_MAX_TEMPLATE_PIXELS) return CORR_EUNSUPPORTED;
+  if (int64_t(ht) * ((wt + 3) / 4) > CORR_NCC_MAX_GENERAL_TEMPLATE_WORDS)
+    return CORR_EUNSUPPORTED;
+  const int dev = current_device();
   int rc;
-  if ((rc = device_view(image, &image)) != CORR_OK ||
-      (rc = device_view(tmpl, &tmpl)) != CORR_OK ||
-      (sums_out && (rc = device_view(sums_out, &sums_out)) != CORR_OK) ||
-      (coef_out && (rc = device_view(coef_out, &coef_out)) != CORR_OK))
+  if ((rc = device_view(dev, image, &image)) != CORR_OK ||
+      (rc = device_view(dev, tmpl, &tmpl)) != CORR_OK ||
+      (sums_out && (rc = device_view(dev, sums_out, &sums_out)) != CORR_OK) ||
+      (coef_out && (rc = device_view(dev, coef_out, &coef_out)) != CORR_OK))
     return rc;
   // output planes are addressed with size_t, coordinates with int
   const int method = tls_ncc_method == CORR_NCC_METHOD_BOX ? corr::kMethodBox
@@ -138,6 +149,11 @@ int corr_xcorr_f32_noalloc(const float *left, int nl, const float *right, int nr
   if ((rc = device_views(&left, &right, &out)) != CORR_OK) return rc;
   return cuda_status(
       corr::xcorr_f32_noalloc_launch(left, nl, right, nr, H, W, out, tls_stream));
+}
+
+int corr_scratch_reserved(size_t *bytes) {
+  if (!bytes) return CORR_EINVAL;
+  return cuda_status(corr::scratch_reserved(bytes));
 }
 
 int corr_set_stream(void *stream) {

@@ -21,6 +21,10 @@ cudaError_t allow_dynamic_smem(const void *kernel);
 // current device (scratch.cu); release it with cudaFreeAsync on `stream`.
 cudaError_t scratch_alloc(void **ptr, size_t bytes, cudaStream_t stream);
 
+// Device memory the library's pool on the current device holds right now
+// (0 if it has none).
+cudaError_t scratch_reserved(size_t *bytes);
+
 // Methods of the u8 fast path (corr.h: CORR_NCC_METHOD_*).
 constexpr int kMethodDp4a = 0;   // SumI, SumISq, SumIT all by dp4a in the tiled kernel
 constexpr int kMethodBox = 1;    // SumI, SumISq as box sums of the tile; SumIT by dp4a

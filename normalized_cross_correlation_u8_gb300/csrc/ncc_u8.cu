@@ -32,7 +32,6 @@ cudaError_t ncc_u8_launch(const uint8_t *image, int w, int h, size_t pitch,
   a.plane = size_t(a.ow) * a.oh;
   a.rows = R;
   a.staged = 0;
-  const size_t smem = size_t(ht) * a.wtp * 4;   // general path: the template
 
   // whole-vector staging needs every row start and width on the vector size
   const bool aligned8 =
@@ -68,6 +67,10 @@ cudaError_t ncc_u8_launch(const uint8_t *image, int w, int h, size_t pitch,
     return table[a.wtw - 1](a, ts, vb, stream);
   }
 general:
+  // the general kernel walks template words one at a time: rows packed at
+  // their own word count, not padded to whole 16-byte vectors
+  a.wtp = a.wtw;
+  const size_t smem = size_t(ht) * a.wtp * 4;
   a.tiles_x = (a.ow + kUnitCols - 1) / kUnitCols;
   const long long units = (long long)a.tiles_x * ((a.oh + R - 1) / R);
   if (units > 0x7fffffffLL - kWarpsPerCta) return cudaErrorInvalidConfiguration;

@@ -1,7 +1,9 @@
 // scratch.cu -- temporary device memory for the kernels of libcorr.so:
-// stream-ordered allocations from one library-owned pool per device whose
-// release threshold is unlimited, so blocks freed by one call are reused by
-// the next without going back to the driver.
+// stream-ordered allocations from one library-owned pool per device.  The
+// pool's release threshold is zero, so the library keeps nothing between
+// calls: a block freed by one call is reused by the next call queued before
+// the stream (or device) is synchronised, and handed back to the driver at
+// that synchronisation.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -29,7 +31,7 @@ cudaError_t scratch_pool(cudaMemPool_t *pool) {
     props.location.id = dev;
     cudaMemPool_t p;
     if ((e = cudaMemPoolCreate(&p, &props)) != cudaSuccess) return e;
-    uint64_t keep = ~uint64_t(0);
+    uint64_t keep = 0;
     if ((e = cudaMemPoolSetAttribute(p, cudaMemPoolAttrReleaseThreshold, &keep)) !=
         cudaSuccess) {
       cudaMemPoolDestroy(p);
@@ -42,6 +44,25 @@ cudaError_t scratch_pool(cudaMemPool_t *pool) {
 }
 
 }  // namespace
+
+cudaError_t scratch_reserved(size_t *bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  *bytes = 0;
+  if (dev < 0 || dev >= kMaxDevices) return cudaSuccess;
+  cudaMemPool_t pool;
+  {
+    std::lock_guard<std::mutex> lock(g_pool_mu);
+    pool = g_pools[dev];
+  }
+  if (!pool) return cudaSuccess;
+  uint64_t v = 0;
+  if ((e = cudaMemPoolGetAttribute(pool, cudaMemPoolAttrReservedMemCurrent, &v)) != cudaSuccess)
+    return e;
+  *bytes = size_t(v);
+  return cudaSuccess;
+}
 
 cudaError_t scratch_alloc(void **ptr, size_t bytes, cudaStream_t stream) {
   cudaMemPool_t pool;

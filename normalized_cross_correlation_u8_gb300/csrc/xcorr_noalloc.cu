@@ -11,7 +11,10 @@
 // array that is part of the library image, so the call allocates nothing.
 //
 // The array is CORR_XCORR_NOALLOC_SCRATCH_BYTES (16 MiB) long.  Every GPU on
-// which the library's device code is loaded holds it until the process exits.
+// which the library's device code is loaded holds it until the process exits;
+// its memory is committed when the driver loads this file's module, which
+// under lazy module loading is the first cudaGetSymbolAddress below (the
+// first call on a device whose shape needs scratch).
 // All calls on all streams share it: calls that overlap on the GPU race on it,
 // so a caller must order them (one stream, or events).  Nothing in it needs to
 // start at zero -- every partial sum a call reads was written earlier in the

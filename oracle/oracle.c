@@ -42,7 +42,7 @@
 #define ORACLE_EUNSUPPORTED (-2)
 
 /* N*255^2 must fit the unsigned 32-bit accumulators [H15] use. */
-#define ORACLE_MAX_TEMPLATE_PIXELS 66052L
+#define ORACLE_MAX_TEMPLATE_PIXELS 66051L
 
 /* ---------------------------------------------------------------------- */
 /* u8 normalized cross-correlation [H15]                                   */

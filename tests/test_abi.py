@@ -71,8 +71,12 @@ def test_ncc_method_setting():
     ((FAKE, 16, 16, FAKE, 20, 4, FAKE, FAKE), -1),           # template wider
     ((FAKE, 16, 16, FAKE, 4, 17, FAKE, FAKE), -1),           # template taller
     ((FAKE, 16, 16, FAKE, 0, 4, FAKE, FAKE), -1),            # empty template
-    ((FAKE, 300, 300, FAKE, 257, 258, FAKE, FAKE), -2),      # odd width, > 66052 pixels
-    ((FAKE, 1000, 1000, FAKE, 260, 260, FAKE, FAKE), -2),    # > 66052 pixels
+    ((FAKE, 300, 300, FAKE, 257, 258, FAKE, FAKE), -2),      # odd width, > 66051 pixels
+    ((FAKE, 1000, 1000, FAKE, 260, 260, FAKE, FAKE), -2),    # > 66051 pixels
+    ((FAKE, 16513, 300, FAKE, 16513, 4, FAKE, FAKE), -2),    # 66052 pixels: SumISq may wrap
+    ((FAKE, 369, 300, FAKE, 369, 179, FAKE, FAKE), -1),      # 66051 pixels: accepted; fake buffer
+    ((FAKE, 4, 60000, FAKE, 1, 58001, FAKE, FAKE), -2),      # 58001 template words
+    ((FAKE, 4, 60000, FAKE, 1, 58000, FAKE, FAKE), -1),      # 58000 words: accepted; fake buffer
     ((FAKE, 16, 16, FAKE, -4, 4, FAKE, FAKE), -1),
 ])
 def test_ncc_argument_errors(args, code):
@@ -84,7 +88,7 @@ def test_ncc_argument_errors(args, code):
     ((FAKE, 16, 16, 0, FAKE, 4, 4, FAKE, FAKE), -1),
     ((None, 16, 16, 32, FAKE, 4, 4, FAKE, FAKE), -1),        # null image
     ((FAKE, 16, 16, 32, FAKE, 20, 4, FAKE, FAKE), -1),       # template wider
-    ((FAKE, 300, 300, 512, FAKE, 257, 258, FAKE, FAKE), -2), # > 66052 pixels
+    ((FAKE, 300, 300, 512, FAKE, 257, 258, FAKE, FAKE), -2), # > 66051 pixels
 ])
 def test_ncc_pitched_argument_errors(args, code):
     assert corr.load().corr_ncc_u8_pitched(*args) == code

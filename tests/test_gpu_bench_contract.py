@@ -36,6 +36,6 @@ def test_bench_line_contract():
     assert 0.05 < rf["frac"] < 1.2
     # achieved = algorithmic dp4a per launch / mean launch time
     per = int(rf["algorithmic_per_unit"].split()[0])
-    assert per == 256                      # 32x32 template, box form: one dp4a per 4 pixels
+    assert per == 1024                     # 64x64 template, box form: one dp4a per 4 pixels
     assert rf["achieved"] * 1e12 == pytest.approx(
         offsets * per / (d["ms_per_step"] * 1e-3), rel=1e-6)

@@ -177,7 +177,7 @@ def test_single_offset_and_thin_shapes():
 
 @pytest.mark.parametrize("h,w,wt,ht", [(260, 264, 256, 258), (440, 300, 128, 430)])
 def test_largest_template(h, w, wt, ht):
-    """wt*ht close to 66052: SumISq near the uint32 limit, on the general
+    """wt*ht close to 66051: SumISq near the uint32 limit, on the general
     path (256 x 258) and on the fast path (128 x 430, a tile that fits the
     shared memory of both forms) with both methods (the box sums' slides
     wrap modulo 2^32 and must still land on the exact sums)."""
@@ -232,9 +232,39 @@ def test_guard_bands_untouched():
 def test_argument_errors_raise():
     dev = torch.device("cuda", 0)
     img = torch.zeros(300, 300, dtype=torch.uint8, device=dev)
-    with pytest.raises(corr.CorrError) as e:   # 258 x 257 > 66052 template pixels
+    with pytest.raises(corr.CorrError) as e:   # 258 x 257 > 66051 template pixels
         corr.ncc_u8(img, torch.zeros(258, 257, dtype=torch.uint8, device=dev))
     assert e.value.code == -2
+    tall = torch.zeros(16520, 8, dtype=torch.uint8, device=dev)
+    with pytest.raises(corr.CorrError) as e:   # 4 x 16513 = 66052 pixels: SumISq may wrap
+        corr.ncc_u8(tall, torch.zeros(16513, 4, dtype=torch.uint8, device=dev))
+    assert e.value.code == -2
+
+
+@pytest.mark.parametrize("h,w,wt,ht", [(200, 400, 369, 179), (7400, 40, 9, 7339),
+                                       (440, 300, 128, 430)])
+def test_all_255_at_the_size_limit(h, w, wt, ht):
+    """All-255 image and template: SumISq and SumIT reach 65025 N, at the
+    32-bit limit N = 66051 on the general kernel (369 x 179, and the narrow
+    9 x 7339), and at the largest template the fast kernel takes (128 x 430),
+    with both methods."""
+    image = np.full((h, w), 255, np.uint8)
+    tmpl = np.full((ht, wt), 255, np.uint8)
+    ref = oracle.ncc_u8(image, tmpl, nthreads=NT)
+    for method in ("box", "dp4a"):
+        s, c = run_gpu(image, tmpl, method=method)
+        assert_parity(image, tmpl, s, c, ref)
+        assert (s[1] == 65025 * wt * ht).all() and (s[2] == 65025 * wt * ht).all()
+
+
+@pytest.mark.parametrize("h,w,wt,ht", [(15000, 8, 3, 14600), (16100, 24, 4, 16000)])
+def test_tall_narrow_template_general_kernel(h, w, wt, ht):
+    """Templates a few pixels wide and thousands tall: the general kernel
+    packs each row into its own word count (one word here)."""
+    image, tmpl = rand_u8(h, w), rand_u8(ht, wt)
+    for method in ("box", "dp4a"):
+        s, c = run_gpu(image, tmpl, method=method)
+        assert_parity(image, tmpl, s, c)
 
 
 @pytest.mark.parametrize("method", ["box", "dp4a"])

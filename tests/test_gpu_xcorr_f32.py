@@ -148,6 +148,20 @@ def test_workload_n_to_m_full():
     check(w.left, w.right)
 
 
+def test_scratch_is_not_kept_between_calls():
+    """A banded shape (one 256x256 pair: two row bands) takes pool scratch
+    for its partial sums; once the device is synchronised the library holds
+    no device memory."""
+    dev = torch.device("cuda", 0)
+    L = torch.from_numpy(rand(1, 256, 256)).to(dev)
+    R = torch.from_numpy(rand(1, 256, 256)).to(dev)
+    out = torch.empty((1, 1, 511, 511), dtype=torch.float32, device=dev)
+    for _ in range(3):
+        corr.xcorr_f32_into(L, R, out)          # queued back to back: one block reused
+    torch.cuda.synchronize()
+    assert corr.scratch_reserved(dev) == 0
+
+
 @pytest.mark.parametrize("nl,nr,H,W", [(1, 2, 130, 257), (1, 1, 24, 800), (2, 2, 3, 700)])
 def test_rows_kernels_item_loop(nl, nr, H, W, monkeypatch):
     """The rows kernels' work-item loop (taken by grids larger than 2^30

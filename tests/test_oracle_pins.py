@@ -207,7 +207,23 @@ def test_u8_argument_errors():
     with pytest.raises(oracle.oracle.OracleError):
         oracle.ncc_u8(rand_u8(4, 4), rand_u8(5, 4))       # template taller
     with pytest.raises(oracle.oracle.OracleError):
-        oracle.ncc_u8(rand_u8(300, 300), rand_u8(258, 258))  # > 66052 px
+        oracle.ncc_u8(rand_u8(300, 300), rand_u8(258, 258))  # > 66051 px
+
+
+@pytest.mark.parametrize("wt,ht", [(369, 179), (9, 7339)])
+def test_u8_sums_at_the_template_size_limit(wt, ht):
+    """Closed form at the 32-bit limit: N = 66051 pixels of 255 over a
+    window of 255s give SumI = 255 N, SumISq = SumIT = 65025 N =
+    4 294 966 275, the largest value below 2^32 any template can reach.
+    One pixel more (66052 * 65025 >= 2^32) is refused."""
+    assert wt * ht == 66051
+    image = np.full((ht + 1, wt + 2), 255, np.uint8)
+    s, c64, _ = oracle.ncc_u8(image, np.full((ht, wt), 255, np.uint8))
+    assert (s[0] == 255 * 66051).all()
+    assert (s[1] == 65025 * 66051).all() and (s[2] == 65025 * 66051).all()
+    assert (c64 == 0).all()                      # flat template
+    with pytest.raises(oracle.oracle.OracleError):
+        oracle.ncc_u8(np.full((5, 16513), 255, np.uint8), np.full((4, 16513), 255, np.uint8))
 
 
 # --------------------------------------------------------------------------

@@ -4,14 +4,21 @@ for their own allocator, plug-ins whose host forbids driver allocations,
 loops that must never wait on an allocator).  Its split-row scratch is a
 fixed array inside the library instead of pool memory.
 
-Checked here, through the C ABI: two calls in a row agree with
-corr_xcorr_f32 on the same inputs within the f32 parity bar (1e-5 * sum|L*R|
-per output), on a shape that uses the scratch (256x256, two row bands) and
-on shapes that need none; and a shape needing more than the array holds is
-rejected with CORR_EUNSUPPORTED before anything runs.  This file is collected
-last so that a failure here stops a -x run only after every other test.
+Checked here, through the C ABI, on two calls in a row:
+  * every output of every pair against the fp64 oracle, within the f32
+    parity bar (1e-5 * sum|L*R| over that output's own overlap);
+  * bit-identity with corr_xcorr_f32 (same plan, same kernels, same
+    summation order) on every pair;
+  * a banded shape run after a different banded / segmented shape has left
+    its own partial sums in the array (a slot the second call failed to
+    write would then show up as a wrong value, not as a zero);
+  * a shape needing more than the array holds is rejected with
+    CORR_EUNSUPPORTED before anything runs.
+This file is collected last so that a failure here stops a -x run only after
+every other test.
 """
 import ctypes
+import os
 
 import numpy as np
 import pytest
@@ -22,6 +29,7 @@ import oracle
 
 pytestmark = pytest.mark.gpu
 REL_TOL = 1e-5
+NT = max(1, os.cpu_count() or 1)
 
 
 def call(fn, L, R, out):
@@ -32,31 +40,58 @@ def call(fn, L, R, out):
               R.shape[0], H, W, ctypes.c_void_p(out.data_ptr()))
 
 
-@pytest.mark.parametrize("nl,nr,H,W", [(1, 1, 256, 256), (1, 2, 130, 257), (1, 1, 24, 800), (2, 3, 40, 40),
-                                       (32, 64, 16, 16)])
-def test_noalloc_matches_allocating_entry_point(nl, nr, H, W):
-    rng = np.random.default_rng(77 + H)
+def inputs(nl, nr, H, W, seed):
+    rng = np.random.default_rng(seed)
     left = rng.uniform(-1, 1, size=(nl, H, W)).astype(np.float32)
     right = rng.uniform(-1, 1, size=(nr, H, W)).astype(np.float32)
     dev = torch.device("cuda", 0)
-    L, R = torch.from_numpy(left).to(dev), torch.from_numpy(right).to(dev)
-    shape = (nl, nr, 2 * H - 1, 2 * W - 1)
-    ref = torch.empty(shape, dtype=torch.float32, device=dev)
+    return left, right, torch.from_numpy(left).to(dev), torch.from_numpy(right).to(dev)
+
+
+def run_both(L, R, calls=2):
+    """corr_xcorr_f32 once, then corr_xcorr_f32_noalloc `calls` times into
+    NaN-filled buffers; returns (reference, [noalloc outputs]) on the host."""
+    nl, H, W = L.shape
+    shape = (nl, R.shape[0], 2 * H - 1, 2 * W - 1)
     lib = corr.load()
+    ref = torch.empty(shape, dtype=torch.float32, device=L.device)
     assert call(lib.corr_xcorr_f32, L, R, ref) == 0
-    # |L|*|R| correlation bounds each output's rounding error
-    _, ab = oracle.xcorr_f32(np.abs(left[:1]), np.abs(right[:1]))
-    for _ in range(2):
-        got = torch.full(shape, float("nan"), dtype=torch.float32, device=dev)
+    outs = []
+    for _ in range(calls):
+        got = torch.full(shape, float("nan"), dtype=torch.float32, device=L.device)
         assert call(lib.corr_xcorr_f32_noalloc, L, R, got) == 0
         torch.cuda.synchronize()
-        g, r = got.cpu().numpy().astype(np.float64), ref.cpu().numpy().astype(np.float64)
+        outs.append(got.cpu())
+    return ref.cpu(), outs
+
+
+@pytest.mark.parametrize("nl,nr,H,W", [(1, 1, 256, 256), (1, 2, 130, 257), (1, 1, 24, 800),
+                                       (2, 3, 40, 40), (32, 64, 16, 16)])
+def test_noalloc_matches_oracle_and_allocating_entry_point(nl, nr, H, W):
+    left, right, L, R = inputs(nl, nr, H, W, 77 + H)
+    ref, outs = run_both(L, R)
+    exact, ab = oracle.xcorr_f32(left, right, nthreads=NT)
+    for got in outs:
+        assert torch.equal(got, ref)             # every pair, bit for bit
+        g = got.numpy().astype(np.float64)
         assert np.isfinite(g).all()
-        err = np.abs(g - r)
-        # pair (0, 0) against its own |L||R| bound; all pairs against a bound
-        # scaled by the matrices' size
-        assert (err[0, 0] <= REL_TOL * ab[0, 0] + 1e-30).all()
-        assert err.max() <= REL_TOL * H * W
+        err = np.abs(g - exact)
+        worst = np.unravel_index(np.argmax(err - REL_TOL * ab), err.shape)
+        assert (err <= REL_TOL * ab + 1e-30).all(), \
+            f"error {err[worst]} > {REL_TOL} * {ab[worst]} at {worst}"
+
+
+def test_noalloc_after_another_shape_left_data_in_the_array():
+    """Two banded / segmented shapes back to back: the second call's reads
+    of the shared array must all be of slots it wrote itself."""
+    _, _, L1, R1 = inputs(1, 1, 24, 800, 5)      # three x segments
+    assert call(corr.load().corr_xcorr_f32_noalloc, L1, R1,
+                torch.empty((1, 1, 47, 1599), dtype=torch.float32, device=L1.device)) == 0
+    left, right, L, R = inputs(1, 1, 256, 256, 6)   # two row bands
+    ref, outs = run_both(L, R, calls=1)
+    assert torch.equal(outs[0], ref)
+    exact, ab = oracle.xcorr_f32(left, right, nthreads=NT)
+    assert (np.abs(outs[0].numpy().astype(np.float64) - exact) <= REL_TOL * ab + 1e-30).all()
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
