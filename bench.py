@@ -2,21 +2,25 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-One step = one corr_ncc_u8 call over the 1920x1080 uint8 image with a 32x32
-template (every valid offset: SumI, SumISq, SumIT and the coefficient), i.e.
-template prep, tile loads, window packing, dp4a accumulation, the box sums
-and the epilogue, all in one launch, with the library's default method (the
-box form: SumI / SumISq as box filters of the staged tile, SumIT by one
-unsigned dp4a per 4 pixels).  Inputs are resident in HBM when the timed
-region starts; a 256 MB buffer is written between steps so every step starts
-with a cold L2 (the workload's inputs and outputs would otherwise fit in the
-129 MB L2).  Prints one JSON line.
+One step = one corr_ncc_u8 call over the 4096x4096 uint8 image with a 64x64
+template (every valid offset, 16 265 089 of them: SumI, SumISq, SumIT and the
+coefficient), i.e. template prep, tile loads, window packing, dp4a
+accumulation, the box sums and the epilogue, all in one launch, with the
+library's default method (the box form: SumI / SumISq as box filters of the
+staged tile, SumIT by one unsigned dp4a per 4 pixels).  Inputs are resident
+in HBM when the timed region starts; before every step a 256 MB read flushes
+L2 (its outputs, 260 MB, exceed L2 anyway), and the write-back of the output
+lines a step leaves dirty in L2 is measured separately ("writeback").  Prints
+one JSON line.
 
 The line also carries the same step with the pages' method (all three sums
-by dp4a, "method_dp4a"), per workload the kernel-only throughput of both
-methods and its roofline fraction for the other five workloads (u8 256x256 /
-4096x4096 and the three f32 cross-correlation batches), an end-to-end number
-through host buffers, and the CPU oracle's throughput on a bounded sample.
+by dp4a, "method_dp4a"), the 1920x1080 / 32x32 step with both methods
+("secondary"), per workload the kernel-only throughput and roofline fraction
+of all six workloads (u8 256x256 / 1920x1080 / 4096x4096 and the three f32
+cross-correlation batches), an FFT cross-correlation comparison
+("fft_comparison"), an end-to-end number through host buffers with the
+copy-only link rates beside it, and the CPU oracle's throughput on a bounded
+sample.
 
 --impl reference times the CPU oracle (the only reference implementation:
 the pages ship no code) on the same workload and metric.
@@ -39,7 +43,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "NCC offsets/s (u8) and xcorr GFLOP/s (f32) on 1 GB300; % of roofline"
 UNIT = "offsets/s"
-HEADLINE = "ncc_1080p"
+HEADLINE = "ncc_4k"
 SM_MAX_MHZ_NOMINAL = 2070.0
 DP4A_PER_SM_CLK = 64     # unsigned dp4a issue per SM per clock (probe: 63.7)
 FFMA_PER_SM_CLK = 128    # FP32 FMA per SM per clock (probe: 124 at live clock)
@@ -164,8 +168,11 @@ class ClockSampler:
 # --------------------------------------------------------------------------
 
 def make_flush(torch, dev):
-    buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
-    return lambda: buf.fill_(1)
+    """L2 flush: a 256 MB read (twice the L2) into one scalar.  A read
+    leaves clean lines behind, so the next step pays no write-back for it."""
+    buf = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    acc = torch.zeros((), dtype=torch.int64, device=dev)
+    return lambda: torch.sum(buf, dtype=torch.int64, out=acc)
 
 
 def event_time_steps(torch, fn, steps, flush):
@@ -260,8 +267,75 @@ def dp4a_per_offset(w, method="box"):
     return words if method == "box" else 3 * words
 
 
+def ncc_roofline(w, avg_s, sms, method="box", sm_mhz=None):
+    """Roofline of one u8 step: unsigned dp4a per offset (the algorithm's
+    own count) x offsets / the step's mean device time, against the dp4a
+    issue peak (152 SMs x 64 per clock x the maximum SM clock)."""
+    per = dp4a_per_offset(w, method)
+    peak = sms * DP4A_PER_SM_CLK * SM_MAX_MHZ_NOMINAL * 1e6
+    achieved = w.offsets * per / avg_s
+    ht, wt = w.tmpl.shape
+    r = {"bound": "alu",
+         "kernel": ("ncc_u8_fixed_kernel, box form (unsigned dp4a issue; SumIT only)"
+                    if method == "box" else
+                    "ncc_u8_fixed_kernel, three-dp4a form (unsigned dp4a issue; 3 sums)"),
+         "achieved": achieved / 1e12, "peak": peak / 1e12, "unit": "Tdp4a/s",
+         "frac": achieved / peak,
+         "peak_basis": (f"{sms} SMs x {DP4A_PER_SM_CLK} dp4a/clk x "
+                        f"{SM_MAX_MHZ_NOMINAL:.0f} MHz max clock (measured issue rate; "
+                        "MEASURED_PEAKS.json has no dp4a entry)"),
+         "algorithmic_per_unit": (
+             f"{per} dp4a per offset (1 per 4 template pixels, SumIT; SumI / SumISq "
+             f"are box sums: {ht + wt} adds per offset amortised, not counted)"
+             if method == "box" else f"{per} dp4a per offset (3 per 4 template pixels)"),
+         "hbm_bytes_algorithmic": int(w.image.size + w.tmpl.size + 16 * w.offsets)}
+    if sm_mhz:
+        r["frac_at_live_clock"] = achieved / (sms * DP4A_PER_SM_CLK * sm_mhz * 1e6)
+    return r
+
+
+def writeback_estimate(torch, fn, flush, reps=20):
+    """Device time of writing back the dirty lines one step leaves in L2:
+    the L2 flush (a 256 MB read, so it leaves clean lines) timed right after
+    a step, minus the same flush timed after another flush.  The timed steps
+    start after such a flush, so they never pay for an earlier write-back."""
+    stream = torch.cuda.current_stream()
+
+    def timed(pre):
+        ts = []
+        for _ in range(reps):
+            flush()
+            pre()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            flush()
+            e1.record(stream)
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+    dirty = timed(fn)
+    clean = timed(flush)
+    return max(0.0, dirty - clean) * 1e3, dirty * 1e3, clean * 1e3
+
+
+def ncc_step_summary(torch, corr, w, dev, flush, sms, steps, method=None):
+    """A u8 step timed per launch with CUDA events (L2 flushed before each),
+    with its roofline and the write-back of its outputs."""
+    *_, fn = ncc_buffers(torch, corr, w, dev, method=method)
+    for _ in range(3):
+        flush()
+        fn()
+    t = event_time_steps(torch, fn, steps, flush)
+    avg_s = (sum(t) / steps) * 1e-3
+    wb_us, _, _ = writeback_estimate(torch, fn, flush, reps=10)
+    return {"workload": w.name, "value": w.offsets / avg_s, "unit": UNIT, "steps": steps,
+            "ms_per_step": avg_s * 1e3,
+            "roofline": ncc_roofline(w, avg_s, sms, method or "box"),
+            "writeback": {"us_per_step": wb_us,
+                          "value_with_writeback": w.offsets / (avg_s + wb_us * 1e-6)}}
+
+
 def run_ours(args, world, rank, local):
-    import numpy as np
     import torch
 
     import normalized_cross_correlation_u8_gb300 as corr
@@ -300,43 +374,45 @@ def run_ours(args, world, rank, local):
 
     avg_launch_s = (sum(times) / args.steps) * 1e-3
     sm_mhz = clocks["sm_mhz"] if clocks else SM_MAX_MHZ_NOMINAL
-    dp4a_peak = sms * DP4A_PER_SM_CLK * SM_MAX_MHZ_NOMINAL * 1e6
-    achieved = w.offsets * dp4a_per_offset(w) / avg_launch_s
     ncc_src = [os.path.join(ROOT, "normalized_cross_correlation_u8_gb300", "csrc", f)
                for f in ("ncc_u8.cu", "ncc_u8_box.cu", "ncc_u8_kernels.cuh")]
-    roofline = {
-        "bound": "alu",
-        "kernel": "ncc_u8_fixed_kernel, box form (unsigned dp4a issue; SumIT only)",
-        "achieved": achieved / 1e12, "peak": dp4a_peak / 1e12, "unit": "Tdp4a/s",
-        "frac": achieved / dp4a_peak,
-        "peak_basis": f"{sms} SMs x {DP4A_PER_SM_CLK} dp4a/clk x {SM_MAX_MHZ_NOMINAL:.0f} MHz max clock",
-        "frac_at_live_clock": achieved / (sms * DP4A_PER_SM_CLK * sm_mhz * 1e6),
-        "probe_dp4a_per_s": dp4a_probe / 1e12,
-        "algorithmic_per_unit": (f"{dp4a_per_offset(w)} dp4a per offset (1 per 4 template "
-                                 "pixels, SumIT; SumI / SumISq are box sums: "
-                                 f"{w.tmpl.shape[0] + w.tmpl.shape[1]} adds per offset "
-                                 "amortised, not counted)"),
-        "traffic": traffic_for("ncc_u8_1080p_box", ncc_src),
-        "hbm_bytes_algorithmic": int(w.image.size + w.tmpl.size + 16 * w.offsets),
-    }
+    roofline = ncc_roofline(w, avg_launch_s, sms, "box", sm_mhz)
+    roofline["probe_dp4a_per_s"] = dp4a_probe / 1e12
+    roofline["timing"] = "CUDA events per step on the launching stream, L2 flushed before each"
+    roofline["traffic"] = traffic_for("ncc_u8_4k_box", ncc_src)
+    wb_us, wb_dirty, wb_clean = writeback_estimate(torch, step, flush)
 
+    h, ww = w.image.shape
+    ht, wt = w.tmpl.shape
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "u8", "data": "synthetic",
-        "config": {"workload": w.name, "image": "1920x1080 uint8 (blurred noise, 30% > 127)",
-                   "template": "32x32 uint8 (patch + U[-8,8])", "offsets": w.offsets,
-                   "outputs": "SumI/SumISq/SumIT uint32 planes + coef f32",
-                   "l2": "flushed between steps (256 MB write)",
+        "config": {"workload": w.name, "image": f"{ww}x{h} uint8 (uniform [0,255])",
+                   "template": f"{wt}x{ht} uint8 (exact patch)", "offsets": w.offsets,
+                   "outputs": "SumI/SumISq/SumIT uint32 planes + coef f32 (260 MB, > L2)",
+                   "l2": "flushed before each step (256 MB read: leaves clean lines)",
                    "parallelism": f"replicas x{world}"},
         "gpu_launches": args.steps,
         "wall_s_timed_region": wall,
         "clocks": clocks, "roofline": roofline,
+        "writeback": {"us_per_step": wb_us, "flush_after_step_us": wb_dirty,
+                      "flush_after_flush_us": wb_clean,
+                      "value_with_writeback": w.offsets / (avg_launch_s + wb_us * 1e-6),
+                      "how": ("dirty output lines left in L2 by a step, written back by the "
+                              "next flush: flush time after a step minus after a flush")},
     }
 
     if args.extras and rank == 0:
-        line["method_dp4a"] = method_dp4a_headline(torch, corr, w, dev, flush, sms, args)
+        line["method_dp4a"] = ncc_step_summary(torch, corr, w, dev, flush, sms,
+                                               max(30, min(args.steps // 5, 400)), "dp4a")
+        w2 = wl.NCC_WORKLOADS["ncc_1080p"]()
+        line["secondary"] = {
+            "box": ncc_step_summary(torch, corr, w2, dev, flush, sms,
+                                    max(50, min(args.steps, 2000))),
+            "dp4a": ncc_step_summary(torch, corr, w2, dev, flush, sms,
+                                     max(50, min(args.steps, 2000)), "dp4a")}
         line["per_workload"] = extras_workloads(torch, corr, wl, dev, flush, sms,
                                                 dp4a_probe, ffma_probe)
         line["e2e"] = e2e_headline(torch, corr, w, dev, args)
@@ -344,28 +420,6 @@ def run_ours(args, world, rank, local):
     elif args.extras:
         line["e2e"] = None
     return line
-
-
-def method_dp4a_headline(torch, corr, w, dev, flush, sms, args):
-    """The headline step with the pages' method (SumI, SumISq and SumIT all
-    by dp4a in the tiled kernel), event-timed the same way, for comparison."""
-    *_, fn = ncc_buffers(torch, corr, w, dev, method="dp4a")
-    for _ in range(3):
-        flush()
-        fn()
-    steps = max(50, min(args.steps // 5, 2000))
-    t = event_time_steps(torch, fn, steps, flush)
-    avg_s = (sum(t) / steps) * 1e-3
-    dp4a_peak = sms * DP4A_PER_SM_CLK * SM_MAX_MHZ_NOMINAL * 1e6
-    achieved = w.offsets * dp4a_per_offset(w, "dp4a") / avg_s
-    return {"value": w.offsets / avg_s, "unit": UNIT, "steps": steps,
-            "ms_per_step": avg_s * 1e3,
-            "roofline": {"bound": "alu",
-                         "kernel": "ncc_u8_fixed_kernel (unsigned dp4a issue; 3 sums)",
-                         "achieved": achieved / 1e12, "peak": dp4a_peak / 1e12,
-                         "unit": "Tdp4a/s", "frac": achieved / dp4a_peak,
-                         "algorithmic_per_unit": f"{dp4a_per_offset(w, 'dp4a')} dp4a per "
-                                                 "offset (3 per 4 template pixels)"}}
 
 
 # Per-workload kernel durations: device time per launch from replaying a
@@ -453,7 +507,7 @@ def e2e_headline(torch, corr, w, dev, args, nstreams=E2E_STREAMS):
     for i in range(2 * nstreams):
         step(i)
     torch.cuda.synchronize()
-    steps = max(60, min(args.steps // 10, 1200))
+    steps = max(20, min(args.steps // 10, 400))
     main = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(main)
@@ -466,10 +520,31 @@ def e2e_headline(torch, corr, w, dev, args, nstreams=E2E_STREAMS):
     e1.record(main)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
+    # the copies alone, one lane, same buffers: the host link's rates
+    st, img, tm, sd, cd, h_s, h_c = lanes[0]
+    d2h = int(sd.numel() * 4 + cd.numel() * 4)
+    h2d = int(w.image.nbytes + w.tmpl.nbytes)
+    reps = 10
+    with torch.cuda.stream(st):
+        e2, e3, e4 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        e2.record(st)
+        for _ in range(reps):
+            h_s.copy_(sd, non_blocking=True)
+            h_c.copy_(cd, non_blocking=True)
+        e3.record(st)
+        for _ in range(reps):
+            img.copy_(h_img, non_blocking=True)
+            tm.copy_(h_tm, non_blocking=True)
+        e4.record(st)
+    torch.cuda.synchronize()
+    d2h_gbs = d2h * reps / (e2.elapsed_time(e3) * 1e-3) / 1e9
+    h2d_gbs = h2d * reps / (e3.elapsed_time(e4) * 1e-3) / 1e9
     return {"value": w.offsets / (ms * 1e-3), "unit": UNIT,
-            "h2d_bytes_per_step": int(w.image.nbytes + w.tmpl.nbytes),
-            "d2h_bytes_per_step": int(lanes[0][3].numel() * 4 + lanes[0][4].numel() * 4),
-            "ms_per_step": ms, "steps": steps, "streams": nstreams}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": ms, "steps": steps, "streams": nstreams,
+            "copy_only": {"d2h_gbs": d2h_gbs, "h2d_gbs": h2d_gbs,
+                          "d2h_ms_per_step": d2h / d2h_gbs / 1e6,
+                          "how": f"{reps} back-to-back pinned copies of one step's buffers"}}
 
 
 # --------------------------------------------------------------------------
