@@ -32,6 +32,7 @@ extern "C" {
 #define CORR_EINVAL (-1)        /* null pointer, size <= 0, template larger than image */
 #define CORR_EUNSUPPORTED (-2)  /* a size the kernels do not handle (see each call) */
 #define CORR_ECUDA (-3)         /* CUDA runtime error (no device, launch failure, ...) */
+#define CORR_ETIMEOUT (-4)      /* a kernel gave up a bounded wait (corr_device_status) */
 
 /* Largest template (pixels) whose SumISq and SumIT (at most N * 255^2)
  * still fit the unsigned 32-bit accumulators: 66051 * 65025 < 2^32 <=
@@ -189,6 +190,14 @@ int corr_xcorr_f32(const float *left, int nl, const float *right, int nr,
 #define CORR_XCORR_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 int corr_xcorr_f32_noalloc(const float *left, int nl, const float *right, int nr,
                            int H, int W, float *out);
+
+/* Synchronises this thread's stream, then reports whether any of the
+ * library's kernels gave up a bounded wait since the previous call
+ * (CORR_ETIMEOUT: the outputs of the call that did are incomplete) or
+ * CORR_OK.  Only the tensor-core cross-correlation kernel waits on other
+ * units (the tensor cores' completion barriers); each wait ends after about
+ * a second, so a fault there returns an error instead of hanging the GPU. */
+int corr_device_status(void);
 
 /* Bytes of device memory the library's scratch pool holds on the current
  * device right now: nonzero only while calls that use scratch are queued or

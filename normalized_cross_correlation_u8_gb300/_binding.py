@@ -22,12 +22,13 @@ CORR_OK = 0
 CORR_EINVAL = -1
 CORR_EUNSUPPORTED = -2
 CORR_ECUDA = -3
+CORR_ETIMEOUT = -4
 NCC_MAX_TEMPLATE_PIXELS = 66051
 NCC_METHOD_DP4A = 0
 NCC_METHOD_BOX = 1
 _NCC_METHODS = {"dp4a": NCC_METHOD_DP4A, "box": NCC_METHOD_BOX}
 
-EXPORTS = ["corr_ncc_u8", "corr_ncc_u8_pitched", "corr_ncc_set_method", "corr_ncc_get_method", "corr_xcorr_f32", "corr_xcorr_f32_noalloc", "corr_scratch_reserved", "corr_set_stream",
+EXPORTS = ["corr_ncc_u8", "corr_ncc_u8_pitched", "corr_ncc_set_method", "corr_ncc_get_method", "corr_xcorr_f32", "corr_xcorr_f32_noalloc", "corr_device_status", "corr_scratch_reserved", "corr_set_stream",
            "corr_get_stream", "corr_strerror", "corr_last_cuda_error",
            "corr_version", "corr_peak_dp4a", "corr_peak_ffma"]
 
@@ -74,6 +75,7 @@ def load(build_if_missing=True):
         lib.corr_xcorr_f32.argtypes = [vp, c_int, vp, c_int, c_int, c_int, vp]
         lib.corr_xcorr_f32_noalloc.argtypes = [vp, c_int, vp, c_int, c_int, c_int, vp]
         lib.corr_scratch_reserved.argtypes = [ctypes.POINTER(ctypes.c_size_t)]
+        lib.corr_device_status.argtypes = []
         lib.corr_set_stream.argtypes = [vp]
         lib.corr_get_stream.argtypes = []
         lib.corr_get_stream.restype = vp
@@ -85,7 +87,7 @@ def load(build_if_missing=True):
         lib.corr_peak_ffma.argtypes = [c_dbl_p, c_dbl_p]
         for f in (lib.corr_ncc_u8, lib.corr_ncc_u8_pitched, lib.corr_ncc_set_method,
                   lib.corr_ncc_get_method,
-                  lib.corr_xcorr_f32, lib.corr_xcorr_f32_noalloc, lib.corr_scratch_reserved,
+                  lib.corr_xcorr_f32, lib.corr_xcorr_f32_noalloc, lib.corr_scratch_reserved, lib.corr_device_status,
                   lib.corr_set_stream,
                   lib.corr_last_cuda_error, lib.corr_version,
                   lib.corr_peak_dp4a, lib.corr_peak_ffma):
@@ -303,6 +305,14 @@ def xcorr_f32(left, right, device=None):
                       device=left.device)
     xcorr_f32_into(left, right, out)
     return out.cpu() if host else out
+
+
+def device_status():
+    """Synchronise the current stream and raise CorrError (CORR_ETIMEOUT)
+    if a library kernel gave up a bounded wait since the last check."""
+    _require_cuda()
+    lib = _bind_stream(torch.device("cuda", torch.cuda.current_device()))
+    _check(lib.corr_device_status())
 
 
 def scratch_reserved(device=None):

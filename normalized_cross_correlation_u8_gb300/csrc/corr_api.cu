@@ -151,6 +151,14 @@ int corr_xcorr_f32_noalloc(const float *left, int nl, const float *right, int nr
       corr::xcorr_f32_noalloc_launch(left, nl, right, nr, H, W, out, tls_stream));
 }
 
+int corr_device_status(void) {
+  cudaError_t e = cudaStreamSynchronize(tls_stream);
+  if (e != cudaSuccess) return cuda_status(e);
+  int gave_up = 0;
+  if ((e = corr::tc::take_status(&gave_up)) != cudaSuccess) return cuda_status(e);
+  return gave_up ? CORR_ETIMEOUT : CORR_OK;
+}
+
 int corr_scratch_reserved(size_t *bytes) {
   if (!bytes) return CORR_EINVAL;
   return cuda_status(corr::scratch_reserved(bytes));
@@ -169,6 +177,7 @@ const char *corr_strerror(int code) {
     case CORR_EINVAL: return "invalid argument";
     case CORR_EUNSUPPORTED: return "unsupported size";
     case CORR_ECUDA: return "CUDA runtime error";
+    case CORR_ETIMEOUT: return "a kernel gave up a bounded wait";
     default: return "unknown error code";
   }
 }

@@ -60,4 +60,20 @@ cudaError_t xcorr_f32_noalloc_launch(const float *left, int nl, const float *rig
                                      int nr, int H, int W, float *out,
                                      cudaStream_t stream);
 
+// Tensor-core form of the f32 cross-correlation for small matrices
+// (xcorr_tc.cu): H, W <= 16.
+namespace tc {
+bool supported(int nl, int nr, int H, int W);
+cudaError_t launch(const float *left, int nl, const float *right, int nr, int H, int W,
+                   float *out, cudaStream_t stream);
+// Reads and clears the flag the kernel sets when a bounded wait gave up.
+cudaError_t take_status(int *gave_up);
+}  // namespace tc
+
+// One warp per overlap with an in-warp reduction (xcorr_warp.cu).
+namespace warp {
+cudaError_t launch(const float *left, int nl, const float *right, int nr, int H, int W,
+                   float *out, cudaStream_t stream);
+}  // namespace warp
+
 }  // namespace corr

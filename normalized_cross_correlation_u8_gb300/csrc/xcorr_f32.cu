@@ -24,6 +24,11 @@
 //    block are added in a fixed order by a second pass.
 //  bcast (32+ rights per left) -- rights in lanes: every lane of a warp
 //    walks the same left row against its own rights, no cross-lane sums.
+//  tensor cores (xcorr_tc.cu; H, W <= 16, large batches) -- the n-to-m
+//    batch as a dense contraction on the tensor cores with split TF32
+//    operands; taken where it measured faster than the scalar kernels.
+//  warp per overlap (xcorr_warp.cu; single rows of 256+ samples) -- a
+//    warp sums one overlap and reduces inside the warp.
 //  tiny  (H*W <= 256, many pairs) -- a block of lefts x rights (32 x 16,
 //    16 x 32, 8 x 64 or 64 x 8, whichever pads the batch least) is staged
 //    interleaved (matrix index fastest); each lane owns 4 lefts x 4 rights
@@ -1081,7 +1086,39 @@ long long rows_grid_cap() {
 namespace {
 
 // Which kernel a shape takes, its arguments and the split-row scratch it needs.
-enum class XKind { Tiny, Bcast, Rows };
+enum class XKind { Tiny, Bcast, Rows, Tc, Warp };
+
+// CORR_XCORR_WARP (read on every call): "1" routes every shape to the
+// warp-per-overlap kernel, "0" none; otherwise the measured policy: single
+// rows (one-dimensional signals) of 256 or more samples, where it beat the
+// rows kernel on GB300 (1 x 4096: 19.6 against 26.4 us; 1 x 16384: 207
+// against 280 us; 1 x 256: 3.2 against 4.3 us), while from two rows up
+// the rows kernel won (2 x 2048: 13.7 against 20.7 us).
+bool use_warp(int nl, int nr, int H, int W) {
+  (void)nl;
+  (void)nr;
+  const char *v = getenv("CORR_XCORR_WARP");
+  if (v && v[0] == '0' && v[1] == '\0') return false;
+  if (v && v[0] == '1' && v[1] == '\0') return true;
+  return H == 1 && W >= 256;
+}
+
+// Whether a shape takes the tensor-core kernel (xcorr_tc.cu): the
+// environment variable CORR_XCORR_TC (read on every call) forces it off
+// ("0") or on wherever it applies ("1"); otherwise the measured policy:
+// matrices of 100+ elements (up to 16 x 16) and pairs * (H*W)^2 >= 2e7
+// products.  Measured on GB300 (CUDA-graph device time, tensor-core /
+// scalar kernel): 32 x 64 of 16^2 12.6 / 20.2 us, 128 x 128 of 16^2 52.8 /
+// 116 us, 32 x 64 of 10^2 8.9 / 9.7 us; below the rule the scalar kernel
+// won (16 x 16 of 16^2 12.5 / 12.1 us, 32 x 64 of 8^2 7.1 / 6.6 us).
+bool use_tc(int nl, int nr, int H, int W) {
+  if (!tc::supported(nl, nr, H, W)) return false;
+  const char *v = getenv("CORR_XCORR_TC");
+  if (v && v[0] == '0' && v[1] == '\0') return false;
+  if (v && v[0] == '1' && v[1] == '\0') return true;
+  const double hw = double(H) * W;
+  return hw >= 100 && double(nl) * nr * hw * hw >= 2e7;
+}
 
 struct XPlan {
   XKind kind;
@@ -1113,6 +1150,14 @@ XPlan make_plan(const float *left, int nl, const float *right, int nr, int H, in
 #ifndef CORR_XC_TINY
 #define CORR_XC_TINY 1
 #endif
+  if (use_warp(nl, nr, H, W)) {
+    pl.kind = XKind::Warp;
+    return pl;
+  }
+  if (use_tc(nl, nr, H, W)) {
+    pl.kind = XKind::Tc;
+    return pl;
+  }
   if (CORR_XC_TINY && H * W <= 256 && pairs >= 64) {
     pl.kind = XKind::Tiny;
     return pl;
@@ -1229,6 +1274,9 @@ XPlan make_plan(const float *left, int nl, const float *right, int nr, int H, in
 // pl.part_bytes long) when given, else from the library's pool.
 cudaError_t run_plan(XPlan &pl, float *fixed, cudaStream_t stream) {
   XArgs &a = pl.a;
+  if (pl.kind == XKind::Tc) return tc::launch(a.left, a.nl, a.right, a.nr, a.H, a.W, a.out, stream);
+  if (pl.kind == XKind::Warp)
+    return warp::launch(a.left, a.nl, a.right, a.nr, a.H, a.W, a.out, stream);
   if (pl.kind == XKind::Tiny)
     return launch_tiny(a.left, a.nl, a.right, a.nr, a.H, a.W, a.out, stream);
   if (pl.kind == XKind::Bcast) {

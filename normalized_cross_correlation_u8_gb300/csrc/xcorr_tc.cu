@@ -1,0 +1,496 @@
+// xcorr_tc.cu -- float32 full 2D cross-correlation of many small matrices
+// (n-to-m batches, H, W <= 16) on the sm_103a tensor cores.
+//
+// The artifact README's n-to-m case ("Efficient GPU-accelerated Parallel
+// Cross-correlation", kernel overview: multi-matrix-both, every left against
+// every right) reuses each matrix against many others.  Here that reuse is
+// written as a dense contraction.  With x' the column of the right matrix,
+//
+//   out[l][r][dy][dx] = sum_{y, x'} L_l[y][x' + dx] * R_r[y - dy][x'],
+//
+// (terms with an index outside a matrix are zero), so for one CTA tile
+//   D[m][n] = sum_k A[m][k] * B[n][k],
+//   m = (left l, shift dx)   A[m][(y, x')] = L_l[y][x' + dx]    (Toeplitz of L)
+//   n = (right r, shift dy)  B[n][(y, x')] = R_r[y - dy][x']    (rows of R)
+//   k = (overlap row y, right column x').
+//   n = (shift dy, right r), r fastest.
+// A CTA owns 4 lefts x 4 rights and every shift of those 16 pairs: M = 4
+// lefts x 32 shift slots dx, N = 32 shift slots dy x 4 rights, K = every
+// row y and column x'.  All CTAs therefore do the same work, and each
+// left's 4 x (2H-1)(2W-1) outputs -- contiguous in memory -- are written by
+// one CTA as one run in whole 32-byte sectors (a store that ends
+// mid-sector costs a DRAM fill, which dominated earlier layouts).
+//
+// Operand placement.  B is read from shared memory in the tensor cores'
+// no-swizzle K-major layout (8 rows x 16 bytes per core matrix, the two
+// core matrices of one 8-deep K step LBO bytes apart, 8-row groups SBO
+// bytes apart).  The CTA's rights are staged once as [x'/4][row slot][right]
+// [4 floats] with rows in reverse order, so the N rows of consecutive
+// shifts dy are consecutive slots: one descriptor per (y, K step), no
+// per-row copy.  A, the Toeplitz rows of L, is written per overlap row by
+// eight builder warps straight from registers into tensor memory
+// (tcgen05.st) and read from there by the MMA, rotating through kABufs
+// column ranges: the products are then bound by the tensor cores, not by
+// shared-memory bandwidth.
+//
+// Precision: the tensor cores multiply TF32 operands (10 mantissa bits).
+// Each operand is split v = hi + lo with hi = tf32(v) and lo = tf32(v - hi)
+// (both rounded to nearest), and a product is formed as
+// hi*hi + hi*lo + lo*hi, dropping lo*lo (the three-pass TF32 scheme of
+// NVIDIA's CUTLASS "3xTF32" GEMMs; split-operand tensor-core products as in
+// Markidis et al., "NVIDIA Tensor Core Programmability, Performance &
+// Precision", 2018).  Each product is then exact to about 3 * 2^-22 of
+// |l * r|, and the sums accumulate in FP32 in tensor memory: well inside
+// the 1e-5 * sum |l * r| bound of the scalar kernels.
+//
+// Issue: one warp issues the tcgen05.mma instructions (3 per K step of 8,
+// M = 128, N = 128, kind::tf32) into a 128-column FP32 accumulator in
+// tensor memory and commits each row's group to an mbarrier; after the
+// last row the builder warps read the accumulator back with tcgen05.ld
+// (lanes = the 32 shifts dx of one left), turn each pair's block around in
+// shared memory and write each left's run out row-major.  Every wait on an mbarrier is bounded:
+// after about a second the CTA gives up, records it in a device flag that
+// corr_device_status() reports, frees its tensor memory and returns.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "internal.cuh"
+
+namespace corr {
+namespace tc {
+namespace {
+
+constexpr int kThreads = 256;           // builder threads: 2 per A row (one K step each)
+constexpr int kABufs = 4;                // A stages in flight (overlap rows)
+constexpr int kLefts = 4;                 // lefts per tile (M = kLefts x kSlots)
+constexpr int kRights = 4;                // rights per tile (N = kSlots x kRights)
+constexpr int kSlots = 32;                // shifts dx (dy) per left (right): 2W-1 <= 31
+constexpr int kM = kLefts * kSlots;       // 128
+constexpr int kN = kRights * kSlots;      // 128
+constexpr int kPadL = 15;                 // zero columns left of a staged left row
+constexpr int kLRow = 64;                 // floats per staged left row
+constexpr int kSlotsR = 48;               // right row slots (2H + 30 <= 47 used)
+constexpr int kBBytes = 4 * kSlotsR * kRights * 16;   // staged B operand (hi or lo): 12 KB
+constexpr int kRunFloats = kRights * 31 * 31;   // one left's outputs in the epilogue
+constexpr uint32_t kTmemCols = 256;       // accumulator (128) + kABufs A stages (32 each)
+constexpr long long kWaitCycles = 1LL << 31;   // ~1 s at 2 GHz
+
+// Instruction descriptor of tcgen05.mma kind::tf32: D = F32 (bits 4-5 = 1),
+// A = B = TF32 (bits 7-9, 10-12 = 2), both K-major (bits 15, 16 = 0),
+// N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (2u << 7) | (2u << 10) |
+                            (uint32_t(kN >> 3) << 17) | (uint32_t(kM >> 4) << 24);
+
+struct TcArgs {
+  const float *left;
+  const float *right;
+  float *out;
+  int nl, nr, H, W;
+  int mtiles, rtiles;    // tiles of kLefts lefts x kRights rights
+  int vec4;              // rows readable as float4
+};
+
+__device__ int g_tc_status;   // bit 0: a bounded wait gave up
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Shared-memory matrix descriptor (tcgen05): start address, leading (K)
+// and stride (M / N) byte offsets, each >> 4 in 14 bits; descriptor version
+// 1 at bit 46; base offset 0, no swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return uint64_t((addr & 0x3FFFFu) >> 4) | (uint64_t((lbo & 0x3FFFFu) >> 4) << 16) |
+         (uint64_t((sbo & 0x3FFFFu) >> 4) << 32) | (uint64_t(1) << 46);
+}
+
+__device__ __forceinline__ uint32_t tf32_rna(float v) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v));
+  return r;
+}
+
+// v = hi + lo (+ a remainder below 2^-22 |v|), hi and lo TF32 bit patterns.
+__device__ __forceinline__ void split_tf32(float v, uint32_t &hi, uint32_t &lo) {
+  hi = tf32_rna(v);
+  lo = tf32_rna(v - __uint_as_float(hi));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for phase `parity` of the barrier to complete; false after about a
+// second without it.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - t0 > kWaitCycles) return false;
+  return true;
+}
+
+__device__ __forceinline__ void fence_before_sync() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after_sync() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "l"(a), "l"(b), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on the barrier once every tcgen05.mma this thread issued so far
+// has completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+// 32 consecutive FP32 columns of this warp's 32 accumulator lanes.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, "
+      "[%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
+        "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]),
+        "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+        "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
+        "=r"(v[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// 8 consecutive 32-bit columns of this warp's 32 accumulator lanes.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_tf32_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// KH: 8-deep K steps per overlap row (1 for W <= 8, else 2), a template
+// parameter so the row's 3 KH tensor-core instructions issue as one
+// straight-line sequence.
+//
+// Warp roles: warps 0-7 write the A operand of one overlap row at a time
+// into kABufs rotating tensor-memory stages (then, after the last row,
+// read the accumulator out); warp 8 issues the tensor-core instructions.
+// Stage b is handed over through two mbarriers: full[b] (one arrival per
+// builder warp once its part is in tensor memory) and empty[b] (a
+// tcgen05.commit: the products that read it have completed), so writing
+// rows i + 1 .. i + kABufs - 1 overlaps the products of row i.
+template <int KH>
+__global__ void __launch_bounds__(kThreads + 32, 1) xcorr_tc_kernel(const TcArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t *b_hi = smem;                                   // [4][kSlotsR][kRights][4] TF32 hi
+  uint8_t *b_lo = smem + kBBytes;                         // same, lo parts
+  float *lp = reinterpret_cast<float *>(smem + 2 * kBBytes);   // [kLefts][16][kLRow]
+  float *runs = lp + kLefts * 16 * kLRow;                 // [kLefts][kRunFloats]
+  uint64_t *full = reinterpret_cast<uint64_t *>(runs + kLefts * kRunFloats);
+  uint64_t *empty = full + kABufs;
+  uint64_t *done = empty + kABufs;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
+
+  const int H = a.H, W = a.W, t = threadIdx.x;
+  const int warp = t >> 5, lane = t & 31;
+  const bool issuer = warp == kThreads / 32;
+  const int rt = blockIdx.x % a.rtiles, mt = blockIdx.x / a.rtiles;
+  const int l0 = mt * kLefts, r0 = rt * kRights;
+
+  if (issuer) {
+    // tensor memory: accumulator at columns 0..127, A stages above it
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    if (lane == 0) {
+#pragma unroll
+      for (int k = 0; k < kABufs; ++k) {
+        mbar_init(smem_u32(&full[k]), kThreads / 32);
+        mbar_init(smem_u32(&empty[k]), 1);
+      }
+      mbar_init(smem_u32(done), 1);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+  } else {
+    // the tile's rights as TF32 hi / lo in the B layout: entry e = (xc,
+    // slot, rq) (rq fastest, so entries are consecutive 16-byte rows) holds
+    // R[r0 + rq][yr][4 xc .. 4 xc + 3] with yr = 2H - 2 - slot, zero
+    // outside the matrix
+    constexpr int kBEntries = 4 * kSlotsR * kRights;
+    constexpr int kBPer = (kBEntries + kThreads - 1) / kThreads;   // all loads in flight at once
+    float4 bv[kBPer];
+#pragma unroll
+    for (int k = 0; k < kBPer; ++k) {
+      const int e = t + k * kThreads;
+      const int rq = e & (kRights - 1), q = e >> 2;
+      const int slot = q % kSlotsR, xc = q / kSlotsR;
+      const int yr = 2 * H - 2 - slot;
+      bv[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (e < kBEntries && r0 + rq < a.nr && yr >= 0 && yr < H && 4 * xc < W) {
+        const float *src = a.right + (size_t(r0 + rq) * H + yr) * W + 4 * xc;
+        if (a.vec4) {
+          bv[k] = __ldg(reinterpret_cast<const float4 *>(src));
+        } else {
+          bv[k].x = __ldg(src);
+          if (4 * xc + 1 < W) bv[k].y = __ldg(src + 1);
+          if (4 * xc + 2 < W) bv[k].z = __ldg(src + 2);
+          if (4 * xc + 3 < W) bv[k].w = __ldg(src + 3);
+        }
+      }
+    }
+    // zero-padded copies of the tile's lefts (a thread per row quarter):
+    //   lp[lt][y][p] = L[l0+lt][y][p - kPadL]       (16 rows, H used)
+    {
+      const int lt = t >> 6, y = (t >> 2) & 15, q = t & 3;
+      float v[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const int x = 16 * q + k - kPadL;
+        v[k] = 0.f;
+        if (y < H && l0 + lt < a.nl && x >= 0 && x < W)
+          v[k] = __ldg(a.left + (size_t(l0 + lt) * H + y) * W + x);
+      }
+      float4 *dst = reinterpret_cast<float4 *>(lp + (lt * 16 + y) * kLRow + 16 * q);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        dst[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+    }
+#pragma unroll
+    for (int k = 0; k < kBPer; ++k) {
+      const int e = t + k * kThreads;
+      if (e >= kBEntries) break;
+      uint4 hi, lo;
+      split_tf32(bv[k].x, hi.x, lo.x);
+      split_tf32(bv[k].y, hi.y, lo.y);
+      split_tf32(bv[k].z, hi.z, lo.z);
+      split_tf32(bv[k].w, hi.w, lo.w);
+      *reinterpret_cast<uint4 *>(b_hi + e * 16) = hi;
+      *reinterpret_cast<uint4 *>(b_lo + e * 16) = lo;
+    }
+    // generic-proxy stores -> the tensor cores' (async proxy) reads
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t a_cols = tmem + uint32_t(kN);     // A stage b: columns + 32 b
+  int failed = 0;
+
+  if (issuer) {
+    if (lane == 0) {
+      const uint32_t bh_base = smem_u32(b_hi), bl_base = smem_u32(b_lo);
+      constexpr uint32_t kLboB = kSlotsR * kRights * 16;   // next 4 columns x'
+      uint32_t fpar = 0;      // bit k: parity of full[k]'s next completion
+      int bb = 0;
+      for (int i = 0; i < H; ++i) {
+        if (!mbar_wait_bounded(smem_u32(&full[bb]), (fpar >> bb) & 1u)) {
+          failed = 1;
+          break;
+        }
+        fpar ^= 1u << bb;
+        fence_after_sync();
+        // N row n = (dyi, rq): right row y - dy = y + (H-1) - dyi, slot
+        // H - 1 - y + dyi, so row n sits n * 16 bytes past slot H - 1 - y
+        const uint32_t s0off = uint32_t((H - 1 - i) * kRights * 16);
+        const uint32_t ab = a_cols + uint32_t(32 * bb);
+#pragma unroll
+        for (int h = 0; h < KH; ++h) {
+          const uint32_t boff = s0off + uint32_t(2 * h) * kLboB;
+          const uint64_t bhi = smem_desc(bh_base + boff, kLboB, 128);
+          const uint64_t blo = smem_desc(bl_base + boff, kLboB, 128);
+          mma_tf32_ta(tmem, ab + 8 * h, bhi, (i > 0 || h > 0) ? 1u : 0u);
+          mma_tf32_ta(tmem, ab + 8 * h, blo, 1u);
+          mma_tf32_ta(tmem, ab + 16 + 8 * h, bhi, 1u);
+        }
+        mma_commit(smem_u32(&empty[bb]));
+        bb = bb + 1 == kABufs ? 0 : bb + 1;
+      }
+      // every product issued so far, then the accumulator is final
+      mma_commit(smem_u32(done));
+      if (!mbar_wait_bounded(smem_u32(done), 0)) failed = 1;
+      // and every stage's last release has landed (no arrival on this
+      // CTA's shared memory is left pending when it exits)
+      for (int k = 0; k < kABufs && k < H; ++k) {
+        const int uses = (H - k + kABufs - 1) / kABufs;   // rows k, k + kABufs, ...
+        if (!mbar_wait_bounded(smem_u32(&empty[k]), uint32_t(uses - 1) & 1u)) failed = 1;
+      }
+    }
+  } else {
+    // this thread writes A row m = 32 (warp % 4) + lane (left m / 32, slot
+    // n = m % 32: dx = n - (W-1)), K step h = warp / 4: the 8 values
+    // L[l0+lt][y][x' + dx], x' = 8h .. 8h + 7, as TF32 hi and lo
+    const int lt = warp & 3, h = warp >> 2, n = lane;
+    const bool active = h < KH;
+    const float *lsrc = lp + lt * 16 * kLRow + n + kPadL - (W - 1) + 8 * h;
+    const uint32_t lane_base = uint32_t(32 * lt) << 16;
+    uint32_t epar = 0;        // bit k: parity of empty[k]'s next completion
+    int bb = 0;
+    for (int i = 0; i < H; ++i) {
+      // the products that read this stage kABufs rows ago have completed
+      if (i >= kABufs) {
+        if (!mbar_wait_bounded(smem_u32(&empty[bb]), (epar >> bb) & 1u)) {
+          failed = 1;
+          break;
+        }
+        epar ^= 1u << bb;
+        fence_after_sync();
+      }
+      if (active) {
+        const float *ls = lsrc + i * kLRow;
+        uint32_t hi[8], lo[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) split_tf32(ls[k], hi[k], lo[k]);
+        const uint32_t col = a_cols + uint32_t(32 * bb + 8 * h);
+        tmem_st8(lane_base + col, hi);
+        tmem_st8(lane_base + col + 16, lo);
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      }
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&full[bb]));
+      bb = bb + 1 == kABufs ? 0 : bb + 1;
+    }
+    if (!failed && !mbar_wait_bounded(smem_u32(done), 0)) failed = 1;
+  }
+  failed = __syncthreads_or(failed);
+  fence_after_sync();
+
+  if (!failed && !issuer) {
+    // epilogue: warp w reads lanes 32 (w % 4) .. + 31 (left l0 + w % 4,
+    // shift slots dx) and columns 64 (w / 4) .. + 63 (shift slots dy 16 (w
+    // / 4) .. + 15 of all 4 rights) into the left's output run, laid out
+    // as in memory: [right][dy][dx]
+    const int lt = warp & 3, half = warp >> 2;
+    const int ndy = 2 * H - 1, ndx = 2 * W - 1, per_pair = ndy * ndx;
+    float *lrun = runs + lt * kRunFloats;
+    const uint32_t lane_base = tmem + (uint32_t(32 * lt) << 16);
+#pragma unroll 1
+    for (int j = 0; j < 2; ++j) {
+      const int c0 = 64 * half + 32 * j;
+      uint32_t v[32];
+      tmem_ld32(lane_base + uint32_t(c0), v);
+      if (lane < ndx) {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const int c = c0 + k, dyi = c >> 2;          // c = dyi * 4 + rq
+          if (dyi < ndy) lrun[(c & 3) * per_pair + dyi * ndx + lane] = __uint_as_float(v[k]);
+        }
+      }
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");   // builder warps only
+    // left l0 + lt: its pairs with rights r0 .. r0 + nrr - 1 are one
+    // contiguous run; warps w and w + 4 store alternate 32-float chunks of
+    // it at 128-byte-aligned addresses (whole sectors but at the run's ends)
+    const int l = l0 + lt;
+    const int nrr = a.nr - r0 < kRights ? a.nr - r0 : kRights;
+    if (l < a.nl) {
+      float *run = a.out + (size_t(l) * a.nr + r0) * per_pair;
+      const int len = nrr * per_pair;
+      const int off = int((reinterpret_cast<uintptr_t>(run) >> 2) & 31);   // floats past 128 B
+#pragma unroll 4
+      for (int f = 32 * half + lane - off; f < len; f += 64)
+        if (f >= 0) run[f] = lrun[f];
+    }
+  } else if (failed && t == 0) {
+    atomicOr(&g_tc_status, 1);
+  }
+  fence_before_sync();
+  __syncthreads();
+  if (issuer) {
+    fence_after_sync();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+}  // namespace
+
+bool supported(int nl, int nr, int H, int W) {
+  (void)nl;
+  (void)nr;
+  return H >= 1 && H <= 16 && W >= 1 && W <= 16;
+}
+
+cudaError_t launch(const float *left, int nl, const float *right, int nr, int H, int W,
+                   float *out, cudaStream_t stream) {
+  if (!supported(nl, nr, H, W)) return cudaErrorInvalidValue;
+  TcArgs a;
+  a.left = left;
+  a.right = right;
+  a.out = out;
+  a.nl = nl;
+  a.nr = nr;
+  a.H = H;
+  a.W = W;
+  a.mtiles = (nl + kLefts - 1) / kLefts;
+  a.rtiles = (nr + kRights - 1) / kRights;
+  a.vec4 = (W % 4 == 0 && (reinterpret_cast<uintptr_t>(right) & 15) == 0) ? 1 : 0;
+  const long long blocks = (long long)a.mtiles * a.rtiles;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const size_t smem = 2 * size_t(kBBytes) + size_t(kLefts) * 16 * kLRow * sizeof(float) +
+                      size_t(kLefts) * kRunFloats * sizeof(float) +
+                      (2 * kABufs + 2) * 8;
+  auto kern = W > 8 ? xcorr_tc_kernel<2> : xcorr_tc_kernel<1>;
+  cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void *>(kern));
+  if (e != cudaSuccess) return e;
+  kern<<<unsigned(blocks), kThreads + 32, smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+// Reads and clears the device flag of bounded waits that gave up.
+cudaError_t take_status(int *gave_up) {
+  int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_tc_status, sizeof(int));
+  if (e != cudaSuccess) return e;
+  *gave_up = v;
+  if (v) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_tc_status, &zero, sizeof(int));
+  }
+  return e;
+}
+
+}  // namespace tc
+}  // namespace corr

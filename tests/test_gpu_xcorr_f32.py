@@ -169,3 +169,13 @@ def test_rows_kernels_item_loop(nl, nr, H, W, monkeypatch):
     CORR_XCORR_MAX_GRID, so each CTA loops over several items."""
     monkeypatch.setenv("CORR_XCORR_MAX_GRID", "37")
     check(rand(nl, H, W), rand(nr, H, W, "normal"))
+
+
+@pytest.mark.parametrize("nl,nr,H,W", [(1, 1, 1, 1), (1, 1, 1, 4096), (2, 3, 2, 700),
+                                       (1, 2, 5, 33), (3, 2, 7, 31), (1, 1, 40, 64),
+                                       (2, 2, 16, 16)])
+def test_warp_per_overlap_kernel(nl, nr, H, W, monkeypatch):
+    """The warp-per-overlap kernel (CORR_XCORR_WARP=1 routes every shape to
+    it): overlaps wider and narrower than a warp, single rows and columns."""
+    monkeypatch.setenv("CORR_XCORR_WARP", "1")
+    check(rand(nl, H, W), rand(nr, H, W, "normal"))
