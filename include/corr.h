@@ -153,6 +153,22 @@ int corr_xcorr_f32(const float *left, int nl, const float *right, int nr,
                    int H, int W, float *out);
 
 /*
+ * corr_xcorr_f32_kernel -- which of the library's kernels corr_xcorr_f32
+ * runs for a batch of this shape on the current device (*kind gets one of
+ * the values below); CORR_EINVAL for non-positive sizes or a NULL kind.
+ * Launches nothing.  The choice also follows the environment variables
+ * CORR_XCORR_TC and CORR_XCORR_WARP ("1" / "0": take / never take that
+ * kernel where it applies), read on every call.
+ */
+#define CORR_XCORR_KERNEL_ROWS 0      /* rows kernel, whole rows staged */
+#define CORR_XCORR_KERNEL_ROWS_WIN 1  /* rows kernel, column windows */
+#define CORR_XCORR_KERNEL_BCAST 2     /* rights in lanes (one-to-many) */
+#define CORR_XCORR_KERNEL_TINY 3      /* small matrices, FP32 FMA */
+#define CORR_XCORR_KERNEL_TENSOR 4    /* small matrices, tensor cores (split TF32) */
+#define CORR_XCORR_KERNEL_WARP 5      /* one warp per overlap */
+int corr_xcorr_f32_kernel(int nl, int nr, int H, int W, int *kind);
+
+/*
  * corr_xcorr_f32_noalloc -- corr_xcorr_f32 for callers that cannot allocate.
  *
  * No counterpart on the pages: this is a deployment variant of

@@ -14,8 +14,8 @@ The library is loaded (and built if needed) on first use, not at import.
 """
 from ._binding import (CorrError, device_status, load, ncc_get_method, ncc_set_method,  # noqa: F401
                        ncc_u8, ncc_u8_into, peak_dp4a, peak_ffma, scratch_reserved, xcorr_f32,
-                       xcorr_f32_into, xcorr_f32_noalloc_into)
+                       xcorr_f32_into, xcorr_f32_kernel, xcorr_f32_noalloc_into)
 
 __all__ = ["CorrError", "device_status", "load", "ncc_u8", "ncc_u8_into", "ncc_set_method", "ncc_get_method", "xcorr_f32",
-           "xcorr_f32_into", "xcorr_f32_noalloc_into", "scratch_reserved", "peak_dp4a",
+           "xcorr_f32_into", "xcorr_f32_kernel", "xcorr_f32_noalloc_into", "scratch_reserved", "peak_dp4a",
            "peak_ffma"]

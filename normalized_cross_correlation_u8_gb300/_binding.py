@@ -28,7 +28,7 @@ NCC_METHOD_DP4A = 0
 NCC_METHOD_BOX = 1
 _NCC_METHODS = {"dp4a": NCC_METHOD_DP4A, "box": NCC_METHOD_BOX}
 
-EXPORTS = ["corr_ncc_u8", "corr_ncc_u8_pitched", "corr_ncc_set_method", "corr_ncc_get_method", "corr_xcorr_f32", "corr_xcorr_f32_noalloc", "corr_device_status", "corr_scratch_reserved", "corr_set_stream",
+EXPORTS = ["corr_ncc_u8", "corr_ncc_u8_pitched", "corr_ncc_set_method", "corr_ncc_get_method", "corr_xcorr_f32", "corr_xcorr_f32_noalloc", "corr_xcorr_f32_kernel", "corr_device_status", "corr_scratch_reserved", "corr_set_stream",
            "corr_get_stream", "corr_strerror", "corr_last_cuda_error",
            "corr_version", "corr_peak_dp4a", "corr_peak_ffma"]
 
@@ -76,6 +76,8 @@ def load(build_if_missing=True):
         lib.corr_xcorr_f32_noalloc.argtypes = [vp, c_int, vp, c_int, c_int, c_int, vp]
         lib.corr_scratch_reserved.argtypes = [ctypes.POINTER(ctypes.c_size_t)]
         lib.corr_device_status.argtypes = []
+        lib.corr_xcorr_f32_kernel.argtypes = [c_int, c_int, c_int, c_int,
+                                              ctypes.POINTER(c_int)]
         lib.corr_set_stream.argtypes = [vp]
         lib.corr_get_stream.argtypes = []
         lib.corr_get_stream.restype = vp
@@ -87,7 +89,7 @@ def load(build_if_missing=True):
         lib.corr_peak_ffma.argtypes = [c_dbl_p, c_dbl_p]
         for f in (lib.corr_ncc_u8, lib.corr_ncc_u8_pitched, lib.corr_ncc_set_method,
                   lib.corr_ncc_get_method,
-                  lib.corr_xcorr_f32, lib.corr_xcorr_f32_noalloc, lib.corr_scratch_reserved, lib.corr_device_status,
+                  lib.corr_xcorr_f32, lib.corr_xcorr_f32_noalloc, lib.corr_scratch_reserved, lib.corr_device_status, lib.corr_xcorr_f32_kernel,
                   lib.corr_set_stream,
                   lib.corr_last_cuda_error, lib.corr_version,
                   lib.corr_peak_dp4a, lib.corr_peak_ffma):
@@ -305,6 +307,17 @@ def xcorr_f32(left, right, device=None):
                       device=left.device)
     xcorr_f32_into(left, right, out)
     return out.cpu() if host else out
+
+
+XCORR_KERNELS = {0: "rows", 1: "rows_win", 2: "bcast", 3: "tiny", 4: "tensor", 5: "warp"}
+
+
+def xcorr_f32_kernel(nl, nr, H, W):
+    """Name of the kernel corr_xcorr_f32 runs for nl x nr pairs of H x W
+    matrices ("rows", "rows_win", "bcast", "tiny", "tensor" or "warp")."""
+    kind = ctypes.c_int()
+    _check(load().corr_xcorr_f32_kernel(nl, nr, H, W, ctypes.byref(kind)))
+    return XCORR_KERNELS[kind.value]
 
 
 def device_status():

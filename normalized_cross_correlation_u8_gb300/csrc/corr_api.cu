@@ -151,6 +151,15 @@ int corr_xcorr_f32_noalloc(const float *left, int nl, const float *right, int nr
       corr::xcorr_f32_noalloc_launch(left, nl, right, nr, H, W, out, tls_stream));
 }
 
+int corr_xcorr_f32_kernel(int nl, int nr, int H, int W, int *kind) {
+  if (!kind || nl <= 0 || nr <= 0 || H <= 0 || W <= 0) return CORR_EINVAL;
+  if (int64_t(nl) * nr > 0x7fffffffLL) return CORR_EUNSUPPORTED;
+  if (int64_t(2) * H - 1 > 0x7fffffffLL || int64_t(2) * W - 1 > 0x7fffffffLL)
+    return CORR_EUNSUPPORTED;
+  *kind = corr::xcorr_f32_kernel_kind(nl, nr, H, W);
+  return CORR_OK;
+}
+
 int corr_device_status(void) {
   cudaError_t e = cudaStreamSynchronize(tls_stream);
   if (e != cudaSuccess) return cuda_status(e);

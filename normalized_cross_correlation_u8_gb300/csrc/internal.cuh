@@ -41,6 +41,10 @@ cudaError_t xcorr_f32_launch(const float *left, int nl, const float *right,
                              int nr, int H, int W, float *out,
                              cudaStream_t stream);
 
+// Which kernel corr_xcorr_f32 runs for this shape (corr.h:
+// CORR_XCORR_KERNEL_*).
+int xcorr_f32_kernel_kind(int nl, int nr, int H, int W);
+
 // Bytes of split-row scratch corr_xcorr_f32 would take for this shape (0
 // when the chosen kernel needs none).
 size_t xcorr_f32_scratch_bytes(const float *left, int nl, const float *right, int nr,

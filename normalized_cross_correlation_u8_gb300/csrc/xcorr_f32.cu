@@ -1325,6 +1325,18 @@ cudaError_t xcorr_f32_launch(const float *left, int nl, const float *right,
   return run_plan(pl, nullptr, stream);
 }
 
+int xcorr_f32_kernel_kind(int nl, int nr, int H, int W) {
+  const XPlan pl = make_plan(nullptr, nl, nullptr, nr, H, W, nullptr);
+  switch (pl.kind) {
+    case XKind::Rows: return pl.chunk ? 0 : 1;
+    case XKind::Bcast: return 2;
+    case XKind::Tiny: return 3;
+    case XKind::Tc: return 4;
+    case XKind::Warp: return 5;
+  }
+  return -1;
+}
+
 size_t xcorr_f32_scratch_bytes(const float *left, int nl, const float *right, int nr,
                                int H, int W) {
   return make_plan(left, nl, right, nr, H, W, nullptr).part_bytes;

@@ -112,3 +112,28 @@ def test_no_gpu_means_loud_failure():
         pytest.skip("a GPU is present")
     with pytest.raises(RuntimeError):
         corr.ncc_u8(torch.zeros(8, 8, dtype=torch.uint8), torch.zeros(4, 4, dtype=torch.uint8))
+
+
+def test_xcorr_kernel_choice(monkeypatch):
+    """Host-side dispatch (no launch, no GPU needed): the named batches take
+    the kernels measured fastest for them, and the environment switches
+    force or forbid the tensor-core and warp-per-overlap kernels."""
+    monkeypatch.delenv("CORR_XCORR_TC", raising=False)
+    monkeypatch.delenv("CORR_XCORR_WARP", raising=False)
+    k = corr.xcorr_f32_kernel
+    assert k(32, 64, 16, 16) == "tensor"       # n-to-m of 16x16
+    assert k(1, 1, 256, 256) == "rows"         # one-to-one
+    assert k(1, 128, 64, 64) == "bcast"        # one-to-many
+    assert k(1, 1, 1024, 1024) == "rows_win"   # rows too wide to stage whole
+    assert k(1, 1, 1, 4096) == "warp"          # a single long row
+    assert k(16, 16, 16, 16) == "tiny"         # small batch, below the tensor rule
+    assert k(32, 64, 8, 8) == "tiny"           # H*W < 100
+    monkeypatch.setenv("CORR_XCORR_TC", "0")
+    assert k(32, 64, 16, 16) == "tiny"
+    monkeypatch.setenv("CORR_XCORR_TC", "1")
+    assert k(2, 2, 3, 5) == "tensor"
+    assert k(1, 1, 17, 16) != "tensor"         # beyond 16 x 16
+    monkeypatch.setenv("CORR_XCORR_WARP", "1")
+    assert k(1, 1, 40, 64) == "warp"
+    with pytest.raises(corr.CorrError):
+        k(0, 1, 4, 4)
