@@ -157,8 +157,8 @@ int corr_xcorr_f32(const float *left, int nl, const float *right, int nr,
  * runs for a batch of this shape on the current device (*kind gets one of
  * the values below); CORR_EINVAL for non-positive sizes or a NULL kind.
  * Launches nothing.  The choice also follows the environment variables
- * CORR_XCORR_TC and CORR_XCORR_WARP ("1" / "0": take / never take that
- * kernel where it applies), read on every call.
+ * CORR_XCORR_TC, CORR_XCORR_TCL and CORR_XCORR_WARP ("1" / "0": take /
+ * never take that kernel where it applies), read on every call.
  */
 #define CORR_XCORR_KERNEL_ROWS 0      /* rows kernel, whole rows staged */
 #define CORR_XCORR_KERNEL_ROWS_WIN 1  /* rows kernel, column windows */
@@ -166,13 +166,19 @@ int corr_xcorr_f32(const float *left, int nl, const float *right, int nr,
 #define CORR_XCORR_KERNEL_TINY 3      /* small matrices, FP32 FMA */
 #define CORR_XCORR_KERNEL_TENSOR 4    /* small matrices, tensor cores (split TF32) */
 #define CORR_XCORR_KERNEL_WARP 5      /* one warp per overlap */
+#define CORR_XCORR_KERNEL_TENSOR_LARGE 6   /* larger matrices, tensor cores (split TF32) */
 int corr_xcorr_f32_kernel(int nl, int nr, int H, int W, int *kind);
 
 /*
  * corr_xcorr_f32_noalloc -- corr_xcorr_f32 for callers that cannot allocate.
  *
  * No counterpart on the pages: this is a deployment variant of
- * corr_xcorr_f32 with the same arguments, layouts, results and error codes.
+ * corr_xcorr_f32 with the same arguments, layouts and error codes.  It runs
+ * the kernel corr_xcorr_f32 would run whenever that kernel's scratch fits
+ * the array below, with bit-identical results; otherwise (large one-to-one
+ * or one-to-many batches, whose tensor-core kernel keeps partial sums of
+ * tens of megabytes) it runs the scalar kernel that fits, whose results
+ * meet the same per-element bound but may differ in the last bits.
  * corr_xcorr_f32 takes temporary device memory for the partial sums of large
  * matrices from a stream-ordered pool that may call the driver's allocator.
  * Some callers cannot allow that -- an application that reserves all device

@@ -309,7 +309,8 @@ def xcorr_f32(left, right, device=None):
     return out.cpu() if host else out
 
 
-XCORR_KERNELS = {0: "rows", 1: "rows_win", 2: "bcast", 3: "tiny", 4: "tensor", 5: "warp"}
+XCORR_KERNELS = {0: "rows", 1: "rows_win", 2: "bcast", 3: "tiny", 4: "tensor", 5: "warp",
+                 6: "tensor_large"}
 
 
 def xcorr_f32_kernel(nl, nr, H, W):

@@ -22,7 +22,7 @@ LIB = os.path.join(OUT, "libcorr.so")
 INCLUDE = os.path.join(ROOT, "include")
 
 SOURCES = ["corr_api.cu", "ncc_u8.cu", "ncc_u8_wide.cu", "ncc_u8_box.cu", "ncc_u8_box_wide.cu",
-           "xcorr_f32.cu", "xcorr_tc.cu", "xcorr_warp.cu", "xcorr_noalloc.cu", "scratch.cu", "device.cu", "peaks.cu"]
+           "xcorr_f32.cu", "xcorr_tc.cu", "xcorr_tcl.cu", "xcorr_warp.cu", "xcorr_noalloc.cu", "scratch.cu", "device.cu", "peaks.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
               "--expt-relaxed-constexpr", "-I", INCLUDE]

@@ -142,7 +142,8 @@ int corr_xcorr_f32_noalloc(const float *left, int nl, const float *right, int nr
   if (int64_t(nl) * nr > 0x7fffffffLL) return CORR_EUNSUPPORTED;
   if (int64_t(2) * H - 1 > 0x7fffffffLL || int64_t(2) * W - 1 > 0x7fffffffLL)
     return CORR_EUNSUPPORTED;
-  if (corr::xcorr_f32_scratch_bytes(left, nl, right, nr, H, W) >
+  if (corr::xcorr_f32_scratch_bytes(left, nl, right, nr, H, W,
+                                    CORR_XCORR_NOALLOC_SCRATCH_BYTES) >
       CORR_XCORR_NOALLOC_SCRATCH_BYTES)
     return CORR_EUNSUPPORTED;
   int rc;
@@ -163,9 +164,10 @@ int corr_xcorr_f32_kernel(int nl, int nr, int H, int W, int *kind) {
 int corr_device_status(void) {
   cudaError_t e = cudaStreamSynchronize(tls_stream);
   if (e != cudaSuccess) return cuda_status(e);
-  int gave_up = 0;
+  int gave_up = 0, gave_up_l = 0;
   if ((e = corr::tc::take_status(&gave_up)) != cudaSuccess) return cuda_status(e);
-  return gave_up ? CORR_ETIMEOUT : CORR_OK;
+  if ((e = corr::tcl::take_status(&gave_up_l)) != cudaSuccess) return cuda_status(e);
+  return gave_up || gave_up_l ? CORR_ETIMEOUT : CORR_OK;
 }
 
 int corr_scratch_reserved(size_t *bytes) {

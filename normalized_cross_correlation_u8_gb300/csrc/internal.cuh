@@ -48,7 +48,7 @@ int xcorr_f32_kernel_kind(int nl, int nr, int H, int W);
 // Bytes of split-row scratch corr_xcorr_f32 would take for this shape (0
 // when the chosen kernel needs none).
 size_t xcorr_f32_scratch_bytes(const float *left, int nl, const float *right, int nr,
-                               int H, int W);
+                               int H, int W, size_t max_scratch = ~size_t(0));
 
 // As xcorr_f32_launch, but split-row partial sums go to `scratch` (at least
 // xcorr_f32_scratch_bytes long; cudaErrorInvalidValue otherwise) instead of
@@ -73,6 +73,15 @@ cudaError_t launch(const float *left, int nl, const float *right, int nr, int H,
 // Reads and clears the flag the kernel sets when a bounded wait gave up.
 cudaError_t take_status(int *gave_up);
 }  // namespace tc
+
+// Tensor-core form for larger matrices (xcorr_tcl.cu): partial sums of
+// K units in `scratch` (scratch_bytes long), added by a second kernel.
+namespace tcl {
+size_t scratch_bytes(int nl, int nr, int H, int W);
+cudaError_t launch(const float *left, int nl, const float *right, int nr, int H, int W,
+                   float *out, float *scratch, cudaStream_t stream);
+cudaError_t take_status(int *gave_up);
+}  // namespace tcl
 
 // One warp per overlap with an in-warp reduction (xcorr_warp.cu).
 namespace warp {

@@ -27,6 +27,9 @@
 //  tensor cores (xcorr_tc.cu; H, W <= 16, large batches) -- the n-to-m
 //    batch as a dense contraction on the tensor cores with split TF32
 //    operands; taken where it measured faster than the scalar kernels.
+//  tensor cores, larger matrices (xcorr_tcl.cu; large one-to-one and
+//    one-to-many batches) -- the same contraction per left, K cut into
+//    units whose partial sums a second kernel adds in a fixed order.
 //  warp per overlap (xcorr_warp.cu; single rows of 256+ samples) -- a
 //    warp sums one overlap and reduces inside the warp.
 //  tiny  (H*W <= 256, many pairs) -- a block of lefts x rights (32 x 16,
@@ -1086,7 +1089,28 @@ long long rows_grid_cap() {
 namespace {
 
 // Which kernel a shape takes, its arguments and the split-row scratch it needs.
-enum class XKind { Tiny, Bcast, Rows, Tc, Warp };
+enum class XKind { Tiny, Bcast, Rows, Tc, Warp, Tcl };
+
+// Largest partial-sum scratch the larger-matrix tensor-core kernel may take.
+constexpr size_t kMaxTclScratch = size_t(512) << 20;
+
+// Whether a shape takes the larger-matrix tensor-core kernel (xcorr_tcl.cu):
+// CORR_XCORR_TCL (read on every call) "1" / "0" forces it on / off where it
+// applies; otherwise the measured policy: pairs * (H*W)^2 >= 5e8 products
+// (its partial-sum pass and 32 x 32 units cost about 30 us on any shape).
+// It never takes more than max_scratch (nor 512 MB) of scratch.  Measured on
+// GB300 (CUDA-graph device time, this kernel / the scalar one): 1 x 1 of
+// 256^2 85 / 213 us, 1 x 128 of 64^2 87 / 131 us, 2 x 96 of 48^2 74 / 102
+// us; below the rule 1 x 1 of 128^2 31 / 31 us, 1 x 128 of 32^2 35 / 20 us.
+bool use_tcl(int nl, int nr, int H, int W, size_t max_scratch) {
+  const size_t need = tcl::scratch_bytes(nl, nr, H, W);
+  if (need > kMaxTclScratch || need > max_scratch) return false;
+  const char *v = getenv("CORR_XCORR_TCL");
+  if (v && v[0] == '0' && v[1] == '\0') return false;
+  if (v && v[0] == '1' && v[1] == '\0') return true;
+  const double hw = double(H) * W;
+  return double(nl) * nr * hw * hw >= 5e8;
+}
 
 // CORR_XCORR_WARP (read on every call): "1" routes every shape to the
 // warp-per-overlap kernel, "0" none; otherwise the measured policy: single
@@ -1131,7 +1155,7 @@ struct XPlan {
 };
 
 XPlan make_plan(const float *left, int nl, const float *right, int nr, int H, int W,
-                float *out) {
+                float *out, size_t max_scratch = ~size_t(0)) {
   XPlan pl;
   pl.smem = 0;
   pl.blocks = 0;
@@ -1156,6 +1180,11 @@ XPlan make_plan(const float *left, int nl, const float *right, int nr, int H, in
   }
   if (use_tc(nl, nr, H, W)) {
     pl.kind = XKind::Tc;
+    return pl;
+  }
+  if (use_tcl(nl, nr, H, W, max_scratch)) {
+    pl.kind = XKind::Tcl;
+    pl.part_bytes = tcl::scratch_bytes(nl, nr, H, W);
     return pl;
   }
   if (CORR_XC_TINY && H * W <= 256 && pairs >= 64) {
@@ -1275,6 +1304,19 @@ XPlan make_plan(const float *left, int nl, const float *right, int nr, int H, in
 cudaError_t run_plan(XPlan &pl, float *fixed, cudaStream_t stream) {
   XArgs &a = pl.a;
   if (pl.kind == XKind::Tc) return tc::launch(a.left, a.nl, a.right, a.nr, a.H, a.W, a.out, stream);
+  if (pl.kind == XKind::Tcl) {
+    float *part = fixed;
+    cudaError_t e = cudaSuccess;
+    if (!part && (e = scratch_alloc(reinterpret_cast<void **>(&part), pl.part_bytes, stream)) !=
+                     cudaSuccess)
+      return e;
+    e = tcl::launch(a.left, a.nl, a.right, a.nr, a.H, a.W, a.out, part, stream);
+    if (!fixed) {
+      const cudaError_t f = cudaFreeAsync(part, stream);
+      if (e == cudaSuccess) e = f;
+    }
+    return e;
+  }
   if (pl.kind == XKind::Warp)
     return warp::launch(a.left, a.nl, a.right, a.nr, a.H, a.W, a.out, stream);
   if (pl.kind == XKind::Tiny)
@@ -1332,20 +1374,21 @@ int xcorr_f32_kernel_kind(int nl, int nr, int H, int W) {
     case XKind::Bcast: return 2;
     case XKind::Tiny: return 3;
     case XKind::Tc: return 4;
+    case XKind::Tcl: return 6;
     case XKind::Warp: return 5;
   }
   return -1;
 }
 
 size_t xcorr_f32_scratch_bytes(const float *left, int nl, const float *right, int nr,
-                               int H, int W) {
-  return make_plan(left, nl, right, nr, H, W, nullptr).part_bytes;
+                               int H, int W, size_t max_scratch) {
+  return make_plan(left, nl, right, nr, H, W, nullptr, max_scratch).part_bytes;
 }
 
 cudaError_t xcorr_f32_launch_scratch(const float *left, int nl, const float *right,
                                      int nr, int H, int W, float *out, float *scratch,
                                      size_t scratch_bytes, cudaStream_t stream) {
-  XPlan pl = make_plan(left, nl, right, nr, H, W, out);
+  XPlan pl = make_plan(left, nl, right, nr, H, W, out, scratch_bytes);
   if (pl.part_bytes > scratch_bytes || (pl.part_bytes > 0 && scratch == nullptr))
     return cudaErrorInvalidValue;
   return run_plan(pl, scratch, stream);

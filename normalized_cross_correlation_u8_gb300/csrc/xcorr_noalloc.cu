@@ -61,7 +61,8 @@ cudaError_t scratch_address(float **out) {
 cudaError_t xcorr_f32_noalloc_launch(const float *left, int nl, const float *right,
                                      int nr, int H, int W, float *out,
                                      cudaStream_t stream) {
-  const size_t need = xcorr_f32_scratch_bytes(left, nl, right, nr, H, W);
+  const size_t need =
+      xcorr_f32_scratch_bytes(left, nl, right, nr, H, W, CORR_XCORR_NOALLOC_SCRATCH_BYTES);
   if (need > CORR_XCORR_NOALLOC_SCRATCH_BYTES) return cudaErrorInvalidValue;
   float *scratch = nullptr;
   if (need > 0) {

@@ -11,9 +11,8 @@
 // (terms with an index outside a matrix are zero), so for one CTA tile
 //   D[m][n] = sum_k A[m][k] * B[n][k],
 //   m = (left l, shift dx)   A[m][(y, x')] = L_l[y][x' + dx]    (Toeplitz of L)
-//   n = (right r, shift dy)  B[n][(y, x')] = R_r[y - dy][x']    (rows of R)
+//   n = (shift dy, right r)  B[n][(y, x')] = R_r[y - dy][x']    (rows of R; r fastest)
 //   k = (overlap row y, right column x').
-//   n = (shift dy, right r), r fastest.
 // A CTA owns 4 lefts x 4 rights and every shift of those 16 pairs: M = 4
 // lefts x 32 shift slots dx, N = 32 shift slots dy x 4 rights, K = every
 // row y and column x'.  All CTAs therefore do the same work, and each
@@ -48,17 +47,21 @@
 // tensor memory and commits each row's group to an mbarrier; after the
 // last row the builder warps read the accumulator back with tcgen05.ld
 // (lanes = the 32 shifts dx of one left), turn each pair's block around in
-// shared memory and write each left's run out row-major.  Every wait on an mbarrier is bounded:
-// after about a second the CTA gives up, records it in a device flag that
-// corr_device_status() reports, frees its tensor memory and returns.
+// shared memory and write each left's run out row-major.  Every wait on an
+// mbarrier is bounded: after about a second the CTA gives up, records it in
+// a device flag that corr_device_status() reports, frees its tensor memory
+// and returns.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "internal.cuh"
+#include "tc_common.cuh"
 
 namespace corr {
 namespace tc {
 namespace {
+
+using namespace tcx;
 
 constexpr int kThreads = 256;           // builder threads: 2 per A row (one K step each)
 constexpr int kABufs = 4;                // A stages in flight (overlap rows)
@@ -73,13 +76,7 @@ constexpr int kSlotsR = 48;               // right row slots (2H + 30 <= 47 used
 constexpr int kBBytes = 4 * kSlotsR * kRights * 16;   // staged B operand (hi or lo): 12 KB
 constexpr int kRunFloats = kRights * 31 * 31;   // one left's outputs in the epilogue
 constexpr uint32_t kTmemCols = 256;       // accumulator (128) + kABufs A stages (32 each)
-constexpr long long kWaitCycles = 1LL << 31;   // ~1 s at 2 GHz
-
-// Instruction descriptor of tcgen05.mma kind::tf32: D = F32 (bits 4-5 = 1),
-// A = B = TF32 (bits 7-9, 10-12 = 2), both K-major (bits 15, 16 = 0),
-// N >> 3 at bits 17-22, M >> 4 at bits 24-28.
-constexpr uint32_t kIdesc = (1u << 4) | (2u << 7) | (2u << 10) |
-                            (uint32_t(kN >> 3) << 17) | (uint32_t(kM >> 4) << 24);
+constexpr uint32_t kIdesc = tcx::idesc_tf32(kM, kN);
 
 struct TcArgs {
   const float *left;
@@ -91,120 +88,6 @@ struct TcArgs {
 };
 
 __device__ int g_tc_status;   // bit 0: a bounded wait gave up
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-// Shared-memory matrix descriptor (tcgen05): start address, leading (K)
-// and stride (M / N) byte offsets, each >> 4 in 14 bits; descriptor version
-// 1 at bit 46; base offset 0, no swizzle.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-  return uint64_t((addr & 0x3FFFFu) >> 4) | (uint64_t((lbo & 0x3FFFFu) >> 4) << 16) |
-         (uint64_t((sbo & 0x3FFFFu) >> 4) << 32) | (uint64_t(1) << 46);
-}
-
-__device__ __forceinline__ uint32_t tf32_rna(float v) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v));
-  return r;
-}
-
-// v = hi + lo (+ a remainder below 2^-22 |v|), hi and lo TF32 bit patterns.
-__device__ __forceinline__ void split_tf32(float v, uint32_t &hi, uint32_t &lo) {
-  hi = tf32_rna(v);
-  lo = tf32_rna(v - __uint_as_float(hi));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Wait for phase `parity` of the barrier to complete; false after about a
-// second without it.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity))
-    if (clock64() - t0 > kWaitCycles) return false;
-  return true;
-}
-
-__device__ __forceinline__ void fence_before_sync() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void fence_after_sync() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b,
-                                         uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}"
-      ::"r"(d_tmem), "l"(a), "l"(b), "r"(kIdesc), "r"(accumulate)
-      : "memory");
-}
-
-// Arrive on the barrier once every tcgen05.mma this thread issued so far
-// has completed.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-
-// 32 consecutive FP32 columns of this warp's 32 accumulator lanes.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, "
-      "[%32];"
-      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
-        "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]),
-        "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
-        "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
-        "=r"(v[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// 8 consecutive 32-bit columns of this warp's 32 accumulator lanes.
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
-      : "memory");
-}
-
-__device__ __forceinline__ void mma_tf32_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
-                                            uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}"
-      ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(kIdesc), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
 
 // KH: 8-deep K steps per overlap row (1 for W <= 8, else 2), a template
 // parameter so the row's 3 KH tensor-core instructions issue as one
@@ -339,9 +222,9 @@ __global__ void __launch_bounds__(kThreads + 32, 1) xcorr_tc_kernel(const TcArgs
           const uint32_t boff = s0off + uint32_t(2 * h) * kLboB;
           const uint64_t bhi = smem_desc(bh_base + boff, kLboB, 128);
           const uint64_t blo = smem_desc(bl_base + boff, kLboB, 128);
-          mma_tf32_ta(tmem, ab + 8 * h, bhi, (i > 0 || h > 0) ? 1u : 0u);
-          mma_tf32_ta(tmem, ab + 8 * h, blo, 1u);
-          mma_tf32_ta(tmem, ab + 16 + 8 * h, bhi, 1u);
+          mma_tf32_ta(tmem, ab + 8 * h, bhi, (i > 0 || h > 0) ? 1u : 0u, kIdesc);
+          mma_tf32_ta(tmem, ab + 8 * h, blo, 1u, kIdesc);
+          mma_tf32_ta(tmem, ab + 16 + 8 * h, bhi, 1u, kIdesc);
         }
         mma_commit(smem_u32(&empty[bb]));
         bb = bb + 1 == kABufs ? 0 : bb + 1;

@@ -118,13 +118,15 @@ def test_xcorr_kernel_choice(monkeypatch):
     """Host-side dispatch (no launch, no GPU needed): the named batches take
     the kernels measured fastest for them, and the environment switches
     force or forbid the tensor-core and warp-per-overlap kernels."""
-    monkeypatch.delenv("CORR_XCORR_TC", raising=False)
-    monkeypatch.delenv("CORR_XCORR_WARP", raising=False)
+    for v in ("CORR_XCORR_TC", "CORR_XCORR_TCL", "CORR_XCORR_WARP"):
+        monkeypatch.delenv(v, raising=False)
     k = corr.xcorr_f32_kernel
     assert k(32, 64, 16, 16) == "tensor"       # n-to-m of 16x16
-    assert k(1, 1, 256, 256) == "rows"         # one-to-one
-    assert k(1, 128, 64, 64) == "bcast"        # one-to-many
-    assert k(1, 1, 1024, 1024) == "rows_win"   # rows too wide to stage whole
+    assert k(1, 1, 256, 256) == "tensor_large" # one-to-one
+    assert k(1, 128, 64, 64) == "tensor_large" # one-to-many
+    assert k(1, 1, 128, 128) == "rows"         # below the larger-matrix rule
+    assert k(1, 128, 32, 32) == "bcast"
+    assert k(1, 1, 1024, 1024) == "rows_win"   # partial sums would pass 512 MB
     assert k(1, 1, 1, 4096) == "warp"          # a single long row
     assert k(16, 16, 16, 16) == "tiny"         # small batch, below the tensor rule
     assert k(32, 64, 8, 8) == "tiny"           # H*W < 100
@@ -133,6 +135,8 @@ def test_xcorr_kernel_choice(monkeypatch):
     monkeypatch.setenv("CORR_XCORR_TC", "1")
     assert k(2, 2, 3, 5) == "tensor"
     assert k(1, 1, 17, 16) != "tensor"         # beyond 16 x 16
+    monkeypatch.setenv("CORR_XCORR_TCL", "0")
+    assert k(1, 1, 256, 256) == "rows"
     monkeypatch.setenv("CORR_XCORR_WARP", "1")
     assert k(1, 1, 40, 64) == "warp"
     with pytest.raises(corr.CorrError):

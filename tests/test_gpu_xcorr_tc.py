@@ -109,3 +109,37 @@ def test_tc_delta_reproduces_shifted_matrix(tc_on):
             want = left[:, y, x] if 0 <= y < H and 0 <= x < W else 0.0
             np.testing.assert_allclose(got[:, 0, dy + H - 1, dx + W - 1], want,
                                        rtol=3e-7, atol=0)
+
+
+# ---- larger matrices: one left's 128 shifts dx x (shift dy, right) slots,
+# K cut into 32 x 32 units whose partial sums a second kernel adds --------
+
+@pytest.fixture
+def tcl_on(monkeypatch):
+    monkeypatch.setenv("CORR_XCORR_TCL", "1")
+    monkeypatch.setenv("CORR_XCORR_TC", "0")
+    monkeypatch.setenv("CORR_XCORR_WARP", "0")
+
+
+@pytest.mark.parametrize("nl,nr,H,W", [
+    (1, 1, 40, 70), (2, 3, 33, 100), (1, 5, 130, 20), (1, 2, 17, 17), (3, 1, 1, 300),
+    (1, 4, 64, 64), (1, 6, 5, 129), (2, 9, 48, 33), (1, 1, 200, 1)])
+def test_tcl_matches_oracle(tcl_on, nl, nr, H, W):
+    assert corr.xcorr_f32_kernel(nl, nr, H, W) == "tensor_large"
+    run_check(rand(nl, H, W), rand(nr, H, W))
+
+
+def test_tcl_unaligned_rows(tcl_on):
+    run_check(rand(1, 50, 60), rand(7, 50, 60), offset=1)
+
+
+def test_tcl_one_to_one_workload_full(tcl_on):
+    """The 256x256 pair, every output (1024 units of K over 16 tiles)."""
+    w = wl.xcorr_one_to_one()
+    run_check(w.left, w.right)
+
+
+def test_tcl_one_to_many_workload_full(tcl_on):
+    """One 64x64 left against 128 rights, every output."""
+    w = wl.xcorr_one_to_many()
+    run_check(w.left, w.right)
