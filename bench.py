@@ -477,7 +477,7 @@ def extras_workloads(torch, corr, wl, dev, flush, sms, dp4a_probe, ffma_probe):
                                  "frac": gflops / (2 * ffma_peak), "timing": ROOFLINE_TIMING,
                                  "frac_single_launch": flops / (2 * ffma_peak),
                                  "algorithmic_per_unit": "2 flops per true overlap product"}}
-        if kernel == "tensor":
+        if kernel in ("tensor", "tensor_large"):
             # the split-TF32 method's own work: 3 TF32 products per product
             tf32_peak = tf32_peak_flops()
             out[key]["roofline_tensor"] = {

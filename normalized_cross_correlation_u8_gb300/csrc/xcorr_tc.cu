@@ -53,6 +53,7 @@
 // and returns.
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
 
 #include "internal.cuh"
 #include "tc_common.cuh"
@@ -85,6 +86,7 @@ struct TcArgs {
   int nl, nr, H, W;
   int mtiles, rtiles;    // tiles of kLefts lefts x kRights rights
   int vec4;              // rows readable as float4
+  int stall;             // test of the bounded waits: the last commit is left out
 };
 
 __device__ int g_tc_status;   // bit 0: a bounded wait gave up
@@ -229,8 +231,9 @@ __global__ void __launch_bounds__(kThreads + 32, 1) xcorr_tc_kernel(const TcArgs
         mma_commit(smem_u32(&empty[bb]));
         bb = bb + 1 == kABufs ? 0 : bb + 1;
       }
-      // every product issued so far, then the accumulator is final
-      mma_commit(smem_u32(done));
+      // every product issued so far, then the accumulator is final (left
+      // out under the stall test: every wait on it then runs out)
+      if (!a.stall) mma_commit(smem_u32(done));
       if (!mbar_wait_bounded(smem_u32(done), 0)) failed = 1;
       // and every stage's last release has landed (no arrival on this
       // CTA's shared memory is left pending when it exits)
@@ -350,6 +353,14 @@ cudaError_t launch(const float *left, int nl, const float *right, int nr, int H,
   a.mtiles = (nl + kLefts - 1) / kLefts;
   a.rtiles = (nr + kRights - 1) / kRights;
   a.vec4 = (W % 4 == 0 && (reinterpret_cast<uintptr_t>(right) & 15) == 0) ? 1 : 0;
+  // CORR_XCORR_TC_STALL=1 (read on every call): a test of the failure path
+  // -- the kernel's last completion barrier is never signalled, each wait
+  // on it gives up after about a second, the outputs stay unwritten and
+  // corr_device_status() reports CORR_ETIMEOUT
+  {
+    const char *v = getenv("CORR_XCORR_TC_STALL");
+    a.stall = (v && v[0] == '1' && v[1] == '\0') ? 1 : 0;
+  }
   const long long blocks = (long long)a.mtiles * a.rtiles;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   const size_t smem = 2 * size_t(kBBytes) + size_t(kLefts) * 16 * kLRow * sizeof(float) +

@@ -343,10 +343,22 @@ __global__ void __launch_bounds__(256) xcorr_tcl_sum_kernel(const TclArgs a) {
     const Tile tl = tile_of(a, b0 * a.ux);
     const int ky0 = tl.ylo / kKY, ky1 = (tl.yhi + kKY - 1) / kKY;
     const int kx0 = tl.xlo / kKX, kx1 = (tl.xhi + kKX - 1) / kKX;
+    // units in order (ky, kx); loads in batches of 8 so that they are in
+    // flight together, the adds in the same fixed order
     float s = 0.f;
-    for (int ky = ky0; ky < ky1; ++ky)
-      for (int kx = kx0; kx < kx1; ++kx)
-        s += __ldg(a.partial + ((b0 + ky) * a.ux + kx) * kTileFloats + n * kM + m);
+    const float *base = a.partial + size_t(n) * kM + m;
+    for (int ky = ky0; ky < ky1; ++ky) {
+      const float *row = base + ((b0 + ky) * a.ux) * size_t(kTileFloats);
+      for (int kx = kx0; kx < kx1; kx += 8) {
+        float v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          v[k] = kx + k < kx1 ? __ldg(row + size_t(kx + k) * kTileFloats) : 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (kx + k < kx1) s += v[k];
+      }
+    }
     a.out[o] = s;
   }
 }

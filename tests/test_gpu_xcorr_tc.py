@@ -143,3 +143,22 @@ def test_tcl_one_to_many_workload_full(tcl_on):
     """One 64x64 left against 128 rights, every output."""
     w = wl.xcorr_one_to_many()
     run_check(w.left, w.right)
+
+
+def test_bounded_wait_gives_up_and_reports(tc_on, monkeypatch):
+    """Failure path without a fault: CORR_XCORR_TC_STALL=1 leaves out the
+    kernel's last completion signal, so every wait on it runs out after
+    about a second; corr_device_status reports CORR_ETIMEOUT, the outputs
+    are left as they were, and the next call on the same context works."""
+    dev = torch.device("cuda", 0)
+    left, right = rand(4, 16, 16), rand(16, 16, 16)
+    L, R = torch.from_numpy(left).to(dev), torch.from_numpy(right).to(dev)
+    out = torch.full((4, 16, 31, 31), 5.0, dtype=torch.float32, device=dev)
+    monkeypatch.setenv("CORR_XCORR_TC_STALL", "1")
+    corr.xcorr_f32_into(L, R, out)
+    with pytest.raises(corr.CorrError) as e:
+        corr.device_status()
+    assert e.value.code == -4                  # CORR_ETIMEOUT
+    assert (out == 5.0).all()
+    monkeypatch.delenv("CORR_XCORR_TC_STALL")
+    run_check(left, right)                     # context still usable, status clear
