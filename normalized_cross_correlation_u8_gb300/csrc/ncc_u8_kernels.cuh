@@ -136,13 +136,25 @@ struct FixedShape {
 // rounded to 16) and the exchange area of the template-row split (groups
 // warp groups, ns sums per output).
 // Box-sum form: the column sums of the tile's TY output rows (row stride
-// box_v_stride words, stored at x + x/8) and the finished SumI / SumISq of
-// its TY x 128 outputs, each for I and I^2.
+// box_v_stride words, column x stored at box_v_col(x) = x + x/8) and the
+// finished SumI / SumISq of its TY x 128 outputs (16-byte chunk q of a row
+// stored at box_s_chunk(q)), each for I and I^2.
+//
+// The row pass reads the column sums as 16 runs of 8 (columns 8 k + j) from
+// two rows at once: column 8 k + j lands in bank 9 k + j + j/8 (mod 32), 16
+// distinct banks, and a row stride of 16 mod 32 puts the second row on the
+// other 16.
+__host__ __device__ inline int box_v_col(int x) { return x + (x >> 3); }
 __host__ __device__ inline int box_v_stride(int wt) {
   const int nv = kHalfUnitCols + wt - 1;              // columns a tile's windows reach
-  const int last = (nv - 1) + ((nv - 1) >> 3);        // skewed index of the last one
+  const int last = box_v_col(nv - 1);                 // skewed index of the last one
   return ((last + 1 - 16 + 31) & ~31) + 16;           // = 16 mod 32: conflict-free rows
 }
+// Finished sums are written and read as two 16-byte chunks 2k, 2k + 1 per
+// thread, 8 threads (k = 8 g .. 8 g + 7) per shared-memory phase: flipping
+// the low bit of every chunk in the upper half of each group of 16 spreads
+// those 8 chunks over all 32 banks.
+__host__ __device__ inline int box_s_chunk(int q) { return q ^ ((q >> 3) & 1); }
 // The box-sum form reuses dead regions: once the dp4a loop is done, the
 // column sums overwrite the template and the finished SumI / SumISq the
 // tile, so its layout is [tile | exchange | template], each of the first
@@ -463,7 +475,7 @@ __device__ __forceinline__ void box_columns(const uint8_t *tile, int ht, int nv,
       s += b;
       q += b * b;
     }
-    const int xs = x + (x >> 3);
+    const int xs = box_v_col(x);
     v_i[xs] = s;
     v_q[xs] = q;
 #pragma unroll
@@ -492,7 +504,7 @@ __device__ __forceinline__ void box_rows(const uint32_t *v_i, const uint32_t *v_
     uint32_t s = 0, q = 0;
 #pragma unroll 4
     for (int j = 0; j < wt; ++j) {
-      const int x = c0 + j, xs = x + (x >> 3);
+      const int x = c0 + j, xs = box_v_col(x);
       s += ri[xs];
       q += rq[xs];
     }
@@ -502,17 +514,18 @@ __device__ __forceinline__ void box_rows(const uint32_t *v_i, const uint32_t *v_
 #pragma unroll
     for (int c = 1; c < kCols; ++c) {
       const int xo = c0 + c - 1, xi = xo + wt;
-      s += ri[xi + (xi >> 3)] - ri[xo + (xo >> 3)];
-      q += rq[xi + (xi >> 3)] - rq[xo + (xo >> 3)];
+      s += ri[box_v_col(xi)] - ri[box_v_col(xo)];
+      q += rq[box_v_col(xi)] - rq[box_v_col(xo)];
       oi[c] = s;
       oq[c] = q;
     }
-    uint4 *di = reinterpret_cast<uint4 *>(s_i + y * kHalfUnitCols + c0);
-    uint4 *dq = reinterpret_cast<uint4 *>(s_q + y * kHalfUnitCols + c0);
+    uint4 *di = reinterpret_cast<uint4 *>(s_i + y * kHalfUnitCols);
+    uint4 *dq = reinterpret_cast<uint4 *>(s_q + y * kHalfUnitCols);
 #pragma unroll
     for (int c = 0; c < kCols; c += 4) {
-      di[c / 4] = make_uint4(oi[c], oi[c + 1], oi[c + 2], oi[c + 3]);
-      dq[c / 4] = make_uint4(oq[c], oq[c + 1], oq[c + 2], oq[c + 3]);
+      const int ch = box_s_chunk((c0 + c) >> 2);
+      di[ch] = make_uint4(oi[c], oi[c + 1], oi[c + 2], oi[c + 3]);
+      dq[ch] = make_uint4(oq[c], oq[c + 1], oq[c + 2], oq[c + 3]);
     }
   }
 }
@@ -739,7 +752,7 @@ __global__ void __launch_bounds__(FixedShape<BOX>::kThreadsPerCta,
       for (int r = 0; r < R; ++r)
 #pragma unroll
         for (int c = 0; c < kCols; c += 4) {
-          const int o = (yr0 + r) * kHalfUnitCols + hl * kCols + c;
+          const int o = (yr0 + r) * kHalfUnitCols + 4 * box_s_chunk((hl * kCols + c) >> 2);
           const uint4 vi = *reinterpret_cast<const uint4 *>(s_i + o);
           const uint4 vq = *reinterpret_cast<const uint4 *>(s_q + o);
           sI[r][c] = vi.x; sI[r][c + 1] = vi.y; sI[r][c + 2] = vi.z; sI[r][c + 3] = vi.w;

@@ -20,14 +20,31 @@ static int fails = 0;
 
 int main() {
   long cases = 0;
+  // finished sums: the chunks 2k (and 2k + 1) of 8 consecutive k fill all
+  // 32 banks
+  for (int g = 0; g < 4; ++g)
+    for (int odd = 0; odd < 2; ++odd) {
+      unsigned banks = 0;
+      for (int k = 8 * (g % 2); k < 8 * (g % 2) + 8; ++k)
+        for (int w = 0; w < 4; ++w) banks |= 1u << ((4 * box_s_chunk(2 * k + odd + 32 * (g / 2)) + w) & 31);
+      CHECK(banks == 0xffffffffu, "finished-sum chunks of group %d conflict\n", g);
+    }
   for (int wt = 1; wt <= 4 * kMaxFixedWords; ++wt) {
     const int wtw = (wt + 3) / 4, wtp = (wtw + 3) & ~3;
-    // column sums: stride = 16 mod 32 and room for the last skewed column
+    // column sums: stride 16 mod 32, room for the last skewed column, and
+    // the row pass's reads (columns 8 k + j of two rows) on 32 distinct banks
     const int vs = box_v_stride(wt);
     const int nv = kHalfUnitCols + wt - 1;
     CHECK(vs % 32 == 16, "wt %d: v stride %d not 16 mod 32\n", wt, vs);
-    CHECK((nv - 1) + ((nv - 1) >> 3) < vs, "wt %d: v stride %d too small\n", wt, vs);
-    for (int ht = 1; ht * wt <= 66052; ++ht) {
+    CHECK(box_v_col(nv - 1) < vs, "wt %d: v stride %d too small\n", wt, vs);
+    for (int x0 = 0; x0 + 8 * 15 + 7 < nv; x0 += 1) {
+      unsigned banks = 0;
+      for (int row = 0; row < 2; ++row)
+        for (int k = 0; k < 16; ++k)
+          banks |= 1u << ((row * vs + box_v_col(x0 + 8 * k)) & 31);
+      CHECK(banks == 0xffffffffu, "wt %d x0 %d: row-pass reads conflict\n", wt, x0);
+    }
+    for (int ht = 1; ht * wt <= 66051; ++ht) {
       for (int box = 0; box < 2; ++box) {
         for (int rows = 1; rows <= 2; ++rows) {
           const int warps = box ? kBoxWarps : kWarpsPerCta;
