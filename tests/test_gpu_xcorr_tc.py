@@ -162,3 +162,28 @@ def test_bounded_wait_gives_up_and_reports(tc_on, monkeypatch):
     assert (out == 5.0).all()
     monkeypatch.delenv("CORR_XCORR_TC_STALL")
     run_check(left, right)                     # context still usable, status clear
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_tc_random_shapes(tc_on, seed):
+    """Random batch shapes within the small-matrix kernel's range."""
+    rng = np.random.default_rng(900 + seed)
+    nl, nr = int(rng.integers(1, 40)), int(rng.integers(1, 70))
+    H, W = int(rng.integers(1, 17)), int(rng.integers(1, 17))
+    run_check(rand(nl, H, W), rand(nr, H, W))
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_tcl_random_shapes(tcl_on, seed):
+    """Random shapes for the larger-matrix kernel: one or a few lefts,
+    1-20 rights, sides 1-90 (tiles cut in every direction, K units that
+    straddle the matrix edges)."""
+    rng = np.random.default_rng(950 + seed)
+    nl, nr = int(rng.integers(1, 3)), int(rng.integers(1, 21))
+    H, W = int(rng.integers(1, 91)), int(rng.integers(1, 91))
+    run_check(rand(nl, H, W), rand(nr, H, W))
+
+
+def test_tc_large_batch_of_small_matrices(tc_on):
+    """A batch of 160 x 96 pairs of 12x12 (many tiles, partial right tiles)."""
+    run_check(rand(160, 12, 12), rand(96, 12, 12))
