@@ -187,3 +187,23 @@ def test_tcl_random_shapes(tcl_on, seed):
 def test_tc_large_batch_of_small_matrices(tc_on):
     """A batch of 160 x 96 pairs of 12x12 (many tiles, partial right tiles)."""
     run_check(rand(160, 12, 12), rand(96, 12, 12))
+
+
+@pytest.mark.parametrize("mode,shape", [("tc", (5, 7, 13, 11)), ("tcl", (1, 6, 45, 70))])
+def test_tensor_core_kernels_write_nothing_outside_the_output(monkeypatch, mode, shape):
+    """Outputs written into the middle of a larger buffer: canaries on both
+    sides survive (the epilogues store whole lines of runs: their edges
+    must stop at the output's)."""
+    monkeypatch.setenv("CORR_XCORR_TC" if mode == "tc" else "CORR_XCORR_TCL", "1")
+    nl, nr, H, W = shape
+    left, right = rand(nl, H, W), rand(nr, H, W)
+    dev = torch.device("cuda", 0)
+    n = nl * nr * (2 * H - 1) * (2 * W - 1)
+    pad = 4099                                  # odd: the output starts mid-line
+    buf = torch.full((n + 2 * pad,), 777.0, dtype=torch.float32, device=dev)
+    out = buf[pad:pad + n].view(nl, nr, 2 * H - 1, 2 * W - 1)
+    corr.xcorr_f32_into(torch.from_numpy(left).to(dev), torch.from_numpy(right).to(dev), out)
+    corr.device_status()
+    assert (buf[:pad] == 777.0).all() and (buf[-pad:] == 777.0).all()
+    ref, ab = oracle.xcorr_f32(left, right, nthreads=NT)
+    assert (np.abs(out.cpu().numpy().astype(np.float64) - ref) <= REL_TOL * ab + 1e-30).all()
