@@ -12,23 +12,37 @@
 // (N = NDY shifts x NR rights, right fastest: 128 shifts of one right for
 // one-to-one, 32 shifts x 4 rights for one-to-many).  Its K -- every row y
 // and column x' that some shift of the tile reaches -- is cut into units of
-// 32 rows x 32 columns, one CTA each, so that a large pair spreads over the
-// whole GPU.  A unit's partial 128 x 128 sums go to scratch memory and a
-// second kernel adds the units of each tile in a fixed order (the result
-// does not depend on scheduling).
+// 32 rows x 32 columns.  An item is one tile's unit column and a group of G
+// consecutive row units (G = 1 up to about 256 x 256, more for larger
+// matrices so that the partial tiles stay within 64 MB).  The kernel is
+// persistent, one CTA per SM taking items in turn; each item's 128 x 128
+// partial sums go to scratch memory and a second kernel adds those of each
+// tile in a fixed order (the result does not depend on scheduling).
 //
-// Operands: B (rows of R) is staged once per unit in shared memory in the
+// Accuracy: the tensor cores accumulate FP32 with truncation, so on inputs
+// of one sign the error of a chain of accumulates grows with its length
+// (measured on GB300: about 2e-8 of the sum per accumulate; 384 of them, one
+// 32-row unit, reached 1.1e-5 of sum |L*R| on uniform [0, 1) inputs).  A
+// chain here is at most 8 rows (96 accumulates) in one of two tensor-memory
+// accumulators; the builder warps add each finished chain into an FP32
+// running sum in registers (round to nearest) while the next chain runs in
+// the other accumulator.
+//
+// Operands: B (rows of R) is staged per unit in shared memory in the
 // no-swizzle K-major layout [x'/4][row slot][right][4 floats], rows in
 // reverse order, so the N rows of consecutive shifts dy are consecutive
-// slots and one descriptor per (y, 8 columns) reads them; A (the Toeplitz
-// rows of L) is written per overlap row by eight builder warps straight
-// into tensor memory (tcgen05.st), double-buffered; one warp issues
-// kind::tf32 tcgen05.mma into a 128-column FP32 accumulator in tensor
-// memory.  Operands are split v = tf32(v) + tf32(v - tf32(v)) and each
-// product is formed as hi*hi + hi*lo + lo*hi (the three-pass TF32 scheme;
-// see xcorr_tc.cu).  Every mbarrier wait is bounded (corr_device_status).
+// slots and one descriptor per (y, 8 columns) reads them; two units are
+// staged at a time.  A (the Toeplitz rows of L) is written per overlap row
+// by eight builder warps straight into tensor memory (tcgen05.st) through
+// four stages; one warp issues kind::tf32 tcgen05.mma, reading per row a
+// record (B offset, K steps, accumulator, chain start / end) that the
+// builders leave beside the stage.  Operands are split v = tf32(v) +
+// tf32(v - tf32(v)) and each product is formed as hi*hi + hi*lo + lo*hi
+// (the three-pass TF32 scheme; see xcorr_tc.cu).  Every mbarrier wait is
+// bounded (corr_device_status).
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
 
 #include "internal.cuh"
 #include "tc_common.cuh"
@@ -45,52 +59,76 @@ constexpr int kN = 128;                   // (shift dy, right) slots
 constexpr int kKY = 32;                   // overlap rows per unit
 constexpr int kKX = 32;                   // right columns per unit
 constexpr int kSteps = kKX / 8;           // 8-deep K steps per row
-constexpr int kABufs = 2;                 // A stages in tensor memory
+constexpr int kSegRows = 8;               // overlap rows per accumulation chain
+constexpr int kABufs = 4;                 // A stages in tensor memory
 constexpr int kStageCols = kSteps * 16;   // hi + lo columns of one A stage
-constexpr uint32_t kTmemCols = 256;       // accumulator (128) + kABufs stages (64 each)
+constexpr uint32_t kAccCols = kN;         // one FP32 accumulator
+constexpr uint32_t kTmemCols = 512;       // 2 accumulators + kABufs A stages
 constexpr int kLRowF = kKX + kM;          // floats of a staged left row segment
+constexpr int kLBuf = kKY * kLRowF;       // floats of one unit's left rows
 constexpr int kMaxSlots = kKY + kN - 1;   // right row slots (NDY = 128)
 constexpr int kMaxBEntries = 8 * (kKY + 32 - 1) * 4;   // NR = 4: the largest B
+constexpr int kBHalf = kMaxBEntries * 16; // bytes of the hi (or lo) parts of one B
+constexpr int kBBuf = 2 * kBHalf;         // one staged B (hi, then lo)
 constexpr int kTileFloats = kM * kN;      // one partial tile
+constexpr size_t kTargetScratch = size_t(64) << 20;   // partial tiles, when row groups allow
 constexpr uint32_t kIdesc = idesc_tf32(kM, kN);
 static_assert(8 * kMaxSlots * 1 <= kMaxBEntries && 8 * (kKY + 64 - 1) * 2 <= kMaxBEntries,
               "B staging holds every right-tile shape");
+static_assert(2 * kAccCols + kABufs * kStageCols == kTmemCols, "tensor memory plan");
+static_assert(kKY % kSegRows == 0, "chains never cross a unit");
+
+// shared memory: two staged B, two units' left rows, the row records the
+// builders pass to the issuer, the mbarriers and the tensor-memory address
+constexpr size_t kLpOff = 2 * size_t(kBBuf);
+constexpr size_t kInfoOff = kLpOff + 2 * size_t(kLBuf) * sizeof(float);
+constexpr size_t kBarOff = kInfoOff + kABufs * sizeof(uint2);
+constexpr int kBars = 2 * kABufs + 3;    // full, empty, chain done x 2, done
+constexpr size_t kSmemBytes = kBarOff + kBars * 8 + 16;
+
+// row record flags (second word): K steps [j_lo, j_hi), accumulator, first
+// and last row of a chain, end of the CTA's work
+constexpr uint32_t kRecAcc = 1u << 8, kRecFirst = 1u << 9, kRecLast = 1u << 10,
+                   kRecStop = 1u << 11;
 
 struct TclArgs {
   const float *left;
   const float *right;
-  float *partial;        // [units][kN][kM]
+  float *partial;        // [items][kN][kM]
   float *out;
   int nl, nr, H, W;
   int nr_log2;           // rights per tile NR = 1 << nr_log2 (1, 2 or 4)
   int ndy;               // shift slots per tile: kN / NR
   int ndxt, ndyt, nrt;   // tiles along dx, dy, rights
   int uy, ux;            // units along rows, columns of K
+  int ug, ugn;           // row units per item, groups of them along the rows
+  long long items;       // work items: tiles x ugn x ux (below 2^31 at launch)
   int vec4;              // rows readable as float4
 };
 
 __device__ int g_tcl_status;   // bit 0: a bounded wait gave up
 
-// The tile of unit b and its ranges: rows y and columns x' that some shift
-// of the tile reaches (nonempty for every tile).
+// The tile of item b (its unit column and row-unit group) and the ranges
+// of the tile: rows y and columns x' that some shift of the tile reaches
+// (nonempty for every tile).
 struct Tile {
-  int l, dxt, dyt, rt, ky, kx;
+  int l, dxt, dyt, rt, kg, kx;
   int dx0, dy0, r0;
   int ylo, yhi, xlo, xhi;
 };
 
-__device__ __forceinline__ Tile tile_of(const TclArgs &a, long long b) {
+__device__ __forceinline__ Tile tile_of(const TclArgs &a, int b) {
   Tile t;
-  t.kx = int(b % a.ux);
+  t.kx = b % a.ux;
   b /= a.ux;
-  t.ky = int(b % a.uy);
-  b /= a.uy;
-  t.rt = int(b % a.nrt);
+  t.kg = b % a.ugn;
+  b /= a.ugn;
+  t.rt = b % a.nrt;
   b /= a.nrt;
-  t.dyt = int(b % a.ndyt);
+  t.dyt = b % a.ndyt;
   b /= a.ndyt;
-  t.dxt = int(b % a.ndxt);
-  t.l = int(b / a.ndxt);
+  t.dxt = b % a.ndxt;
+  t.l = b / a.ndxt;
   t.dx0 = t.dxt * kM - (a.W - 1);
   t.dy0 = t.dyt * a.ndy - (a.H - 1);
   t.r0 = t.rt << a.nr_log2;
@@ -102,27 +140,167 @@ __device__ __forceinline__ Tile tile_of(const TclArgs &a, long long b) {
   return t;
 }
 
-__global__ void __launch_bounds__(kThreads + 32, 2) xcorr_tcl_kernel(const TclArgs a) {
+// An item: one tile's unit column kx and its row units [ka, kb) that hold
+// rows of the tile; K steps [j_lo, j_hi) of the columns it reaches.
+struct Item {
+  int b;                 // -1: none
+  int l, dx0, dy0, r0, ylo, yhi;
+  int xa, ka, kb, j_lo, j_hi;
+};
+
+__device__ __forceinline__ bool item_at(const TclArgs &a, int b, Item &it) {
+  const Tile tl = tile_of(a, b);
+  it.b = b;
+  it.l = tl.l;
+  it.dx0 = tl.dx0;
+  it.dy0 = tl.dy0;
+  it.r0 = tl.r0;
+  it.ylo = tl.ylo;
+  it.yhi = tl.yhi;
+  it.xa = tl.kx * kKX;
+  const int x0 = it.xa > tl.xlo ? it.xa : tl.xlo;
+  const int x1 = it.xa + kKX < tl.xhi ? it.xa + kKX : tl.xhi;
+  const int kvlo = tl.ylo / kKY, kvhi = (tl.yhi + kKY - 1) / kKY;
+  it.ka = tl.kg * a.ug > kvlo ? tl.kg * a.ug : kvlo;
+  it.kb = (tl.kg + 1) * a.ug < kvhi ? (tl.kg + 1) * a.ug : kvhi;
+  it.j_lo = (x0 - it.xa) >> 3;
+  it.j_hi = (x1 - it.xa + 7) >> 3;
+  return it.ka < it.kb && x0 < x1;
+}
+
+// The first item from b on, in steps of the grid, that holds products.
+__device__ __forceinline__ void first_item(const TclArgs &a, int b, Item &it) {
+  for (; b < a.items; b += int(gridDim.x))
+    if (item_at(a, b, it)) return;
+  it.b = -1;
+}
+
+// Rows of unit ky of an item: [max(ky kKY, ylo), min(ky kKY + kKY, yhi)).
+__device__ __forceinline__ void unit_rows(const Item &it, int ky, int &y0, int &y1) {
+  const int ya = ky * kKY;
+  y0 = ya > it.ylo ? ya : it.ylo;
+  y1 = ya + kKY < it.yhi ? ya + kKY : it.yhi;
+}
+
+// Stage unit ky of an item: B entry e = (xc, slot, r) -> R[r0 + r][yr][xa +
+// 4 xc .. + 3] with yr = ya + kKY - 1 - dy0 - slot, as TF32 hi (bb) and lo
+// (bb + kBHalf), consecutive 16-byte rows; the left's rows y0 .. y1 - 1,
+// columns xa + dx0 .. + kLRowF - 1: lpu[y - y0][p] = L[l][y][xa + dx0 + p]
+// (zero outside the matrices).
+__device__ __forceinline__ void stage_unit(const TclArgs &a, const Item &it, int ky, uint8_t *bb,
+                                           float *lpu, int t, int NS) {
+  const int H = a.H, W = a.W, NR = 1 << a.nr_log2;
+  const int ya = ky * kKY;
+  int y0, y1;
+  unit_rows(it, ky, y0, y1);
+  // (two batches each, to bound the registers held: the builders keep
+  // their running sums live across this)
+  {
+    const int nl_ent = (y1 - y0) * kLRowF;
+    constexpr int kLPer = (kLBuf + 2 * kThreads - 1) / (2 * kThreads);
+    const float *lrow = a.left + size_t(it.l) * H * W;
+    const int xb = it.xa + it.dx0;
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+      float lv[kLPer];
+#pragma unroll
+      for (int k = 0; k < kLPer; ++k) {
+        const int i = t + (h * kLPer + k) * kThreads;
+        const int p = i % kLRowF, ry = i / kLRowF;
+        const int x = xb + p;
+        lv[k] = 0.f;
+        if (i < nl_ent && x >= 0 && x < W) lv[k] = __ldg(lrow + size_t(y0 + ry) * W + x);
+      }
+#pragma unroll
+      for (int k = 0; k < kLPer; ++k) {
+        const int i = t + (h * kLPer + k) * kThreads;
+        if (i < nl_ent) lpu[i] = lv[k];
+      }
+    }
+  }
+  const int nent = 8 * NS * NR;
+  const int yc = ya + kKY - 1 - it.dy0;
+  constexpr int kPer = (kMaxBEntries + 2 * kThreads - 1) / (2 * kThreads);
+#pragma unroll 1
+  for (int h = 0; h < 2; ++h) {
+    float4 bv[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int e = t + (h * kPer + k) * kThreads;
+      bv[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (e < nent) {
+        const int r = e & (NR - 1), qq = e >> a.nr_log2;
+        const int sl = qq % NS, xc = qq / NS;
+        const int yr = yc - sl, rr = it.r0 + r, x = it.xa + 4 * xc;
+        if (rr < a.nr && yr >= 0 && yr < H && x < W) {
+          const float *src = a.right + (size_t(rr) * H + yr) * W + x;
+          if (a.vec4) {
+            bv[k] = __ldg(reinterpret_cast<const float4 *>(src));
+          } else {
+            bv[k].x = __ldg(src);
+            if (x + 1 < W) bv[k].y = __ldg(src + 1);
+            if (x + 2 < W) bv[k].z = __ldg(src + 2);
+            if (x + 3 < W) bv[k].w = __ldg(src + 3);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int e = t + (h * kPer + k) * kThreads;
+      if (e >= nent) break;
+      uint4 hi, lo;
+      split_tf32(bv[k].x, hi.x, lo.x);
+      split_tf32(bv[k].y, hi.y, lo.y);
+      split_tf32(bv[k].z, hi.z, lo.z);
+      split_tf32(bv[k].w, hi.w, lo.w);
+      *reinterpret_cast<uint4 *>(bb + e * 16) = hi;
+      *reinterpret_cast<uint4 *>(bb + kBHalf + e * 16) = lo;
+    }
+  }
+  // generic-proxy stores -> the tensor cores' (async proxy) reads
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Barrier of the builder warps (named barrier 1) returning the OR of v.
+__device__ __forceinline__ int builders_sync_or(int v) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.s32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, 1, %2, q;\n\t"
+      "selp.s32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(v), "n"(kThreads)
+      : "memory");
+  return r;
+}
+
+// Persistent: CTA c takes the items c, c + grid, ... that hold products.
+// Its row stream (every row of every unit of those items) runs through
+// kABufs A stages; each chain of up to kSegRows rows of one unit
+// accumulates in one of two accumulators (the tensor cores' FP32
+// accumulation truncates, so a chain stays short: at most 96 updates), and
+// the builders add the finished chain into an FP32 running sum of the item
+// held in registers (thread: accumulator row 32 (warp % 4) + lane, columns
+// 64 (warp / 4) .. + 63), while the next chain runs in the other
+// accumulator.  At the end of an item the running sum goes to its partial
+// tile.
+__global__ void __launch_bounds__(kThreads + 32, 1) xcorr_tcl_kernel(const TclArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint8_t *b_hi = smem;                                   // [8][NS][NR][4] TF32 hi
-  uint8_t *b_lo = smem + kMaxBEntries * 16;               // lo parts
-  float *lp = reinterpret_cast<float *>(smem + 2 * kMaxBEntries * 16);   // [kKY][kLRowF]
-  uint64_t *full = reinterpret_cast<uint64_t *>(lp + kKY * kLRowF);
-  uint64_t *empty = full + kABufs;
-  uint64_t *done = empty + kABufs;
+  float *lp = reinterpret_cast<float *>(smem + kLpOff);                  // [2][kLBuf]
+  uint2 *info = reinterpret_cast<uint2 *>(smem + kInfoOff);             // [kABufs]
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + kBarOff);        // [kABufs]
+  uint64_t *empty = full + kABufs;                                       // [kABufs]
+  uint64_t *chain = empty + kABufs;                                      // [2]
+  uint64_t *done = chain + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
 
-  const Tile tl = tile_of(a, blockIdx.x);
-  const int ya = tl.ky * kKY, xa = tl.kx * kKX;
-  const int y0 = ya > tl.ylo ? ya : tl.ylo;
-  const int y1 = ya + kKY < tl.yhi ? ya + kKY : tl.yhi;
-  const int x0 = xa > tl.xlo ? xa : tl.xlo;
-  const int x1 = xa + kKX < tl.xhi ? xa + kKX : tl.xhi;
-  if (y0 >= y1 || x0 >= x1) return;            // no product of the tile here
-  const int j_lo = (x0 - xa) >> 3, j_hi = (x1 - xa + 7) >> 3;   // K steps used
+  Item cur;
+  first_item(a, int(blockIdx.x), cur);
+  if (cur.b < 0) return;                       // no products for this CTA
   const int NR = 1 << a.nr_log2, NS = kKY + a.ndy - 1;
-  const int H = a.H, W = a.W, t = threadIdx.x;
-  const int warp = t >> 5, lane = t & 31;
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const bool issuer = warp == kThreads / 32;
 
   if (issuer) {
@@ -137,180 +315,213 @@ __global__ void __launch_bounds__(kThreads + 32, 2) xcorr_tcl_kernel(const TclAr
         mbar_init(smem_u32(&full[k]), kThreads / 32);
         mbar_init(smem_u32(&empty[k]), 1);
       }
+      mbar_init(smem_u32(&chain[0]), 1);
+      mbar_init(smem_u32(&chain[1]), 1);
       mbar_init(smem_u32(done), 1);
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-  } else {
-    // B: entry e = (xc, slot, r) -> R[r0 + r][yr][xa + 4 xc .. + 3] with
-    // yr = ya + kKY - 1 - dy0 - slot (zero outside the matrix); entries are
-    // consecutive 16-byte rows, all loads of a thread in flight together
-    const int nent = 8 * NS * NR;
-    const int yc = ya + kKY - 1 - tl.dy0;
-    constexpr int kPer = (kMaxBEntries + kThreads - 1) / kThreads;
-    float4 bv[kPer];
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const int e = t + k * kThreads;
-      bv[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (e < nent) {
-        const int r = e & (NR - 1), q = e >> a.nr_log2;
-        const int s = q % NS, xc = q / NS;
-        const int yr = yc - s, rr = tl.r0 + r, x = xa + 4 * xc;
-        if (rr < a.nr && yr >= 0 && yr < H && x < W) {
-          const float *src = a.right + (size_t(rr) * H + yr) * W + x;
-          if (a.vec4) {
-            bv[k] = __ldg(reinterpret_cast<const float4 *>(src));
-          } else {
-            bv[k].x = __ldg(src);
-            if (x + 1 < W) bv[k].y = __ldg(src + 1);
-            if (x + 2 < W) bv[k].z = __ldg(src + 2);
-            if (x + 3 < W) bv[k].w = __ldg(src + 3);
-          }
-        }
-      }
-    }
-    // the left's rows y0 .. y1 - 1, columns xa + dx0 .. + kLRowF - 1
-    // (zero outside the matrix): lp[y - y0][p] = L[l][y][xa + dx0 + p]
-    {
-      const int nl_ent = (y1 - y0) * kLRowF;
-      constexpr int kLPer = (kKY * kLRowF + kThreads - 1) / kThreads;
-      const float *lrow = a.left + size_t(tl.l) * H * W;
-      const int xb = xa + tl.dx0;
-      float lv[kLPer];
-#pragma unroll
-      for (int k = 0; k < kLPer; ++k) {
-        const int i = t + k * kThreads;
-        const int p = i % kLRowF, ry = i / kLRowF;
-        const int x = xb + p;
-        lv[k] = 0.f;
-        if (i < nl_ent && x >= 0 && x < W) lv[k] = __ldg(lrow + size_t(y0 + ry) * W + x);
-      }
-#pragma unroll
-      for (int k = 0; k < kLPer; ++k) {
-        const int i = t + k * kThreads;
-        if (i < nl_ent) lp[i] = lv[k];
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const int e = t + k * kThreads;
-      if (e >= nent) break;
-      uint4 hi, lo;
-      split_tf32(bv[k].x, hi.x, lo.x);
-      split_tf32(bv[k].y, hi.y, lo.y);
-      split_tf32(bv[k].z, hi.z, lo.z);
-      split_tf32(bv[k].w, hi.w, lo.w);
-      *reinterpret_cast<uint4 *>(b_hi + e * 16) = hi;
-      *reinterpret_cast<uint4 *>(b_lo + e * 16) = lo;
-    }
-    // generic-proxy stores -> the tensor cores' (async proxy) reads
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t a_cols = tmem + uint32_t(kN);     // A stage b: columns + kStageCols b
-  const int ny = y1 - y0;
+  const uint32_t a_cols = tmem + 2 * kAccCols;     // A stage s: columns + kStageCols s
   int failed = 0;
 
   if (issuer) {
     if (lane == 0) {
-      const uint32_t bh_base = smem_u32(b_hi), bl_base = smem_u32(b_lo);
+      const uint32_t b_base = smem_u32(smem);
       const uint32_t lbo_b = uint32_t(NS * NR * 16);     // next 4 columns x'
-      uint32_t fpar = 0;
-      int bb = 0;
-      for (int i = 0; i < ny; ++i) {
-        if (!mbar_wait_bounded(smem_u32(&full[bb]), (fpar >> bb) & 1u)) {
+      int g = 0;
+      for (;; ++g) {
+        const int s = g % kABufs;
+        if (!mbar_wait_bounded(smem_u32(&full[s]), uint32_t(g / kABufs) & 1u)) {
           failed = 1;
           break;
         }
-        fpar ^= 1u << bb;
         fence_after_sync();
-        // N row n = (dyi, r): right row y - dy0 - dyi, slot
-        // (ya + kKY - 1 - y) + dyi, so row n sits n * 16 bytes past it
-        const uint32_t s0off = uint32_t((ya + kKY - 1 - (y0 + i)) * NR * 16);
-        const uint32_t ab = a_cols + uint32_t(kStageCols * bb);
+        const uint2 rec = info[s];
+        if (rec.y & kRecStop) break;
+        const int j_lo = rec.y & 15, j_hi = (rec.y >> 4) & 15;
+        const uint32_t d = tmem + ((rec.y & kRecAcc) ? kAccCols : 0u);
+        const uint32_t ab = a_cols + uint32_t(kStageCols * s);
 #pragma unroll
         for (int j = 0; j < kSteps; ++j) {
           if (j < j_lo || j >= j_hi) continue;
-          const uint32_t boff = s0off + uint32_t(2 * j) * lbo_b;
-          const uint64_t bhi = smem_desc(bh_base + boff, lbo_b, 128);
-          const uint64_t blo = smem_desc(bl_base + boff, lbo_b, 128);
-          const uint32_t acc = (i > 0 || j > j_lo) ? 1u : 0u;
-          mma_tf32_ta(tmem, ab + 16 * j, bhi, acc, kIdesc);
-          mma_tf32_ta(tmem, ab + 16 * j, blo, 1u, kIdesc);
-          mma_tf32_ta(tmem, ab + 16 * j + 8, bhi, 1u, kIdesc);
+          const uint32_t boff = b_base + rec.x + uint32_t(2 * j) * lbo_b;
+          const uint64_t bhi = smem_desc(boff, lbo_b, 128);
+          const uint64_t blo = smem_desc(boff + kBHalf, lbo_b, 128);
+          const uint32_t acc = ((rec.y & kRecFirst) && j == j_lo) ? 0u : 1u;
+          mma_tf32_ta(d, ab + 16 * j, bhi, acc, kIdesc);
+          mma_tf32_ta(d, ab + 16 * j, blo, 1u, kIdesc);
+          mma_tf32_ta(d, ab + 16 * j + 8, bhi, 1u, kIdesc);
         }
-        mma_commit(smem_u32(&empty[bb]));
-        bb = bb + 1 == kABufs ? 0 : bb + 1;
+        mma_commit(smem_u32(&empty[s]));
+        if (rec.y & kRecLast) mma_commit(smem_u32(&chain[(rec.y & kRecAcc) ? 1 : 0]));
       }
       mma_commit(smem_u32(done));
       if (!mbar_wait_bounded(smem_u32(done), 0)) failed = 1;
-      for (int k = 0; k < kABufs && k < ny; ++k) {
-        const int uses = (ny - k + kABufs - 1) / kABufs;
+      // every stage's last release has landed (no arrival on this CTA's
+      // shared memory is left pending when it exits)
+      for (int k = 0; k < kABufs && k < g; ++k) {
+        const int uses = (g - k + kABufs - 1) / kABufs;
         if (!mbar_wait_bounded(smem_u32(&empty[k]), uint32_t(uses - 1) & 1u)) failed = 1;
       }
     }
   } else {
-    // thread: A row m = 32 (warp % 4) + lane (shift dx = dx0 + m), K steps
-    // j = warp / 4 and j + 2: the 8 values L[l][y][x' + dx], x' = xa + 8j ..
-    // + 7, as TF32 hi and lo
+    // thread: A row m = 32 q + lane (shift dx = dx0 + m) with q = warp % 4,
+    // K steps j = jh and jh + 2 (jh = warp / 4): the 8 values L[l][y][x' +
+    // dx], x' = xa + 8j .. + 7, as TF32 hi and lo; accumulator columns
+    // 64 jh .. + 63 of row m
     const int q = warp & 3, jh = warp >> 2;
     const int m = 32 * q + lane;
     const uint32_t lane_base = uint32_t(32 * q) << 16;
+    float sum[64];
+#pragma unroll
+    for (int k = 0; k < 64; ++k) sum[k] = 0.f;
+
+    // the current unit (item cb, row unit cky) and the one after it (nb,
+    // nky; nb < 0: none); item geometry is recomputed where it is needed
+    int cb = cur.b, nb;
+    int cky = cur.ka, nky;
+    auto advance = [&]() {
+      Item it;
+      item_at(a, cb, it);
+      if (cky + 1 < it.kb) {
+        nb = cb;
+        nky = cky + 1;
+      } else {
+        first_item(a, cb + int(gridDim.x), it);
+        nb = it.b;
+        nky = it.ka;
+      }
+    };
+    auto stage_next = [&](int buf) {
+      Item it;
+      item_at(a, nb, it);
+      stage_unit(a, it, nky, smem + buf * kBBuf, lp + buf * kLBuf, t, NS);
+    };
+    advance();
+    stage_unit(a, cur, cky, smem, lp, t, NS);
+    if (nb >= 0) stage_next(1);
+    failed = builders_sync_or(failed);
+
+    // the chain whose sum is still to be taken in
+    int pseg = -1;            // its index (chains built before it: pseg)
+    int pitem = -1;           // its item, if it ends that item
+    bool punit_end = false;   // whether it ends its unit
+    int g = 0, seg = 0, u = 0;
     uint32_t epar = 0;
-    int bb = 0;
-    for (int i = 0; i < ny; ++i) {
-      if (i >= kABufs) {
-        if (!mbar_wait_bounded(smem_u32(&empty[bb]), (epar >> bb) & 1u)) {
-          failed = 1;
-          break;
-        }
-        epar ^= 1u << bb;
-        fence_after_sync();
-      }
-      const float *ls = lp + i * kLRowF + m;
+
+    // Take in chain pseg: wait for its products, add its accumulator to the
+    // running sum; at the end of an item store the sum; at the end of a
+    // unit, stage the unit after the current one into the buffers that
+    // unit used.
+    auto take_in = [&]() {
+      const int pb = pseg & 1;
+      if (!failed && !mbar_wait_bounded(smem_u32(&chain[pb]), uint32_t(pseg >> 1) & 1u))
+        failed = 1;
+      failed = __any_sync(~0u, failed);     // the warp's .aligned steps stay together
+      fence_after_sync();
+      if (!failed) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + uint32_t(pb) * kAccCols + uint32_t(64 * jh), v);
 #pragma unroll
-      for (int jj = 0; jj < 2; ++jj) {
-        const int j = jh + 2 * jj;
-        if (j < j_lo || j >= j_hi) continue;
-        uint32_t hi[8], lo[8];
+        for (int k = 0; k < 32; ++k) sum[k] += __uint_as_float(v[k]);
+        tmem_ld32(tmem + lane_base + uint32_t(pb) * kAccCols + uint32_t(64 * jh + 32), v);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) split_tf32(ls[8 * j + k], hi[k], lo[k]);
-        const uint32_t col = a_cols + uint32_t(kStageCols * bb + 16 * j);
-        tmem_st8(lane_base + col, hi);
-        tmem_st8(lane_base + col + 8, lo);
+        for (int k = 0; k < 32; ++k) sum[32 + k] += __uint_as_float(v[k]);
       }
-      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&full[bb]));
-      bb = bb + 1 == kABufs ? 0 : bb + 1;
+      if (pitem >= 0) {
+        if (!failed) {
+          float *dst = a.partial + size_t(pitem) * kTileFloats + m;
+#pragma unroll
+          for (int k = 0; k < 64; ++k) dst[size_t(64 * jh + k) * kM] = sum[k];
+        }
+#pragma unroll
+        for (int k = 0; k < 64; ++k) sum[k] = 0.f;
+      }
+      if (punit_end && nb >= 0 && !failed) stage_next((u + 1) & 1);
+    };
+
+    while (!failed) {
+      const int buf = u & 1;
+      const float *lpu = lp + buf * kLBuf;
+      item_at(a, cb, cur);
+      int y0, y1;
+      unit_rows(cur, cky, y0, y1);
+      const int ya = cky * kKY;
+      const int j_lo = cur.j_lo, j_hi = cur.j_hi;
+      const bool item_end = cky + 1 == cur.kb;
+      for (int sy = y0; sy < y1; sy += kSegRows) {
+        const int sy1 = sy + kSegRows < y1 ? sy + kSegRows : y1;
+        // take in the previous chain once this one is kABufs rows deep
+        // (its products are then done and the stages still hold work)
+        const int take_at = sy + kABufs - 1 < sy1 - 1 ? sy + kABufs - 1 : sy1 - 1;
+        for (int y = sy; y < sy1; ++y, ++g) {
+          const int s = g % kABufs;
+          if (g >= kABufs) {
+            if (!failed && !mbar_wait_bounded(smem_u32(&empty[s]), (epar >> s) & 1u)) failed = 1;
+            failed = __any_sync(~0u, failed);
+            epar ^= 1u << s;
+            fence_after_sync();
+          }
+          if (!failed) {
+            const float *ls = lpu + (y - y0) * kLRowF + m;
+#pragma unroll 1
+            for (int jj = 0; jj < 2; ++jj) {
+              const int j = jh + 2 * jj;
+              if (j < j_lo || j >= j_hi) continue;
+              uint32_t hi[8], lo[8];
+#pragma unroll
+              for (int k = 0; k < 8; ++k) split_tf32(ls[8 * j + k], hi[k], lo[k]);
+              const uint32_t col = a_cols + uint32_t(kStageCols * s + 16 * j);
+              tmem_st8(lane_base + col, hi);
+              tmem_st8(lane_base + col + 8, lo);
+            }
+          }
+          if (t == 0) {
+            // row n = (dyi, r) of B: right row y - dy0 - dyi at slot
+            // (ya + kKY - 1 - y) + dyi, n * 16 bytes past slot ya + kKY - 1 - y
+            info[s] = make_uint2(uint32_t(buf * kBBuf + (ya + kKY - 1 - y) * NR * 16),
+                                 uint32_t(j_lo) | (uint32_t(j_hi) << 4) |
+                                     ((seg & 1) ? kRecAcc : 0u) | (y == sy ? kRecFirst : 0u) |
+                                     (y == sy1 - 1 ? kRecLast : 0u));
+          }
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+          fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&full[s]));
+          if (y == take_at && pseg >= 0) take_in();
+        }
+        pseg = seg++;
+        const bool unit_end = sy1 == y1;
+        pitem = (unit_end && item_end) ? cb : -1;
+        punit_end = unit_end;
+      }
+      if (nb < 0) break;
+      cb = nb;
+      cky = nky;
+      advance();
+      ++u;
+      // the next unit's staged rows are in place for every builder
+      failed = builders_sync_or(failed);
     }
-    if (!failed && !mbar_wait_bounded(smem_u32(done), 0)) failed = 1;
+    if (pseg >= 0) {
+      nb = -1;
+      take_in();
+    }
+    // end of the row stream
+    const int s = g % kABufs;
+    if (g >= kABufs && !failed && !mbar_wait_bounded(smem_u32(&empty[s]), (epar >> s) & 1u))
+      failed = 1;
+    if (t == 0) info[s] = make_uint2(0u, kRecStop);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&full[s]));
   }
   failed = __syncthreads_or(failed);
-  fence_after_sync();
-
-  if (!failed && !issuer) {
-    // partial[unit][n][m]: warp w reads lanes 32 (w % 4) .. + 31 (rows m)
-    // and columns 64 (w / 4) .. + 63 (n); for each n the lanes write 32
-    // consecutive floats
-    const int q = warp & 3, half = warp >> 2;
-    float *dst = a.partial + size_t(blockIdx.x) * kTileFloats + 32 * q + lane;
-    const uint32_t lane_base = tmem + (uint32_t(32 * q) << 16);
-#pragma unroll 1
-    for (int j = 0; j < 2; ++j) {
-      const int c0 = 64 * half + 32 * j;
-      uint32_t v[32];
-      tmem_ld32(lane_base + uint32_t(c0), v);
-#pragma unroll
-      for (int k = 0; k < 32; ++k) dst[size_t(c0 + k) * kM] = __uint_as_float(v[k]);
-    }
-  } else if (failed && t == 0) {
-    atomicOr(&g_tcl_status, 1);
-  }
+  if (failed && t == 0) atomicOr(&g_tcl_status, 1);
   fence_before_sync();
   __syncthreads();
   if (issuer) {
@@ -321,8 +532,9 @@ __global__ void __launch_bounds__(kThreads + 32, 2) xcorr_tcl_kernel(const TclAr
   }
 }
 
-// out[l][r][oy][ox] = the sum, in unit order, of the partial tiles of the
-// units of its tile that hold any of its products.
+// out[l][r][oy][ox] = the sum, in a fixed order (row-unit group, then unit
+// column), of the partial tiles of its tile's CTAs that hold any of its
+// products.
 __global__ void __launch_bounds__(256) xcorr_tcl_sum_kernel(const TclArgs a) {
   const int ndy = 2 * a.H - 1, ndx = 2 * a.W - 1;
   const long long total = (long long)a.nl * a.nr * ndy * ndx;
@@ -339,16 +551,18 @@ __global__ void __launch_bounds__(256) xcorr_tcl_sum_kernel(const TclArgs a) {
     const int dxt = ox / kM, m = ox - dxt * kM;
     const int dyt = oy / a.ndy, dyi = oy - dyt * a.ndy;
     const int rt = r >> a.nr_log2, n = (dyi << a.nr_log2) + (r & (NR - 1));
-    const long long b0 = ((((long long)l * a.ndxt + dxt) * a.ndyt + dyt) * a.nrt + rt) * a.uy;
-    const Tile tl = tile_of(a, b0 * a.ux);
-    const int ky0 = tl.ylo / kKY, ky1 = (tl.yhi + kKY - 1) / kKY;
+    const long long b0 = ((((long long)l * a.ndxt + dxt) * a.ndyt + dyt) * a.nrt + rt) * a.ugn;
+    const Tile tl = tile_of(a, int(b0 * a.ux));
+    // groups holding a row unit in [ylo / kKY, ceil(yhi / kKY)), unit
+    // columns in [xlo / kKX, ceil(xhi / kKX)): every such CTA wrote its tile
+    const int kg0 = tl.ylo / kKY / a.ug, kg1 = ((tl.yhi + kKY - 1) / kKY - 1) / a.ug + 1;
     const int kx0 = tl.xlo / kKX, kx1 = (tl.xhi + kKX - 1) / kKX;
-    // units in order (ky, kx); loads in batches of 8 so that they are in
-    // flight together, the adds in the same fixed order
+    // loads in batches of 8 so that they are in flight together, the adds
+    // in the same fixed order
     float s = 0.f;
     const float *base = a.partial + size_t(n) * kM + m;
-    for (int ky = ky0; ky < ky1; ++ky) {
-      const float *row = base + ((b0 + ky) * a.ux) * size_t(kTileFloats);
+    for (int kg = kg0; kg < kg1; ++kg) {
+      const float *row = base + ((b0 + kg) * a.ux) * size_t(kTileFloats);
       for (int kx = kx0; kx < kx1; kx += 8) {
         float v[8];
 #pragma unroll
@@ -382,32 +596,42 @@ TclArgs make_args(const float *left, int nl, const float *right, int nr, int H, 
   a.nrt = (nr + (1 << a.nr_log2) - 1) >> a.nr_log2;
   a.uy = (H + kKY - 1) / kKY;
   a.ux = (W + kKX - 1) / kKX;
+  // row units per CTA: 1, else the smallest power of two (at most all of
+  // them) that keeps the partial tiles within kTargetScratch;
+  // CORR_XCORR_TCL_GROUP=n (read on every call) sets it to n instead
+  a.ug = 1;
+  while (a.ug < a.uy &&
+         (double)nl * a.ndxt * a.ndyt * a.nrt * ((a.uy + a.ug - 1) / a.ug) * a.ux * kTileFloats *
+                 sizeof(float) > double(kTargetScratch))
+    a.ug *= 2;
+  if (const char *v = getenv("CORR_XCORR_TCL_GROUP")) {
+    const int n = atoi(v);
+    if (n > 0) a.ug = n;
+  }
+  if (a.ug > a.uy) a.ug = a.uy;
+  a.ugn = (a.uy + a.ug - 1) / a.ug;
+  a.items = (long long)nl * a.ndxt * a.ndyt * a.nrt * a.ugn * a.ux;
   a.vec4 = (W % 4 == 0 && (reinterpret_cast<uintptr_t>(right) & 15) == 0) ? 1 : 0;
   return a;
-}
-
-long long units_of(const TclArgs &a) {
-  return (long long)a.nl * a.ndxt * a.ndyt * a.nrt * a.uy * a.ux;
 }
 
 }  // namespace
 
 size_t scratch_bytes(int nl, int nr, int H, int W) {
   const TclArgs a = make_args(nullptr, nl, nullptr, nr, H, W, nullptr);
-  return size_t(units_of(a)) * kTileFloats * sizeof(float);
+  return size_t(a.items) * kTileFloats * sizeof(float);
 }
 
 cudaError_t launch(const float *left, int nl, const float *right, int nr, int H, int W,
                    float *out, float *scratch, cudaStream_t stream) {
   TclArgs a = make_args(left, nl, right, nr, H, W, out);
   a.partial = scratch;
-  const long long units = units_of(a);
-  if (units > 0x7fffffffLL || scratch == nullptr) return cudaErrorInvalidValue;
-  const size_t smem = 2 * size_t(kMaxBEntries) * 16 + size_t(kKY) * kLRowF * sizeof(float) +
-                      (2 * kABufs + 2) * 8;
+  if (a.items > 0x7fffffffLL || scratch == nullptr) return cudaErrorInvalidValue;
   cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void *>(xcorr_tcl_kernel));
   if (e != cudaSuccess) return e;
-  xcorr_tcl_kernel<<<unsigned(units), kThreads + 32, smem, stream>>>(a);
+  // persistent: one CTA per SM (its shared memory and tensor memory fill one)
+  const long long ctas = a.items < device_sm_count() ? a.items : device_sm_count();
+  xcorr_tcl_kernel<<<unsigned(ctas), kThreads + 32, kSmemBytes, stream>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const long long outs = (long long)nl * nr * (2LL * H - 1) * (2LL * W - 1);
   const long long cap = 8LL * device_sm_count() * 8;

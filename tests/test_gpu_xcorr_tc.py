@@ -207,3 +207,97 @@ def test_tensor_core_kernels_write_nothing_outside_the_output(monkeypatch, mode,
     assert (buf[:pad] == 777.0).all() and (buf[-pad:] == 777.0).all()
     ref, ab = oracle.xcorr_f32(left, right, nthreads=NT)
     assert (np.abs(out.cpu().numpy().astype(np.float64) - ref) <= REL_TOL * ab + 1e-30).all()
+
+
+# Non-negative inputs: every product adds in the same direction, so the
+# tensor cores' truncating FP32 accumulation drifts with the number of
+# accumulates in a chain; the kernels keep chains to at most 96 and must
+# stay well inside the bar.
+
+def rand_pos(n, H, W):
+    return RNG.uniform(0, 1, size=(n, H, W)).astype(np.float32)
+
+
+@pytest.mark.parametrize("mode,shape", [
+    ("tc", (32, 64, 16, 16)), ("tcl", (1, 1, 256, 256)), ("tcl", (1, 128, 64, 64)),
+    ("tcl", (2, 3, 100, 130))])
+def test_nonnegative_inputs_well_inside_the_bar(monkeypatch, mode, shape):
+    monkeypatch.setenv("CORR_XCORR_TC", "1" if mode == "tc" else "0")
+    monkeypatch.setenv("CORR_XCORR_TCL", "1" if mode == "tcl" else "0")
+    nl, nr, H, W = shape
+    got, ref, ab = run_check(rand_pos(nl, H, W), rand_pos(nr, H, W))
+    assert (np.abs(got - ref) / (ab + 1e-30)).max() < 5e-6
+
+
+# Items of several row units (partial tiles shrink by that factor) --------
+
+@pytest.mark.parametrize("group,shape", [
+    (2, (1, 1, 200, 130)), (3, (2, 3, 100, 70)), (4, (1, 5, 150, 40)),
+    (64, (1, 2, 170, 90)), (5, (1, 1, 129, 257))])
+def test_tcl_row_unit_groups(tcl_on, monkeypatch, group, shape):
+    """Groups forced small (CORR_XCORR_TCL_GROUP) so that the oracle checks
+    every output: a ragged last group, groups that start above a tile's
+    first row, every row unit in one group; signed and non-negative."""
+    monkeypatch.setenv("CORR_XCORR_TCL_GROUP", str(group))
+    nl, nr, H, W = shape
+    run_check(rand(nl, H, W), rand(nr, H, W))
+    run_check(rand_pos(nl, H, W), rand_pos(nr, H, W))
+
+
+def line_sums(v, w):
+    """s[o] = sum_i v[i + o - (n - 1)] w[i] (n = len(v) = len(w)), in fp64:
+    the sum of the full cross-correlation of two matrices over one output
+    row (v, w their row sums) or column (their column sums)."""
+    return np.convolve(v.astype(np.float64), w.astype(np.float64)[::-1])
+
+
+def check_line_sums(left, right, got):
+    """Row and column sums of a pair's output against line_sums of the
+    matrices' row and column sums, within the parity bar summed over the
+    line (inputs non-negative, so sum |L*R| is the sum itself).  A partial
+    tile or a row unit left out moves some line sum by well over the bar."""
+    L, R = left[0].astype(np.float64), right[0].astype(np.float64)
+    g = got[0, 0]
+    rows = line_sums(L.sum(1), R.sum(1))
+    cols = line_sums(L.sum(0), R.sum(0))
+    for have, want in ((g.sum(1), rows), (g.sum(0), cols)):
+        bad = np.abs(have - want) > REL_TOL * want + 1e-9
+        assert not bad.any(), f"{bad.sum()} line sums out of tolerance, first at {np.argmax(bad)}"
+
+
+def test_line_sums_match_the_oracle():
+    left = RNG.uniform(0, 1, size=(1, 21, 34)).astype(np.float32)
+    right = RNG.uniform(0, 1, size=(1, 21, 34)).astype(np.float32)
+    ref, _ = oracle.xcorr_f32(left, right)
+    check_line_sums(left, right, ref)
+
+
+@pytest.mark.parametrize("n", [512, 1024])
+def test_tcl_large_pair(n):
+    """Default choice for one n x n pair (row-unit groups of 16 and 32): at
+    sampled outputs (every tile's corner rows and columns, plus random
+    ones) against the oracle, and every output row and column through its
+    sum."""
+    for v in ("CORR_XCORR_TCL", "CORR_XCORR_TC", "CORR_XCORR_WARP", "CORR_XCORR_TCL_GROUP"):
+        assert v not in os.environ
+    assert corr.xcorr_f32_kernel(1, 1, n, n) == "tensor_large"
+    rng = np.random.default_rng(4242 + n)
+    left = rng.uniform(0, 1, size=(1, n, n)).astype(np.float32)
+    right = rng.uniform(0, 1, size=(1, n, n)).astype(np.float32)
+    dev = torch.device("cuda", 0)
+    out = torch.full((1, 1, 2 * n - 1, 2 * n - 1), float("nan"), dtype=torch.float32,
+                     device=dev)
+    corr.xcorr_f32_into(torch.from_numpy(left).to(dev), torch.from_numpy(right).to(dev), out)
+    corr.device_status()
+    got = out.cpu().numpy()
+    assert np.isfinite(got).all()
+    edges = sorted({e for t in range(0, 2 * n - 1, 128) for e in (t, t + 127) if e < 2 * n - 1}
+                   | {2 * n - 2})
+    oy, ox = np.meshgrid(edges, edges, indexing="ij")
+    oy = np.concatenate([oy.ravel(), rng.integers(0, 2 * n - 1, 1500)])
+    ox = np.concatenate([ox.ravel(), rng.integers(0, 2 * n - 1, 1500)])
+    zeros = np.zeros(oy.size, np.int32)
+    want, ab = oracle.xcorr_f32_at(left, right, zeros, zeros, oy, ox)
+    have = got[0, 0, oy, ox].astype(np.float64)
+    assert (np.abs(have - want) <= REL_TOL * ab + 1e-30).all()
+    check_line_sums(left, right, got)
