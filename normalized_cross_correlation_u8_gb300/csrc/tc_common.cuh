@@ -32,10 +32,15 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
          (uint64_t((sbo & 0x3FFFFu) >> 4) << 32) | (uint64_t(1) << 46);
 }
 
+// v rounded to TF32 (10 explicit mantissa bits), to nearest with ties away
+// from zero, as an FP32 bit pattern with the low 13 bits clear: adding half
+// of the dropped unit (bit 12) to the sign-magnitude pattern carries into
+// the kept bits exactly when the dropped part is at least half, and a
+// carry out of the mantissa moves to the next binade (or to infinity) as
+// rounding does.  Integer ALU work only; the same bits as cvt.rna.tf32.f32
+// for every finite v and for infinities.
 __device__ __forceinline__ uint32_t tf32_rna(float v) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v));
-  return r;
+  return (__float_as_uint(v) + 0x1000u) & 0xFFFFE000u;
 }
 
 // v = hi + lo (+ a remainder below 2^-22 |v|), hi and lo TF32 bit patterns.
@@ -60,6 +65,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, letting the hardware suspend the thread for up to
+// `ns` nanoseconds while the phase is incomplete (it resumes as soon as the
+// phase completes), so that a waiting warp takes no issue slots from the
+// warps that share its scheduler.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for phase `parity` of the barrier to complete; false after about a
 // second without it.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
@@ -68,6 +89,32 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
   while (!mbar_try_wait(bar, parity))
     if (clock64() - t0 > kWaitCycles) return false;
   return true;
+}
+
+// mbar_wait_bounded for threads whose waits should leave the scheduler to
+// others: each try suspends the thread for up to 20 us.
+__device__ __forceinline__ bool mbar_wait_bounded_sleep(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait_sleep(bar, parity, 20000u))
+    if (clock64() - t0 > kWaitCycles) return false;
+  return true;
+}
+
+// Three tcgen05.mma kind::tf32 with A in tensor memory into one FP32
+// accumulator: A a0 x B b0 (accumulating unless first == 0), A a0 x B b1,
+// A a1 x B b0 -- hi*hi, hi*lo and lo*hi of one K step.
+__device__ __forceinline__ void mma3_tf32_ta(uint32_t d, uint32_t a0, uint32_t a1, uint64_t b0,
+                                             uint64_t b1, uint32_t first, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "setp.eq.b32 q, %5, %5;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %3, %5, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %4, %5, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%2], %3, %5, q;\n\t}"
+      ::"r"(d), "r"(a0), "r"(a1), "l"(b0), "l"(b1), "r"(idesc), "r"(first)
+      : "memory");
 }
 
 __device__ __forceinline__ void fence_before_sync() {

@@ -1091,8 +1091,9 @@ namespace {
 // Which kernel a shape takes, its arguments and the split-row scratch it needs.
 enum class XKind { Tiny, Bcast, Rows, Tc, Warp, Tcl };
 
-// Largest partial-sum scratch the larger-matrix tensor-core kernel may take.
-constexpr size_t kMaxTclScratch = size_t(512) << 20;
+// Largest scratch the larger-matrix tensor-core kernel may take: 512 MB of
+// partial tiles and its item counter.
+constexpr size_t kMaxTclScratch = (size_t(512) << 20) + 256;
 
 // Whether a shape takes the larger-matrix tensor-core kernel (xcorr_tcl.cu):
 // CORR_XCORR_TCL (read on every call) "1" / "0" forces it on / off where it

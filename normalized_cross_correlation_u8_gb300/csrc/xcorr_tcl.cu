@@ -13,11 +13,12 @@
 // one-to-one, 32 shifts x 4 rights for one-to-many).  Its K -- every row y
 // and column x' that some shift of the tile reaches -- is cut into units of
 // 32 rows x 32 columns.  An item is one tile's unit column and a group of G
-// consecutive row units (G = 1 up to about 256 x 256, more for larger
-// matrices so that the partial tiles stay within 64 MB).  The kernel is
-// persistent, one CTA per SM taking items in turn; each item's 128 x 128
-// partial sums go to scratch memory and a second kernel adds those of each
-// tile in a fixed order (the result does not depend on scheduling).
+// consecutive row units (G = 4 where the matrix has that many, more for
+// larger matrices so that the partial tiles stay within 128 MB).  The
+// kernel is persistent, one CTA per SM claiming items in turn; each item's
+// 128 x 128 partial sums go to scratch memory and a second kernel adds
+// those of each tile in a fixed order (the result does not depend on
+// scheduling).
 //
 // Accuracy: the tensor cores accumulate FP32 with truncation, so on inputs
 // of one sign the error of a chain of accumulates grows with its length
@@ -53,7 +54,7 @@ namespace {
 
 using namespace tcx;
 
-constexpr int kThreads = 256;             // builder threads (8 warps)
+constexpr int kThreads = 512;             // builder threads (16 warps)
 constexpr int kM = 128;                   // shifts dx of one left
 constexpr int kN = 128;                   // (shift dy, right) slots
 constexpr int kKY = 32;                   // overlap rows per unit
@@ -71,23 +72,27 @@ constexpr int kMaxBEntries = 8 * (kKY + 32 - 1) * 4;   // NR = 4: the largest B
 constexpr int kBHalf = kMaxBEntries * 16; // bytes of the hi (or lo) parts of one B
 constexpr int kBBuf = 2 * kBHalf;         // one staged B (hi, then lo)
 constexpr int kTileFloats = kM * kN;      // one partial tile
-constexpr size_t kTargetScratch = size_t(64) << 20;   // partial tiles, when row groups allow
+constexpr size_t kTargetScratch = size_t(128) << 20;  // partial tiles, when row groups allow
 constexpr uint32_t kIdesc = idesc_tf32(kM, kN);
 static_assert(8 * kMaxSlots * 1 <= kMaxBEntries && 8 * (kKY + 64 - 1) * 2 <= kMaxBEntries,
               "B staging holds every right-tile shape");
 static_assert(2 * kAccCols + kABufs * kStageCols == kTmemCols, "tensor memory plan");
 static_assert(kKY % kSegRows == 0, "chains never cross a unit");
 
-// shared memory: two staged B, two units' left rows, the row records the
-// builders pass to the issuer, the mbarriers and the tensor-memory address
-constexpr size_t kLpOff = 2 * size_t(kBBuf);
+// shared memory: two staged B (TF32 hi / lo), the raw rows of the B after
+// them (as copied), two units' left rows, the row records the builders
+// pass to the issuer, the mbarriers, two claimed-item slots and the
+// tensor-memory address
+constexpr size_t kRawOff = 2 * size_t(kBBuf);
+constexpr size_t kLpOff = kRawOff + size_t(kBHalf);
 constexpr size_t kInfoOff = kLpOff + 2 * size_t(kLBuf) * sizeof(float);
 constexpr size_t kBarOff = kInfoOff + kABufs * sizeof(uint2);
 constexpr int kBars = 2 * kABufs + 3;    // full, empty, chain done x 2, done
-constexpr size_t kSmemBytes = kBarOff + kBars * 8 + 16;
+constexpr size_t kClaimOff = kBarOff + kBars * 8;
+constexpr size_t kSmemBytes = kClaimOff + 2 * sizeof(int) + 16;
 
-// row record flags (second word): K steps [j_lo, j_hi), accumulator, first
-// and last row of a chain, end of the CTA's work
+// row record flags (second word): accumulator, first and last row of a
+// chain, end of the CTA's work
 constexpr uint32_t kRecAcc = 1u << 8, kRecFirst = 1u << 9, kRecLast = 1u << 10,
                    kRecStop = 1u << 11;
 
@@ -103,6 +108,7 @@ struct TclArgs {
   int uy, ux;            // units along rows, columns of K
   int ug, ugn;           // row units per item, groups of them along the rows
   long long items;       // work items: tiles x ugn x ux (below 2^31 at launch)
+  int *counter;          // items claimed so far (zero at launch)
   int vec4;              // rows readable as float4
 };
 
@@ -141,11 +147,11 @@ __device__ __forceinline__ Tile tile_of(const TclArgs &a, int b) {
 }
 
 // An item: one tile's unit column kx and its row units [ka, kb) that hold
-// rows of the tile; K steps [j_lo, j_hi) of the columns it reaches.
+// rows of the tile; empty when the column holds none that the tile reaches.
 struct Item {
   int b;                 // -1: none
   int l, dx0, dy0, r0, ylo, yhi;
-  int xa, ka, kb, j_lo, j_hi;
+  int xa, ka, kb;
 };
 
 __device__ __forceinline__ bool item_at(const TclArgs &a, int b, Item &it) {
@@ -163,16 +169,18 @@ __device__ __forceinline__ bool item_at(const TclArgs &a, int b, Item &it) {
   const int kvlo = tl.ylo / kKY, kvhi = (tl.yhi + kKY - 1) / kKY;
   it.ka = tl.kg * a.ug > kvlo ? tl.kg * a.ug : kvlo;
   it.kb = (tl.kg + 1) * a.ug < kvhi ? (tl.kg + 1) * a.ug : kvhi;
-  it.j_lo = (x0 - it.xa) >> 3;
-  it.j_hi = (x1 - it.xa + 7) >> 3;
   return it.ka < it.kb && x0 < x1;
 }
 
-// The first item from b on, in steps of the grid, that holds products.
-__device__ __forceinline__ void first_item(const TclArgs &a, int b, Item &it) {
-  for (; b < a.items; b += int(gridDim.x))
-    if (item_at(a, b, it)) return;
-  it.b = -1;
+// Claim the next item that holds products (one thread): items go out in
+// index order from the counter; -1 once none is left.
+__device__ __forceinline__ int claim_item(const TclArgs &a) {
+  for (;;) {
+    const int c = atomicAdd(a.counter, 1);
+    if (c >= a.items) return -1;
+    Item it;
+    if (item_at(a, c, it)) return c;
+  }
 }
 
 // Rows of unit ky of an item: [max(ky kKY, ylo), min(ky kKY + kKY, yhi)).
@@ -182,81 +190,96 @@ __device__ __forceinline__ void unit_rows(const Item &it, int ky, int &y0, int &
   y1 = ya + kKY < it.yhi ? ya + kKY : it.yhi;
 }
 
-// Stage unit ky of an item: B entry e = (xc, slot, r) -> R[r0 + r][yr][xa +
-// 4 xc .. + 3] with yr = ya + kKY - 1 - dy0 - slot, as TF32 hi (bb) and lo
-// (bb + kBHalf), consecutive 16-byte rows; the left's rows y0 .. y1 - 1,
-// columns xa + dx0 .. + kLRowF - 1: lpu[y - y0][p] = L[l][y][xa + dx0 + p]
-// (zero outside the matrices).
-__device__ __forceinline__ void stage_unit(const TclArgs &a, const Item &it, int ky, uint8_t *bb,
-                                           float *lpu, int t, int NS) {
+// Asynchronous copies global -> shared (cp.async); `ok` false writes zeros
+// (nothing is read).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool ok) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(ok ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, bool ok) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src),
+               "r"(ok ? 4 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
+// Copy the right rows of unit ky of an item: raw entry e = (xc, slot, r)
+// <- R[r0 + r][yr][xa + 4 xc .. + 3] with yr = ya + kKY - 1 - dy0 - slot
+// (zero outside the matrix), 16 bytes each.  Thread t takes the entries
+// t + k kThreads, as in convert_b.
+__device__ __forceinline__ void copy_b_raw(const TclArgs &a, const Item &it, int ky,
+                                           uint32_t raw, int t, int NS) {
   const int H = a.H, W = a.W, NR = 1 << a.nr_log2;
-  const int ya = ky * kKY;
-  int y0, y1;
-  unit_rows(it, ky, y0, y1);
-  // (two batches each, to bound the registers held: the builders keep
-  // their running sums live across this)
-  {
-    const int nl_ent = (y1 - y0) * kLRowF;
-    constexpr int kLPer = (kLBuf + 2 * kThreads - 1) / (2 * kThreads);
-    const float *lrow = a.left + size_t(it.l) * H * W;
-    const int xb = it.xa + it.dx0;
-#pragma unroll 1
-    for (int h = 0; h < 2; ++h) {
-      float lv[kLPer];
+  const int nent = 8 * NS * NR;
+  const int yc = ky * kKY + kKY - 1 - it.dy0;
+  constexpr int kPer = (kMaxBEntries + kThreads - 1) / kThreads;
+#pragma unroll 2
+  for (int k = 0; k < kPer; ++k) {
+    const int e = t + k * kThreads;
+    if (e >= nent) break;
+    const int r = e & (NR - 1), qq = e >> a.nr_log2;
+    const int sl = qq % NS, xc = qq / NS;
+    const int yr = yc - sl, rr = it.r0 + r, x = it.xa + 4 * xc;
+    const bool row_ok = rr < a.nr && yr >= 0 && yr < H;
+    const float *src = row_ok ? a.right + (size_t(rr) * H + yr) * W + x : a.right;
+    const uint32_t dst = raw + uint32_t(e) * 16;
+    if (a.vec4) {
+      cp_async16(dst, row_ok && x < W ? src : a.right, row_ok && x < W);
+    } else {
 #pragma unroll
-      for (int k = 0; k < kLPer; ++k) {
-        const int i = t + (h * kLPer + k) * kThreads;
-        const int p = i % kLRowF, ry = i / kLRowF;
-        const int x = xb + p;
-        lv[k] = 0.f;
-        if (i < nl_ent && x >= 0 && x < W) lv[k] = __ldg(lrow + size_t(y0 + ry) * W + x);
-      }
-#pragma unroll
-      for (int k = 0; k < kLPer; ++k) {
-        const int i = t + (h * kLPer + k) * kThreads;
-        if (i < nl_ent) lpu[i] = lv[k];
+      for (int c = 0; c < 4; ++c) {
+        const bool ok = row_ok && x + c < W;
+        cp_async4(dst + 4 * c, ok ? src + c : a.right, ok);
       }
     }
   }
-  const int nent = 8 * NS * NR;
-  const int yc = ya + kKY - 1 - it.dy0;
-  constexpr int kPer = (kMaxBEntries + 2 * kThreads - 1) / (2 * kThreads);
-#pragma unroll 1
-  for (int h = 0; h < 2; ++h) {
-    float4 bv[kPer];
+}
+
+// Copy the left's rows y0 .. y1 - 1 of unit ky, columns xa + dx0 .. +
+// kLRowF - 1: lpu[y - y0][p] <- L[l][y][xa + dx0 + p] (zero outside the
+// matrix).
+__device__ __forceinline__ void copy_lp(const TclArgs &a, const Item &it, int ky, uint32_t lpu,
+                                        int t) {
+  const int H = a.H, W = a.W;
+  int y0, y1;
+  unit_rows(it, ky, y0, y1);
+  const int nl_ent = (y1 - y0) * kLRowF;
+  const float *lrow = a.left + size_t(it.l) * H * W;
+  const int xb = it.xa + it.dx0;
+  constexpr int kPer = (kLBuf + kThreads - 1) / kThreads;
+#pragma unroll 4
+  for (int k = 0; k < kPer; ++k) {
+    const int i = t + k * kThreads;
+    if (i >= nl_ent) break;
+    const int p = i % kLRowF, ry = i / kLRowF;
+    const int x = xb + p;
+    const bool ok = x >= 0 && x < W;
+    cp_async4(lpu + uint32_t(i) * 4, ok ? lrow + size_t(y0 + ry) * W + x : a.left, ok);
+  }
+}
+
+// B entries t + k kThreads of this thread's (landed) raw copies, split into
+// TF32 hi (bb) and lo (bb + kBHalf).
+__device__ __forceinline__ void convert_b(const uint8_t *raw, uint8_t *bb, int t, int nent) {
+  constexpr int kPer = (kMaxBEntries + kThreads - 1) / kThreads;
 #pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const int e = t + (h * kPer + k) * kThreads;
-      bv[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (e < nent) {
-        const int r = e & (NR - 1), qq = e >> a.nr_log2;
-        const int sl = qq % NS, xc = qq / NS;
-        const int yr = yc - sl, rr = it.r0 + r, x = it.xa + 4 * xc;
-        if (rr < a.nr && yr >= 0 && yr < H && x < W) {
-          const float *src = a.right + (size_t(rr) * H + yr) * W + x;
-          if (a.vec4) {
-            bv[k] = __ldg(reinterpret_cast<const float4 *>(src));
-          } else {
-            bv[k].x = __ldg(src);
-            if (x + 1 < W) bv[k].y = __ldg(src + 1);
-            if (x + 2 < W) bv[k].z = __ldg(src + 2);
-            if (x + 3 < W) bv[k].w = __ldg(src + 3);
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const int e = t + (h * kPer + k) * kThreads;
-      if (e >= nent) break;
-      uint4 hi, lo;
-      split_tf32(bv[k].x, hi.x, lo.x);
-      split_tf32(bv[k].y, hi.y, lo.y);
-      split_tf32(bv[k].z, hi.z, lo.z);
-      split_tf32(bv[k].w, hi.w, lo.w);
-      *reinterpret_cast<uint4 *>(bb + e * 16) = hi;
-      *reinterpret_cast<uint4 *>(bb + kBHalf + e * 16) = lo;
-    }
+  for (int k = 0; k < kPer; ++k) {
+    const int e = t + k * kThreads;
+    if (e >= nent) break;
+    const float4 v = *reinterpret_cast<const float4 *>(raw + e * 16);
+    uint4 hi, lo;
+    split_tf32(v.x, hi.x, lo.x);
+    split_tf32(v.y, hi.y, lo.y);
+    split_tf32(v.z, hi.z, lo.z);
+    split_tf32(v.w, hi.w, lo.w);
+    *reinterpret_cast<uint4 *>(bb + e * 16) = hi;
+    *reinterpret_cast<uint4 *>(bb + kBHalf + e * 16) = lo;
   }
   // generic-proxy stores -> the tensor cores' (async proxy) reads
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -276,29 +299,32 @@ __device__ __forceinline__ int builders_sync_or(int v) {
   return r;
 }
 
-// Persistent: CTA c takes the items c, c + grid, ... that hold products.
-// Its row stream (every row of every unit of those items) runs through
-// kABufs A stages; each chain of up to kSegRows rows of one unit
-// accumulates in one of two accumulators (the tensor cores' FP32
-// accumulation truncates, so a chain stays short: at most 96 updates), and
-// the builders add the finished chain into an FP32 running sum of the item
-// held in registers (thread: accumulator row 32 (warp % 4) + lane, columns
-// 64 (warp / 4) .. + 63), while the next chain runs in the other
-// accumulator.  At the end of an item the running sum goes to its partial
-// tile.
+// Persistent: each CTA claims items in turn (a counter in scratch memory)
+// and runs their units as one row stream through kABufs A stages; each
+// chain of up to kSegRows rows of one unit accumulates in one of two
+// accumulators (the tensor cores' FP32 accumulation truncates, so a chain
+// stays short: at most 96 updates), and the builders add the finished
+// chain into an FP32 running sum of the item held in registers (thread:
+// accumulator row 32 (warp % 4) + lane, columns 32 (warp / 4) .. + 31)
+// while the next chain runs in the other accumulator.  At the end of an
+// item the running sum goes to its partial tile.
+//
+// Staging runs two units ahead: during unit u the builders turn the raw
+// rows of unit u + 1 (copied during unit u - 1) into its TF32 B and start
+// the asynchronous copies of unit u + 2's raw rows and unit u + 1's left
+// rows, into the buffers unit u - 1 has just released.
 __global__ void __launch_bounds__(kThreads + 32, 1) xcorr_tcl_kernel(const TclArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t *raw = smem + kRawOff;
   float *lp = reinterpret_cast<float *>(smem + kLpOff);                  // [2][kLBuf]
   uint2 *info = reinterpret_cast<uint2 *>(smem + kInfoOff);             // [kABufs]
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + kBarOff);        // [kABufs]
   uint64_t *empty = full + kABufs;                                       // [kABufs]
   uint64_t *chain = empty + kABufs;                                      // [2]
   uint64_t *done = chain + 2;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
+  int *claimed = reinterpret_cast<int *>(smem + kClaimOff);             // [2]
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(claimed + 2);
 
-  Item cur;
-  first_item(a, int(blockIdx.x), cur);
-  if (cur.b < 0) return;                       // no products for this CTA
   const int NR = 1 << a.nr_log2, NS = kKY + a.ndy - 1;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const bool issuer = warp == kThreads / 32;
@@ -330,8 +356,12 @@ __global__ void __launch_bounds__(kThreads + 32, 1) xcorr_tcl_kernel(const TclAr
 
   if (issuer) {
     if (lane == 0) {
-      const uint32_t b_base = smem_u32(smem);
       const uint32_t lbo_b = uint32_t(NS * NR * 16);     // next 4 columns x'
+      // descriptor of B at the start of shared memory; a row's descriptors
+      // add their byte offset / 16 to its address field (addresses stay
+      // below 2^18, so nothing carries out of it)
+      const uint64_t desc0 = smem_desc(smem_u32(smem), lbo_b, 128);
+      const uint64_t step_j = uint64_t((2 * lbo_b) >> 4), to_lo = uint64_t(kBHalf >> 4);
       int g = 0;
       for (;; ++g) {
         const int s = g % kABufs;
@@ -342,20 +372,17 @@ __global__ void __launch_bounds__(kThreads + 32, 1) xcorr_tcl_kernel(const TclAr
         fence_after_sync();
         const uint2 rec = info[s];
         if (rec.y & kRecStop) break;
-        const int j_lo = rec.y & 15, j_hi = (rec.y >> 4) & 15;
+        // all kSteps K steps, straight-line (a branch between tcgen05.mma
+        // issues slows them well below the tensor pipe's rate): columns x'
+        // no shift of the tile reaches meet left values staged as zero
         const uint32_t d = tmem + ((rec.y & kRecAcc) ? kAccCols : 0u);
         const uint32_t ab = a_cols + uint32_t(kStageCols * s);
+        const uint64_t bhi = desc0 + uint64_t(rec.x >> 4);
+        mma3_tf32_ta(d, ab, ab + 8, bhi, bhi + to_lo, (rec.y & kRecFirst) ? 0u : 1u, kIdesc);
 #pragma unroll
-        for (int j = 0; j < kSteps; ++j) {
-          if (j < j_lo || j >= j_hi) continue;
-          const uint32_t boff = b_base + rec.x + uint32_t(2 * j) * lbo_b;
-          const uint64_t bhi = smem_desc(boff, lbo_b, 128);
-          const uint64_t blo = smem_desc(boff + kBHalf, lbo_b, 128);
-          const uint32_t acc = ((rec.y & kRecFirst) && j == j_lo) ? 0u : 1u;
-          mma_tf32_ta(d, ab + 16 * j, bhi, acc, kIdesc);
-          mma_tf32_ta(d, ab + 16 * j, blo, 1u, kIdesc);
-          mma_tf32_ta(d, ab + 16 * j + 8, bhi, 1u, kIdesc);
-        }
+        for (int j = 1; j < kSteps; ++j)
+          mma3_tf32_ta(d, ab + 16 * j, ab + 16 * j + 8, bhi + j * step_j, bhi + j * step_j + to_lo,
+                       1u, kIdesc);
         mma_commit(smem_u32(&empty[s]));
         if (rec.y & kRecLast) mma_commit(smem_u32(&chain[(rec.y & kRecAcc) ? 1 : 0]));
       }
@@ -370,40 +397,83 @@ __global__ void __launch_bounds__(kThreads + 32, 1) xcorr_tcl_kernel(const TclAr
     }
   } else {
     // thread: A row m = 32 q + lane (shift dx = dx0 + m) with q = warp % 4,
-    // K steps j = jh and jh + 2 (jh = warp / 4): the 8 values L[l][y][x' +
-    // dx], x' = xa + 8j .. + 7, as TF32 hi and lo; accumulator columns
-    // 64 jh .. + 63 of row m
+    // K step jh = warp / 4: the 8 values L[l][y][x' + dx], x' = xa + 8 jh ..
+    // + 7, as TF32 hi and lo; accumulator columns 32 jh .. + 31 of row m
     const int q = warp & 3, jh = warp >> 2;
     const int m = 32 * q + lane;
     const uint32_t lane_base = uint32_t(32 * q) << 16;
-    float sum[64];
+    const int nent = 8 * NS * NR;
+    const uint32_t raw_u32 = smem_u32(raw), lp_u32 = smem_u32(lp);
+    float sum[32];
 #pragma unroll
-    for (int k = 0; k < 64; ++k) sum[k] = 0.f;
+    for (int k = 0; k < 32; ++k) sum[k] = 0.f;
 
-    // the current unit (item cb, row unit cky) and the one after it (nb,
-    // nky; nb < 0: none); item geometry is recomputed where it is needed
-    int cb = cur.b, nb;
-    int cky = cur.ka, nky;
-    auto advance = [&]() {
+    // The unit ring: the current unit (item cb, row unit cky), the next
+    // (b1, ky1) and the one after (b2, ky2); item -1: none.  The unit after
+    // (b, ky) is (b, ky + 1) within the item, else the first unit of the
+    // item thread 0 claimed into claimed[slot] before the last barrier.
+    auto is_item_end = [&](int b, int ky) {
       Item it;
-      item_at(a, cb, it);
-      if (cky + 1 < it.kb) {
-        nb = cb;
-        nky = cky + 1;
-      } else {
-        first_item(a, cb + int(gridDim.x), it);
-        nb = it.b;
-        nky = it.ka;
+      item_at(a, b, it);
+      return ky + 1 >= it.kb;
+    };
+    auto successor = [&](int b, int ky, int slot, int &ob, int &oky) {
+      ob = -1;
+      oky = 0;
+      if (b < 0) return;
+      Item it;
+      item_at(a, b, it);
+      if (ky + 1 < it.kb) {
+        ob = b;
+        oky = ky + 1;
+        return;
+      }
+      ob = claimed[slot];
+      if (ob >= 0) {
+        item_at(a, ob, it);
+        oky = it.ka;
       }
     };
-    auto stage_next = [&](int buf) {
+    int cb, cky = 0, b1, ky1, b2, ky2;
+    if (t == 0) claimed[0] = claim_item(a);
+    failed = builders_sync_or(failed);
+    cb = claimed[0];
+    if (cb >= 0) {
       Item it;
-      item_at(a, nb, it);
-      stage_unit(a, it, nky, smem + buf * kBBuf, lp + buf * kLBuf, t, NS);
-    };
-    advance();
-    stage_unit(a, cur, cky, smem, lp, t, NS);
-    if (nb >= 0) stage_next(1);
+      item_at(a, cb, it);
+      cky = it.ka;
+    }
+    if (t == 0 && cb >= 0 && is_item_end(cb, cky)) claimed[1] = claim_item(a);
+    failed = builders_sync_or(failed);
+    successor(cb, cky, 1, b1, ky1);
+    if (t == 0 && b1 >= 0 && is_item_end(b1, ky1)) claimed[0] = claim_item(a);
+    failed = builders_sync_or(failed);
+    successor(b1, ky1, 0, b2, ky2);
+    // the first two units' B and the first unit's left rows; then the copies
+    // of the third unit's raw rows and the second unit's left rows
+    if (cb >= 0) {
+      Item it;
+      item_at(a, cb, it);
+      copy_b_raw(a, it, cky, raw_u32, t, NS);
+      copy_lp(a, it, cky, lp_u32, t);
+      cp_async_commit();
+      cp_async_wait_all();
+      convert_b(raw, smem, t, nent);
+      if (b1 >= 0) {
+        item_at(a, b1, it);
+        copy_b_raw(a, it, ky1, raw_u32, t, NS);
+        cp_async_commit();
+        cp_async_wait_all();
+        convert_b(raw, smem + kBBuf, t, nent);
+        if (b2 >= 0) {
+          Item i2;
+          item_at(a, b2, i2);
+          copy_b_raw(a, i2, ky2, raw_u32, t, NS);
+        }
+        copy_lp(a, it, ky1, lp_u32 + uint32_t(kLBuf) * 4, t);
+        cp_async_commit();
+      }
+    }
     failed = builders_sync_or(failed);
 
     // the chain whose sum is still to be taken in
@@ -414,45 +484,54 @@ __global__ void __launch_bounds__(kThreads + 32, 1) xcorr_tcl_kernel(const TclAr
     uint32_t epar = 0;
 
     // Take in chain pseg: wait for its products, add its accumulator to the
-    // running sum; at the end of an item store the sum; at the end of a
-    // unit, stage the unit after the current one into the buffers that
-    // unit used.
+    // running sum; at the end of an item store the sum.  At the end of a
+    // unit (its products all done, its buffers free): turn unit u + 1's
+    // raw rows into B and start the copies of unit u + 2's raw rows and
+    // unit u + 1's left rows.
     auto take_in = [&]() {
       const int pb = pseg & 1;
-      if (!failed && !mbar_wait_bounded(smem_u32(&chain[pb]), uint32_t(pseg >> 1) & 1u))
+      if (!failed && !mbar_wait_bounded_sleep(smem_u32(&chain[pb]), uint32_t(pseg >> 1) & 1u))
         failed = 1;
       failed = __any_sync(~0u, failed);     // the warp's .aligned steps stay together
       fence_after_sync();
       if (!failed) {
         uint32_t v[32];
-        tmem_ld32(tmem + lane_base + uint32_t(pb) * kAccCols + uint32_t(64 * jh), v);
+        tmem_ld32(tmem + lane_base + uint32_t(pb) * kAccCols + uint32_t(32 * jh), v);
 #pragma unroll
         for (int k = 0; k < 32; ++k) sum[k] += __uint_as_float(v[k]);
-        tmem_ld32(tmem + lane_base + uint32_t(pb) * kAccCols + uint32_t(64 * jh + 32), v);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) sum[32 + k] += __uint_as_float(v[k]);
       }
       fence_before_sync();
       if (pitem >= 0) {
         if (!failed) {
           float *dst = a.partial + size_t(pitem) * kTileFloats + m;
 #pragma unroll
-          for (int k = 0; k < 64; ++k) dst[size_t(64 * jh + k) * kM] = sum[k];
+          for (int k = 0; k < 32; ++k) dst[size_t(32 * jh + k) * kM] = sum[k];
         }
 #pragma unroll
-        for (int k = 0; k < 64; ++k) sum[k] = 0.f;
+        for (int k = 0; k < 32; ++k) sum[k] = 0.f;
       }
-      if (punit_end && nb >= 0 && !failed) stage_next((u + 1) & 1);
+      if (punit_end && b1 >= 0 && !failed) {
+        const int nbuf = (u + 1) & 1;
+        convert_b(raw, smem + nbuf * kBBuf, t, nent);
+        Item it;
+        if (b2 >= 0) {
+          item_at(a, b2, it);
+          copy_b_raw(a, it, ky2, raw_u32, t, NS);
+        }
+        item_at(a, b1, it);
+        copy_lp(a, it, ky1, lp_u32 + uint32_t(nbuf * kLBuf) * 4, t);
+        cp_async_commit();
+      }
     };
 
-    while (!failed) {
+    while (cb >= 0) {
       const int buf = u & 1;
       const float *lpu = lp + buf * kLBuf;
+      Item cur;
       item_at(a, cb, cur);
       int y0, y1;
       unit_rows(cur, cky, y0, y1);
       const int ya = cky * kKY;
-      const int j_lo = cur.j_lo, j_hi = cur.j_hi;
       const bool item_end = cky + 1 == cur.kb;
       for (int sy = y0; sy < y1; sy += kSegRows) {
         const int sy1 = sy + kSegRows < y1 ? sy + kSegRows : y1;
@@ -462,31 +541,26 @@ __global__ void __launch_bounds__(kThreads + 32, 1) xcorr_tcl_kernel(const TclAr
         for (int y = sy; y < sy1; ++y, ++g) {
           const int s = g % kABufs;
           if (g >= kABufs) {
-            if (!failed && !mbar_wait_bounded(smem_u32(&empty[s]), (epar >> s) & 1u)) failed = 1;
+            if (!failed && !mbar_wait_bounded_sleep(smem_u32(&empty[s]), (epar >> s) & 1u))
+              failed = 1;
             failed = __any_sync(~0u, failed);
             epar ^= 1u << s;
             fence_after_sync();
           }
           if (!failed) {
-            const float *ls = lpu + (y - y0) * kLRowF + m;
-#pragma unroll 1
-            for (int jj = 0; jj < 2; ++jj) {
-              const int j = jh + 2 * jj;
-              if (j < j_lo || j >= j_hi) continue;
-              uint32_t hi[8], lo[8];
+            const float *ls = lpu + (y - y0) * kLRowF + m + 8 * jh;
+            uint32_t hi[8], lo[8];
 #pragma unroll
-              for (int k = 0; k < 8; ++k) split_tf32(ls[8 * j + k], hi[k], lo[k]);
-              const uint32_t col = a_cols + uint32_t(kStageCols * s + 16 * j);
-              tmem_st8(lane_base + col, hi);
-              tmem_st8(lane_base + col + 8, lo);
-            }
+            for (int k = 0; k < 8; ++k) split_tf32(ls[k], hi[k], lo[k]);
+            const uint32_t col = a_cols + uint32_t(kStageCols * s + 16 * jh);
+            tmem_st8(lane_base + col, hi);
+            tmem_st8(lane_base + col + 8, lo);
           }
           if (t == 0) {
             // row n = (dyi, r) of B: right row y - dy0 - dyi at slot
             // (ya + kKY - 1 - y) + dyi, n * 16 bytes past slot ya + kKY - 1 - y
             info[s] = make_uint2(uint32_t(buf * kBBuf + (ya + kKY - 1 - y) * NR * 16),
-                                 uint32_t(j_lo) | (uint32_t(j_hi) << 4) |
-                                     ((seg & 1) ? kRecAcc : 0u) | (y == sy ? kRecFirst : 0u) |
+                                 ((seg & 1) ? kRecAcc : 0u) | (y == sy ? kRecFirst : 0u) |
                                      (y == sy1 - 1 ? kRecLast : 0u));
           }
           asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
@@ -500,18 +574,25 @@ __global__ void __launch_bounds__(kThreads + 32, 1) xcorr_tcl_kernel(const TclAr
         pitem = (unit_end && item_end) ? cb : -1;
         punit_end = unit_end;
       }
-      if (nb < 0) break;
-      cb = nb;
-      cky = nky;
-      advance();
+      // next unit: claim the item after the ring's last unit if it needs
+      // one; this thread's copies of the next unit's left rows (and the
+      // raw rows after it) have landed; then everyone's have
       ++u;
-      // the next unit's staged rows are in place for every builder
+      if (t == 0 && b2 >= 0 && is_item_end(b2, ky2)) claimed[u & 1] = claim_item(a);
+      cp_async_wait_all();
       failed = builders_sync_or(failed);
+      if (failed) break;
+      cb = b1;
+      cky = ky1;
+      b1 = b2;
+      ky1 = ky2;
+      successor(b1, ky1, u & 1, b2, ky2);
     }
     if (pseg >= 0) {
-      nb = -1;
+      b1 = -1;
       take_in();
     }
+    cp_async_wait_all();                 // no copy in flight when the CTA ends
     // end of the row stream
     const int s = g % kABufs;
     if (g >= kABufs && !failed && !mbar_wait_bounded(smem_u32(&empty[s]), (epar >> s) & 1u))
@@ -584,6 +665,7 @@ TclArgs make_args(const float *left, int nl, const float *right, int nr, int H, 
   a.right = right;
   a.out = out;
   a.partial = nullptr;
+  a.counter = nullptr;
   a.nl = nl;
   a.nr = nr;
   a.H = H;
@@ -596,10 +678,13 @@ TclArgs make_args(const float *left, int nl, const float *right, int nr, int H, 
   a.nrt = (nr + (1 << a.nr_log2) - 1) >> a.nr_log2;
   a.uy = (H + kKY - 1) / kKY;
   a.ux = (W + kKX - 1) / kKX;
-  // row units per CTA: 1, else the smallest power of two (at most all of
-  // them) that keeps the partial tiles within kTargetScratch;
+  // row units per item: the smallest power of two from min(4, uy) on (at
+  // most all of them) that keeps the partial tiles within kTargetScratch
+  // (measured on GB300: items of 4 - 8 units beat 1, whose per-item work
+  // shows, and 16 - 32, whose few items balance badly);
   // CORR_XCORR_TCL_GROUP=n (read on every call) sets it to n instead
   a.ug = 1;
+  while (a.ug < 4 && a.ug < a.uy) a.ug *= 2;
   while (a.ug < a.uy &&
          (double)nl * a.ndxt * a.ndyt * a.nrt * ((a.uy + a.ug - 1) / a.ug) * a.ux * kTileFloats *
                  sizeof(float) > double(kTargetScratch))
@@ -619,7 +704,8 @@ TclArgs make_args(const float *left, int nl, const float *right, int nr, int H, 
 
 size_t scratch_bytes(int nl, int nr, int H, int W) {
   const TclArgs a = make_args(nullptr, nl, nullptr, nr, H, W, nullptr);
-  return size_t(a.items) * kTileFloats * sizeof(float);
+  // partial tiles, then the item counter
+  return size_t(a.items) * kTileFloats * sizeof(float) + 256;
 }
 
 cudaError_t launch(const float *left, int nl, const float *right, int nr, int H, int W,
@@ -627,8 +713,10 @@ cudaError_t launch(const float *left, int nl, const float *right, int nr, int H,
   TclArgs a = make_args(left, nl, right, nr, H, W, out);
   a.partial = scratch;
   if (a.items > 0x7fffffffLL || scratch == nullptr) return cudaErrorInvalidValue;
+  a.counter = reinterpret_cast<int *>(scratch + size_t(a.items) * kTileFloats);
   cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void *>(xcorr_tcl_kernel));
   if (e != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(a.counter, 0, sizeof(int), stream)) != cudaSuccess) return e;
   // persistent: one CTA per SM (its shared memory and tensor memory fill one)
   const long long ctas = a.items < device_sm_count() ? a.items : device_sm_count();
   xcorr_tcl_kernel<<<unsigned(ctas), kThreads + 32, kSmemBytes, stream>>>(a);

@@ -274,7 +274,7 @@ def test_line_sums_match_the_oracle():
 
 @pytest.mark.parametrize("n", [512, 1024])
 def test_tcl_large_pair(n):
-    """Default choice for one n x n pair (row-unit groups of 16 and 32): at
+    """Default choice for one n x n pair (row-unit groups of 8 and 32): at
     sampled outputs (every tile's corner rows and columns, plus random
     ones) against the oracle, and every output row and column through its
     sum."""
