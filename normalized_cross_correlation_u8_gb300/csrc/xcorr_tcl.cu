@@ -24,23 +24,22 @@
 // of one sign the error of a chain of accumulates grows with its length
 // (measured on GB300: about 2e-8 of the sum per accumulate; 384 of them, one
 // 32-row unit, reached 1.1e-5 of sum |L*R| on uniform [0, 1) inputs).  A
-// chain here is at most 8 rows (96 accumulates) in one of two tensor-memory
-// accumulators; the builder warps add each finished chain into an FP32
-// running sum in registers (round to nearest) while the next chain runs in
-// the other accumulator.
+// chain here is at most 8 rows (96 accumulates) in one tensor-memory
+// accumulator; the builder warps add each finished chain into an FP32
+// running sum in registers (round to nearest).
 //
 // Operands: B (rows of R) is staged per unit in shared memory in the
 // no-swizzle K-major layout [x'/4][row slot][right][4 floats], rows in
 // reverse order, so the N rows of consecutive shifts dy are consecutive
 // slots and one descriptor per (y, 8 columns) reads them; two units are
 // staged at a time.  A (the Toeplitz rows of L) is written per overlap row
-// by eight builder warps straight into tensor memory (tcgen05.st) through
-// four stages; one warp issues kind::tf32 tcgen05.mma, reading per row a
-// record (B offset, K steps, accumulator, chain start / end) that the
-// builders leave beside the stage.  Operands are split v = tf32(v) +
-// tf32(v - tf32(v)) and each product is formed as hi*hi + hi*lo + lo*hi
-// (the three-pass TF32 scheme; see xcorr_tc.cu).  Every mbarrier wait is
-// bounded (corr_device_status).
+// by sixteen builder warps straight into tensor memory (tcgen05.st); the
+// rows alternate between two streams, each with two A stages, one
+// accumulator and one warp issuing kind::tf32 tcgen05.mma, which reads per
+// row a record (B offset, chain start / end) the builders leave beside the
+// stage.  Operands are split v = tf32(v) + tf32(v - tf32(v)) and each
+// product is formed as hi*hi + hi*lo + lo*hi (the three-pass TF32 scheme;
+// see xcorr_tc.cu).  Every mbarrier wait is bounded (corr_device_status).
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -60,8 +59,9 @@ constexpr int kN = 128;                   // (shift dy, right) slots
 constexpr int kKY = 32;                   // overlap rows per unit
 constexpr int kKX = 32;                   // right columns per unit
 constexpr int kSteps = kKX / 8;           // 8-deep K steps per row
-constexpr int kSegRows = 8;               // overlap rows per accumulation chain
-constexpr int kABufs = 4;                 // A stages in tensor memory
+constexpr int kStreams = 2;               // row streams, one issuer and accumulator each
+constexpr int kBlockRows = 16;            // rows per block: kBlockRows / 2 per stream's chain
+constexpr int kABufs = 4;                 // A stages in tensor memory (2 per stream)
 constexpr int kStageCols = kSteps * 16;   // hi + lo columns of one A stage
 constexpr uint32_t kAccCols = kN;         // one FP32 accumulator
 constexpr uint32_t kTmemCols = 512;       // 2 accumulators + kABufs A stages
@@ -77,7 +77,8 @@ constexpr uint32_t kIdesc = idesc_tf32(kM, kN);
 static_assert(8 * kMaxSlots * 1 <= kMaxBEntries && 8 * (kKY + 64 - 1) * 2 <= kMaxBEntries,
               "B staging holds every right-tile shape");
 static_assert(2 * kAccCols + kABufs * kStageCols == kTmemCols, "tensor memory plan");
-static_assert(kKY % kSegRows == 0, "chains never cross a unit");
+static_assert(kKY % kBlockRows == 0, "blocks never cross a unit");
+static_assert(kABufs == 2 * kStreams, "two A stages per stream");
 
 // shared memory: two staged B (TF32 hi / lo), the raw rows of the B after
 // them (as copied), two units' left rows, the row records the builders
@@ -87,14 +88,13 @@ constexpr size_t kRawOff = 2 * size_t(kBBuf);
 constexpr size_t kLpOff = kRawOff + size_t(kBHalf);
 constexpr size_t kInfoOff = kLpOff + 2 * size_t(kLBuf) * sizeof(float);
 constexpr size_t kBarOff = kInfoOff + kABufs * sizeof(uint2);
-constexpr int kBars = 2 * kABufs + 3;    // full, empty, chain done x 2, done
+constexpr int kBars = 2 * kABufs + 3;    // full, empty, chain done per stream, done
 constexpr size_t kClaimOff = kBarOff + kBars * 8;
 constexpr size_t kSmemBytes = kClaimOff + 2 * sizeof(int) + 16;
 
-// row record flags (second word): accumulator, first and last row of a
-// chain, end of the CTA's work
-constexpr uint32_t kRecAcc = 1u << 8, kRecFirst = 1u << 9, kRecLast = 1u << 10,
-                   kRecStop = 1u << 11;
+// row record flags (second word): first and last row of a chain, end of
+// the stream
+constexpr uint32_t kRecFirst = 1u << 9, kRecLast = 1u << 10, kRecStop = 1u << 11;
 
 struct TclArgs {
   const float *left;
@@ -300,36 +300,42 @@ __device__ __forceinline__ int builders_sync_or(int v) {
 }
 
 // Persistent: each CTA claims items in turn (a counter in scratch memory)
-// and runs their units as one row stream through kABufs A stages; each
-// chain of up to kSegRows rows of one unit accumulates in one of two
-// accumulators (the tensor cores' FP32 accumulation truncates, so a chain
-// stays short: at most 96 updates), and the builders add the finished
-// chain into an FP32 running sum of the item held in registers (thread:
-// accumulator row 32 (warp % 4) + lane, columns 32 (warp / 4) .. + 31)
-// while the next chain runs in the other accumulator.  At the end of an
-// item the running sum goes to its partial tile.
+// and runs their units' overlap rows in blocks of kBlockRows.  Within a
+// block the rows alternate between two streams, each with its own issuing
+// thread, two A stages and FP32 accumulator: one thread alone cannot issue
+// 128 x 128 x 8 MMAs as fast as the tensor pipe runs them (about 54
+// against 64 cycles each, with any per-row bookkeeping on top, and the
+// pipe queues almost nothing ahead), two together can.  A stream's rows of
+// one block are one accumulation chain (at most 8 rows, 96 accumulates:
+// the tensor cores' FP32 accumulation truncates, so a chain stays short).
+// Before a block's first rows the builders add both finished chains into
+// an FP32 running sum of the item held in registers (thread: accumulator
+// row 32 (warp % 4) + lane, columns 32 (warp / 4) .. + 31); at the end of
+// an item the running sum goes to its partial tile.
 //
-// Staging runs two units ahead: during unit u the builders turn the raw
-// rows of unit u + 1 (copied during unit u - 1) into its TF32 B and start
-// the asynchronous copies of unit u + 2's raw rows and unit u + 1's left
-// rows, into the buffers unit u - 1 has just released.
-__global__ void __launch_bounds__(kThreads + 32, 1) xcorr_tcl_kernel(const TclArgs a) {
+// Staging runs two units ahead: at the first block of unit u the builders
+// turn the raw rows of unit u + 1 (copied during unit u - 1) into its TF32
+// B and start the asynchronous copies of unit u + 2's raw rows and unit u +
+// 1's left rows, into the buffers unit u - 1 has just released.
+__global__ void __launch_bounds__(kThreads + 32 * kStreams, 1)
+    xcorr_tcl_kernel(const TclArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t *raw = smem + kRawOff;
   float *lp = reinterpret_cast<float *>(smem + kLpOff);                  // [2][kLBuf]
   uint2 *info = reinterpret_cast<uint2 *>(smem + kInfoOff);             // [kABufs]
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + kBarOff);        // [kABufs]
   uint64_t *empty = full + kABufs;                                       // [kABufs]
-  uint64_t *chain = empty + kABufs;                                      // [2]
+  uint64_t *chain = empty + kABufs;                                      // [kStreams]
   uint64_t *done = chain + 2;
   int *claimed = reinterpret_cast<int *>(smem + kClaimOff);             // [2]
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(claimed + 2);
 
   const int NR = 1 << a.nr_log2, NS = kKY + a.ndy - 1;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const bool issuer = warp == kThreads / 32;
+  const int stream = warp - kThreads / 32;     // issuer warps: 0, 1; builders < 0
+  const bool issuer = stream >= 0;
 
-  if (issuer) {
+  if (stream == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)),
                  "r"(kTmemCols)
@@ -343,7 +349,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1) xcorr_tcl_kernel(const TclAr
       }
       mbar_init(smem_u32(&chain[0]), 1);
       mbar_init(smem_u32(&chain[1]), 1);
-      mbar_init(smem_u32(done), 1);
+      mbar_init(smem_u32(done), kStreams);
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
   }
@@ -362,10 +368,11 @@ __global__ void __launch_bounds__(kThreads + 32, 1) xcorr_tcl_kernel(const TclAr
       // below 2^18, so nothing carries out of it)
       const uint64_t desc0 = smem_desc(smem_u32(smem), lbo_b, 128);
       const uint64_t step_j = uint64_t((2 * lbo_b) >> 4), to_lo = uint64_t(kBHalf >> 4);
-      int g = 0;
-      for (;; ++g) {
-        const int s = g % kABufs;
-        if (!mbar_wait_bounded(smem_u32(&full[s]), uint32_t(g / kABufs) & 1u)) {
+      const uint32_t d = tmem + uint32_t(stream) * kAccCols;
+      int k = 0;                                   // this stream's rows so far
+      for (;; ++k) {
+        const int s = 2 * stream + (k & 1);
+        if (!mbar_wait_bounded(smem_u32(&full[s]), uint32_t(k >> 1) & 1u)) {
           failed = 1;
           break;
         }
@@ -375,7 +382,6 @@ __global__ void __launch_bounds__(kThreads + 32, 1) xcorr_tcl_kernel(const TclAr
         // all kSteps K steps, straight-line (a branch between tcgen05.mma
         // issues slows them well below the tensor pipe's rate): columns x'
         // no shift of the tile reaches meet left values staged as zero
-        const uint32_t d = tmem + ((rec.y & kRecAcc) ? kAccCols : 0u);
         const uint32_t ab = a_cols + uint32_t(kStageCols * s);
         const uint64_t bhi = desc0 + uint64_t(rec.x >> 4);
         mma3_tf32_ta(d, ab, ab + 8, bhi, bhi + to_lo, (rec.y & kRecFirst) ? 0u : 1u, kIdesc);
@@ -384,15 +390,16 @@ __global__ void __launch_bounds__(kThreads + 32, 1) xcorr_tcl_kernel(const TclAr
           mma3_tf32_ta(d, ab + 16 * j, ab + 16 * j + 8, bhi + j * step_j, bhi + j * step_j + to_lo,
                        1u, kIdesc);
         mma_commit(smem_u32(&empty[s]));
-        if (rec.y & kRecLast) mma_commit(smem_u32(&chain[(rec.y & kRecAcc) ? 1 : 0]));
+        if (rec.y & kRecLast) mma_commit(smem_u32(&chain[stream]));
       }
       mma_commit(smem_u32(done));
       if (!mbar_wait_bounded(smem_u32(done), 0)) failed = 1;
-      // every stage's last release has landed (no arrival on this CTA's
-      // shared memory is left pending when it exits)
-      for (int k = 0; k < kABufs && k < g; ++k) {
-        const int uses = (g - k + kABufs - 1) / kABufs;
-        if (!mbar_wait_bounded(smem_u32(&empty[k]), uint32_t(uses - 1) & 1u)) failed = 1;
+      // each of this stream's stages: its last release has landed (no
+      // arrival on this CTA's shared memory is left pending when it exits)
+      for (int b = 0; b < 2 && b < k; ++b) {
+        const int uses = (k - b + 1) / 2;
+        if (!mbar_wait_bounded(smem_u32(&empty[2 * stream + b]), uint32_t(uses - 1) & 1u))
+          failed = 1;
       }
     }
   } else {
@@ -476,29 +483,35 @@ __global__ void __launch_bounds__(kThreads + 32, 1) xcorr_tcl_kernel(const TclAr
     }
     failed = builders_sync_or(failed);
 
-    // the chain whose sum is still to be taken in
-    int pseg = -1;            // its index (chains built before it: pseg)
-    int pitem = -1;           // its item, if it ends that item
+    // the chains of the last block, still to be taken in
+    int pstreams = 0;         // streams that had rows in it (1 or 2; 0: none)
+    int pitem = -1;           // its item, if the block ends that item
     bool punit_end = false;   // whether it ends its unit
-    int g = 0, seg = 0, u = 0;
+    int nch0 = 0, nch1 = 0;   // chains taken in per stream
+    int gs0 = 0, gs1 = 0, u = 0;   // rows built per stream; units begun
     uint32_t epar = 0;
 
-    // Take in chain pseg: wait for its products, add its accumulator to the
-    // running sum; at the end of an item store the sum.  At the end of a
-    // unit (its products all done, its buffers free): turn unit u + 1's
-    // raw rows into B and start the copies of unit u + 2's raw rows and
-    // unit u + 1's left rows.
+    // Take in the last block's chains: wait for their products, add the
+    // accumulators to the running sum; at the end of an item store the sum.
+    // At the end of a unit (its products all done, its buffers free): turn
+    // unit u + 1's raw rows into B and start the copies of unit u + 2's raw
+    // rows and unit u + 1's left rows.
     auto take_in = [&]() {
-      const int pb = pseg & 1;
-      if (!failed && !mbar_wait_bounded_sleep(smem_u32(&chain[pb]), uint32_t(pseg >> 1) & 1u))
-        failed = 1;
-      failed = __any_sync(~0u, failed);     // the warp's .aligned steps stay together
-      fence_after_sync();
-      if (!failed) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_base + uint32_t(pb) * kAccCols + uint32_t(32 * jh), v);
 #pragma unroll
-        for (int k = 0; k < 32; ++k) sum[k] += __uint_as_float(v[k]);
+      for (int st = 0; st < kStreams; ++st) {
+        if (st >= pstreams) break;
+        const int n = st == 0 ? nch0 : nch1;
+        if (!failed && !mbar_wait_bounded_sleep(smem_u32(&chain[st]), uint32_t(n) & 1u))
+          failed = 1;
+        failed = __any_sync(~0u, failed);     // the warp's .aligned steps stay together
+        fence_after_sync();
+        if (!failed) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_base + uint32_t(st) * kAccCols + uint32_t(32 * jh), v);
+#pragma unroll
+          for (int k = 0; k < 32; ++k) sum[k] += __uint_as_float(v[k]);
+        }
+        if (st == 0) ++nch0; else ++nch1;
       }
       fence_before_sync();
       if (pitem >= 0) {
@@ -522,6 +535,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1) xcorr_tcl_kernel(const TclAr
         copy_lp(a, it, ky1, lp_u32 + uint32_t(nbuf * kLBuf) * 4, t);
         cp_async_commit();
       }
+      pstreams = 0;
     };
 
     while (cb >= 0) {
@@ -533,14 +547,14 @@ __global__ void __launch_bounds__(kThreads + 32, 1) xcorr_tcl_kernel(const TclAr
       unit_rows(cur, cky, y0, y1);
       const int ya = cky * kKY;
       const bool item_end = cky + 1 == cur.kb;
-      for (int sy = y0; sy < y1; sy += kSegRows) {
-        const int sy1 = sy + kSegRows < y1 ? sy + kSegRows : y1;
-        // take in the previous chain once this one is kABufs rows deep
-        // (its products are then done and the stages still hold work)
-        const int take_at = sy + kABufs - 1 < sy1 - 1 ? sy + kABufs - 1 : sy1 - 1;
-        for (int y = sy; y < sy1; ++y, ++g) {
-          const int s = g % kABufs;
-          if (g >= kABufs) {
+      for (int sy = y0; sy < y1; sy += kBlockRows) {
+        const int sy1 = sy + kBlockRows < y1 ? sy + kBlockRows : y1;
+        if (pstreams) take_in();
+        for (int y = sy; y < sy1; ++y) {
+          const int st = (y - sy) & 1;
+          const int kr = st ? gs1 : gs0;
+          const int s = 2 * st + (kr & 1);
+          if (kr >= 2) {
             if (!failed && !mbar_wait_bounded_sleep(smem_u32(&empty[s]), (epar >> s) & 1u))
               failed = 1;
             failed = __any_sync(~0u, failed);
@@ -560,16 +574,15 @@ __global__ void __launch_bounds__(kThreads + 32, 1) xcorr_tcl_kernel(const TclAr
             // row n = (dyi, r) of B: right row y - dy0 - dyi at slot
             // (ya + kKY - 1 - y) + dyi, n * 16 bytes past slot ya + kKY - 1 - y
             info[s] = make_uint2(uint32_t(buf * kBBuf + (ya + kKY - 1 - y) * NR * 16),
-                                 ((seg & 1) ? kRecAcc : 0u) | (y == sy ? kRecFirst : 0u) |
-                                     (y == sy1 - 1 ? kRecLast : 0u));
+                                 (y - sy < 2 ? kRecFirst : 0u) | (y + 2 >= sy1 ? kRecLast : 0u));
           }
           asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
           fence_before_sync();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&full[s]));
-          if (y == take_at && pseg >= 0) take_in();
+          if (st) ++gs1; else ++gs0;
         }
-        pseg = seg++;
+        pstreams = sy1 - sy >= 2 ? 2 : 1;
         const bool unit_end = sy1 == y1;
         pitem = (unit_end && item_end) ? cb : -1;
         punit_end = unit_end;
@@ -588,24 +601,28 @@ __global__ void __launch_bounds__(kThreads + 32, 1) xcorr_tcl_kernel(const TclAr
       ky1 = ky2;
       successor(b1, ky1, u & 1, b2, ky2);
     }
-    if (pseg >= 0) {
+    if (pstreams) {
       b1 = -1;
       take_in();
     }
     cp_async_wait_all();                 // no copy in flight when the CTA ends
-    // end of the row stream
-    const int s = g % kABufs;
-    if (g >= kABufs && !failed && !mbar_wait_bounded(smem_u32(&empty[s]), (epar >> s) & 1u))
-      failed = 1;
-    if (t == 0) info[s] = make_uint2(0u, kRecStop);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&full[s]));
+    // end of both row streams
+#pragma unroll
+    for (int st = 0; st < kStreams; ++st) {
+      const int kr = st ? gs1 : gs0;
+      const int s = 2 * st + (kr & 1);
+      if (kr >= 2 && !failed && !mbar_wait_bounded(smem_u32(&empty[s]), (epar >> s) & 1u))
+        failed = 1;
+      if (t == 0) info[s] = make_uint2(0u, kRecStop);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&full[s]));
+    }
   }
   failed = __syncthreads_or(failed);
   if (failed && t == 0) atomicOr(&g_tcl_status, 1);
   fence_before_sync();
   __syncthreads();
-  if (issuer) {
+  if (stream == 0) {
     fence_after_sync();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(kTmemCols)
@@ -719,7 +736,7 @@ cudaError_t launch(const float *left, int nl, const float *right, int nr, int H,
   if ((e = cudaMemsetAsync(a.counter, 0, sizeof(int), stream)) != cudaSuccess) return e;
   // persistent: one CTA per SM (its shared memory and tensor memory fill one)
   const long long ctas = a.items < device_sm_count() ? a.items : device_sm_count();
-  xcorr_tcl_kernel<<<unsigned(ctas), kThreads + 32, kSmemBytes, stream>>>(a);
+  xcorr_tcl_kernel<<<unsigned(ctas), kThreads + 32 * kStreams, kSmemBytes, stream>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const long long outs = (long long)nl * nr * (2LL * H - 1) * (2LL * W - 1);
   const long long cap = 8LL * device_sm_count() * 8;
