@@ -1097,13 +1097,13 @@ constexpr size_t kMaxTclScratch = (size_t(512) << 20) + 256;
 
 // Whether a shape takes the larger-matrix tensor-core kernel (xcorr_tcl.cu):
 // CORR_XCORR_TCL (read on every call) "1" / "0" forces it on / off where it
-// applies; otherwise the measured policy: pairs * (H*W)^2 >= 1.5e9 products
-// (its partial-sum pass and 32 x 32 units cost about 30 us on any shape).
-// It never takes more than max_scratch (nor 512 MB) of scratch.  Measured on
-// GB300 (CUDA-graph device time, this kernel / the scalar one): 1 x 1 of
-// 256^2 135 / 213 us, 1 x 128 of 64^2 113 / 131 us, 1 x 1 of 512^2 1.13 /
-// 2.84 ms, 1 x 1 of 1024^2 13.2 / 43.9 ms; below the rule 2 x 96 of 48^2
-// 132 / 102 us, 1 x 1 of 128^2 31 / 31 us.
+// applies; otherwise the measured policy: pairs * (H*W)^2 >= 4e8 products.
+// It never takes more than max_scratch (nor 512 MB of partial tiles).
+// Measured on GB300 (CUDA-graph device time, this kernel / the scalar
+// one): 1 x 1 of 160^2 50 / 56 us, of 256^2 89 / 214 us, of 1024^2 10.3 /
+// 43.8 ms; 1 x 32 of 64^2 39 / 74 us, 4 x 16 of 64^2 64 / 118 us, 2 x 96 of
+// 48^2 96 / 102 us; below the rule 1 x 64 of 48^2 48 / 49 us, 1 x 1 of
+// 128^2 32 / 31 us, 1 x 16 of 64^2 35 / 32 us, 1 x 128 of 32^2 37 / 20 us.
 bool use_tcl(int nl, int nr, int H, int W, size_t max_scratch) {
   const size_t need = tcl::scratch_bytes(nl, nr, H, W);
   if (need > kMaxTclScratch || need > max_scratch) return false;
@@ -1111,7 +1111,7 @@ bool use_tcl(int nl, int nr, int H, int W, size_t max_scratch) {
   if (v && v[0] == '0' && v[1] == '\0') return false;
   if (v && v[0] == '1' && v[1] == '\0') return true;
   const double hw = double(H) * W;
-  return double(nl) * nr * hw * hw >= 1.5e9;
+  return double(nl) * nr * hw * hw >= 4e8;
 }
 
 // CORR_XCORR_WARP (read on every call): "1" routes every shape to the

@@ -13,7 +13,7 @@
 // one-to-one, 32 shifts x 4 rights for one-to-many).  Its K -- every row y
 // and column x' that some shift of the tile reaches -- is cut into units of
 // 32 rows x 32 columns.  An item is one tile's unit column and a group of G
-// consecutive row units (G = 4 where the matrix has that many, more for
+// consecutive row units (G = 1, 2 or 4 as the items balance best, more for
 // larger matrices so that the partial tiles stay within 128 MB).  The
 // kernel is persistent, one CTA per SM claiming items in turn; each item's
 // 128 x 128 partial sums go to scratch memory and a second kernel adds
@@ -695,16 +695,22 @@ TclArgs make_args(const float *left, int nl, const float *right, int nr, int H, 
   a.nrt = (nr + (1 << a.nr_log2) - 1) >> a.nr_log2;
   a.uy = (H + kKY - 1) / kKY;
   a.ux = (W + kKX - 1) / kKX;
-  // row units per item: the smallest power of two from min(4, uy) on (at
-  // most all of them) that keeps the partial tiles within kTargetScratch
-  // (measured on GB300: items of 4 - 8 units beat 1, whose per-item work
-  // shows, and 16 - 32, whose few items balance badly);
-  // CORR_XCORR_TCL_GROUP=n (read on every call) sets it to n instead
+  // row units per item (measured on GB300): 1 while that leaves at most
+  // 3 items per SM; else 4 or 2 (the largest that divides the row units
+  // and leaves at least 1.5 items per SM; groups that end ragged balance
+  // badly); then doubled while the partial tiles would pass kTargetScratch.
+  // CORR_XCORR_TCL_GROUP=n (read on every call) sets it to n instead.
+  const double tiles = double(nl) * a.ndxt * a.ndyt * a.nrt;
+  auto items_of = [&](int g) { return tiles * ((a.uy + g - 1) / g) * a.ux; };
+  const double sms = double(device_sm_count());
   a.ug = 1;
-  while (a.ug < 4 && a.ug < a.uy) a.ug *= 2;
-  while (a.ug < a.uy &&
-         (double)nl * a.ndxt * a.ndyt * a.nrt * ((a.uy + a.ug - 1) / a.ug) * a.ux * kTileFloats *
-                 sizeof(float) > double(kTargetScratch))
+  if (items_of(1) > 3 * sms)
+    for (int g = 4; g >= 2; g /= 2)
+      if (a.uy % g == 0 && items_of(g) >= 1.5 * sms) {
+        a.ug = g;
+        break;
+      }
+  while (a.ug < a.uy && items_of(a.ug) * kTileFloats * sizeof(float) > double(kTargetScratch))
     a.ug *= 2;
   if (const char *v = getenv("CORR_XCORR_TCL_GROUP")) {
     const int n = atoi(v);

@@ -128,7 +128,8 @@ def test_xcorr_kernel_choice(monkeypatch):
     assert k(1, 128, 32, 32) == "bcast"
     assert k(1, 1, 1024, 1024) == "tensor_large"   # 32 row units per item: 512 MB
     assert k(1, 1, 2048, 2048) == "rows_win"   # partial sums would pass 512 MB
-    assert k(2, 96, 48, 48) == "bcast"         # below the larger-matrix rule
+    assert k(2, 96, 48, 48) == "tensor_large"  # 1.0e9 products
+    assert k(1, 64, 48, 48) == "bcast"         # below the larger-matrix rule
     assert k(1, 1, 1, 4096) == "warp"          # a single long row
     assert k(16, 16, 16, 16) == "tiny"         # small batch, below the tensor rule
     assert k(32, 64, 8, 8) == "tiny"           # H*W < 100
