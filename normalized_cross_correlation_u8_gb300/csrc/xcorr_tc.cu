@@ -76,7 +76,8 @@ constexpr int kLRow = 64;                 // floats per staged left row
 constexpr int kSlotsR = 48;               // right row slots (2H + 30 <= 47 used)
 constexpr int kBBytes = 4 * kSlotsR * kRights * 16;   // staged B operand (hi or lo): 12 KB
 constexpr int kRunFloats = kRights * 31 * 31;   // one left's outputs in the epilogue
-constexpr uint32_t kTmemCols = 256;       // accumulator (128) + kABufs A stages (32 each)
+constexpr int kStreams = 2;               // row streams: an issuing warp and accumulator each
+constexpr uint32_t kTmemCols = 512;       // 2 accumulators (128 each) + kABufs A stages (32 each)
 constexpr uint32_t kIdesc = tcx::idesc_tf32(kM, kN);
 
 struct TcArgs {
@@ -97,13 +98,18 @@ __device__ int g_tc_status;   // bit 0: a bounded wait gave up
 //
 // Warp roles: warps 0-7 write the A operand of one overlap row at a time
 // into kABufs rotating tensor-memory stages (then, after the last row,
-// read the accumulator out); warp 8 issues the tensor-core instructions.
-// Stage b is handed over through two mbarriers: full[b] (one arrival per
-// builder warp once its part is in tensor memory) and empty[b] (a
-// tcgen05.commit: the products that read it have completed), so writing
-// rows i + 1 .. i + kABufs - 1 overlaps the products of row i.
+// read the accumulators out); warps 8 and 9 issue the tensor-core
+// instructions, for the even and the odd overlap rows, each into its own
+// accumulator (one thread issues a 128x128x8 MMA in about 54 cycles against
+// the tensor pipe's 64, with its per-row bookkeeping on top, and the pipe
+// queues almost nothing ahead; two issuers keep it busy, and each chain of
+// accumulates is at most 8 rows x KH x 3 = 48 long).  Stream s owns stages
+// 2s and 2s + 1; stage b is handed over through two mbarriers: full[b] (one
+// arrival per builder warp once its part is in tensor memory) and empty[b]
+// (a tcgen05.commit: the products that read it have completed).
 template <int KH>
-__global__ void __launch_bounds__(kThreads + 32, 1) xcorr_tc_kernel(const TcArgs a) {
+__global__ void __launch_bounds__(kThreads + 32 * kStreams, 1)
+    xcorr_tc_kernel(const TcArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t *b_hi = smem;                                   // [4][kSlotsR][kRights][4] TF32 hi
   uint8_t *b_lo = smem + kBBytes;                         // same, lo parts
@@ -116,12 +122,13 @@ __global__ void __launch_bounds__(kThreads + 32, 1) xcorr_tc_kernel(const TcArgs
 
   const int H = a.H, W = a.W, t = threadIdx.x;
   const int warp = t >> 5, lane = t & 31;
-  const bool issuer = warp == kThreads / 32;
+  const int stream = warp - kThreads / 32;      // issuer warps: 0, 1; builders < 0
+  const bool issuer = stream >= 0;
   const int rt = blockIdx.x % a.rtiles, mt = blockIdx.x / a.rtiles;
   const int l0 = mt * kLefts, r0 = rt * kRights;
 
-  if (issuer) {
-    // tensor memory: accumulator at columns 0..127, A stages above it
+  if (stream == 0) {
+    // tensor memory: accumulators at columns 0..127 and 128..255, A stages above
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)),
                  "r"(kTmemCols)
@@ -133,10 +140,10 @@ __global__ void __launch_bounds__(kThreads + 32, 1) xcorr_tc_kernel(const TcArgs
         mbar_init(smem_u32(&full[k]), kThreads / 32);
         mbar_init(smem_u32(&empty[k]), 1);
       }
-      mbar_init(smem_u32(done), 1);
+      mbar_init(smem_u32(done), kStreams);
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-  } else {
+  } else if (!issuer) {
     // the tile's rights as TF32 hi / lo in the B layout: entry e = (xc,
     // slot, rq) (rq fastest, so entries are consecutive 16-byte rows) holds
     // R[r0 + rq][yr][4 xc .. 4 xc + 3] with yr = 2H - 2 - slot, zero
@@ -199,21 +206,21 @@ __global__ void __launch_bounds__(kThreads + 32, 1) xcorr_tc_kernel(const TcArgs
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t a_cols = tmem + uint32_t(kN);     // A stage b: columns + 32 b
+  const uint32_t a_cols = tmem + uint32_t(kStreams * kN);   // A stage b: columns + 32 b
   int failed = 0;
 
   if (issuer) {
     if (lane == 0) {
       const uint32_t bh_base = smem_u32(b_hi), bl_base = smem_u32(b_lo);
       constexpr uint32_t kLboB = kSlotsR * kRights * 16;   // next 4 columns x'
-      uint32_t fpar = 0;      // bit k: parity of full[k]'s next completion
-      int bb = 0;
-      for (int i = 0; i < H; ++i) {
-        if (!mbar_wait_bounded(smem_u32(&full[bb]), (fpar >> bb) & 1u)) {
+      const uint32_t d = tmem + uint32_t(stream * kN);
+      const int rows = (H - stream + 1) / 2;               // rows stream, stream + 2, ...
+      for (int k = 0; k < rows; ++k) {
+        const int i = 2 * k + stream, bb = 2 * stream + (k & 1);
+        if (!mbar_wait_bounded(smem_u32(&full[bb]), uint32_t(k >> 1) & 1u)) {
           failed = 1;
           break;
         }
-        fpar ^= 1u << bb;
         fence_after_sync();
         // N row n = (dyi, rq): right row y - dy = y + (H-1) - dyi, slot
         // H - 1 - y + dyi, so row n sits n * 16 bytes past slot H - 1 - y
@@ -224,22 +231,21 @@ __global__ void __launch_bounds__(kThreads + 32, 1) xcorr_tc_kernel(const TcArgs
           const uint32_t boff = s0off + uint32_t(2 * h) * kLboB;
           const uint64_t bhi = smem_desc(bh_base + boff, kLboB, 128);
           const uint64_t blo = smem_desc(bl_base + boff, kLboB, 128);
-          mma_tf32_ta(tmem, ab + 8 * h, bhi, (i > 0 || h > 0) ? 1u : 0u, kIdesc);
-          mma_tf32_ta(tmem, ab + 8 * h, blo, 1u, kIdesc);
-          mma_tf32_ta(tmem, ab + 16 + 8 * h, bhi, 1u, kIdesc);
+          mma3_tf32_ta(d, ab + 8 * h, ab + 16 + 8 * h, bhi, blo, (k > 0 || h > 0) ? 1u : 0u,
+                       kIdesc);
         }
         mma_commit(smem_u32(&empty[bb]));
-        bb = bb + 1 == kABufs ? 0 : bb + 1;
       }
       // every product issued so far, then the accumulator is final (left
       // out under the stall test: every wait on it then runs out)
       if (!a.stall) mma_commit(smem_u32(done));
       if (!mbar_wait_bounded(smem_u32(done), 0)) failed = 1;
-      // and every stage's last release has landed (no arrival on this
-      // CTA's shared memory is left pending when it exits)
-      for (int k = 0; k < kABufs && k < H; ++k) {
-        const int uses = (H - k + kABufs - 1) / kABufs;   // rows k, k + kABufs, ...
-        if (!mbar_wait_bounded(smem_u32(&empty[k]), uint32_t(uses - 1) & 1u)) failed = 1;
+      // and each of this stream's stages: its last release has landed (no
+      // arrival on this CTA's shared memory is left pending when it exits)
+      for (int b = 0; b < 2 && b < rows; ++b) {
+        const int uses = (rows - b + 1) / 2;             // stream rows b, b + 2, ...
+        if (!mbar_wait_bounded(smem_u32(&empty[2 * stream + b]), uint32_t(uses - 1) & 1u))
+          failed = 1;
       }
     }
   } else {
@@ -251,9 +257,10 @@ __global__ void __launch_bounds__(kThreads + 32, 1) xcorr_tc_kernel(const TcArgs
     const float *lsrc = lp + lt * 16 * kLRow + n + kPadL - (W - 1) + 8 * h;
     const uint32_t lane_base = uint32_t(32 * lt) << 16;
     uint32_t epar = 0;        // bit k: parity of empty[k]'s next completion
-    int bb = 0;
     for (int i = 0; i < H; ++i) {
-      // the products that read this stage kABufs rows ago have completed
+      // row i: stream i % 2, its row k = i / 2, stage 2 (i % 2) + k % 2; the
+      // products that read the stage two rows of the stream ago are done
+      const int bb = 2 * (i & 1) + ((i >> 1) & 1);
       if (i >= kABufs) {
         if (!mbar_wait_bounded(smem_u32(&empty[bb]), (epar >> bb) & 1u)) {
           failed = 1;
@@ -275,7 +282,6 @@ __global__ void __launch_bounds__(kThreads + 32, 1) xcorr_tc_kernel(const TcArgs
       fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&full[bb]));
-      bb = bb + 1 == kABufs ? 0 : bb + 1;
     }
     if (!failed && !mbar_wait_bounded(smem_u32(done), 0)) failed = 1;
   }
@@ -294,13 +300,20 @@ __global__ void __launch_bounds__(kThreads + 32, 1) xcorr_tc_kernel(const TcArgs
 #pragma unroll 1
     for (int j = 0; j < 2; ++j) {
       const int c0 = 64 * half + 32 * j;
-      uint32_t v[32];
-      tmem_ld32(lane_base + uint32_t(c0), v);
+      uint32_t v[32], w[32];
+      tmem_ld32(lane_base + uint32_t(c0), v);           // even rows' accumulator
+      tmem_ld32(lane_base + uint32_t(kN + c0), w);      // odd rows' (none when H = 1)
+      if (H == 1) {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) w[k] = 0u;
+      }
       if (lane < ndx) {
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
           const int c = c0 + k, dyi = c >> 2;          // c = dyi * 4 + rq
-          if (dyi < ndy) lrun[(c & 3) * per_pair + dyi * ndx + lane] = __uint_as_float(v[k]);
+          if (dyi < ndy)
+            lrun[(c & 3) * per_pair + dyi * ndx + lane] =
+                __uint_as_float(v[k]) + __uint_as_float(w[k]);
         }
       }
     }
@@ -323,7 +336,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1) xcorr_tc_kernel(const TcArgs
   }
   fence_before_sync();
   __syncthreads();
-  if (issuer) {
+  if (stream == 0) {
     fence_after_sync();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(kTmemCols)
@@ -369,7 +382,7 @@ cudaError_t launch(const float *left, int nl, const float *right, int nr, int H,
   auto kern = W > 8 ? xcorr_tc_kernel<2> : xcorr_tc_kernel<1>;
   cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void *>(kern));
   if (e != cudaSuccess) return e;
-  kern<<<unsigned(blocks), kThreads + 32, smem, stream>>>(a);
+  kern<<<unsigned(blocks), kThreads + 32 * kStreams, smem, stream>>>(a);
   return cudaGetLastError();
 }
 
