@@ -1132,18 +1132,18 @@ bool use_warp(int nl, int nr, int H, int W) {
 // Whether a shape takes the tensor-core kernel (xcorr_tc.cu): the
 // environment variable CORR_XCORR_TC (read on every call) forces it off
 // ("0") or on wherever it applies ("1"); otherwise the measured policy:
-// matrices of 100+ elements (up to 16 x 16) and pairs * (H*W)^2 >= 2e7
-// products.  Measured on GB300 (CUDA-graph device time, tensor-core /
-// scalar kernel): 32 x 64 of 16^2 12.6 / 20.2 us, 128 x 128 of 16^2 52.8 /
-// 116 us, 32 x 64 of 10^2 8.9 / 9.7 us; below the rule the scalar kernel
-// won (16 x 16 of 16^2 12.5 / 12.1 us, 32 x 64 of 8^2 7.1 / 6.6 us).
+// matrices of 144+ elements (up to 16 x 16) in batches of 64+ pairs.
+// Measured on GB300 (CUDA-graph device time, tensor-core / scalar kernel):
+// 32 x 64 of 16^2 9.8 / 20.3 us, 16 x 16 of 16^2 9.5 / 11.9 us, 8 x 8 of
+// 16^2 9.7 / 11.7 us, 8 x 8 of 12^2 7.8 / 8.3 us; outside the rule the
+// scalar kernels won (64 x 64 of 10^2 13.2 / 11.7 us, 4 x 8 of 16^2 9.6 /
+// 4.6 us, 1 x 8 of 16^2 9.4 / 3.7 us).
 bool use_tc(int nl, int nr, int H, int W) {
   if (!tc::supported(nl, nr, H, W)) return false;
   const char *v = getenv("CORR_XCORR_TC");
   if (v && v[0] == '0' && v[1] == '\0') return false;
   if (v && v[0] == '1' && v[1] == '\0') return true;
-  const double hw = double(H) * W;
-  return hw >= 100 && double(nl) * nr * hw * hw >= 2e7;
+  return H * W >= 144 && double(nl) * nr >= 64;
 }
 
 struct XPlan {

@@ -131,8 +131,11 @@ def test_xcorr_kernel_choice(monkeypatch):
     assert k(2, 96, 48, 48) == "tensor_large"  # 1.0e9 products
     assert k(1, 64, 48, 48) == "bcast"         # below the larger-matrix rule
     assert k(1, 1, 1, 4096) == "warp"          # a single long row
-    assert k(16, 16, 16, 16) == "tiny"         # small batch, below the tensor rule
-    assert k(32, 64, 8, 8) == "tiny"           # H*W < 100
+    assert k(16, 16, 16, 16) == "tensor"       # 256 pairs of 16x16
+    assert k(8, 8, 12, 12) == "tensor"         # 64 pairs of 12x12
+    assert k(64, 64, 10, 10) == "tiny"         # H*W < 144
+    assert k(32, 64, 8, 8) == "tiny"
+    assert k(4, 8, 16, 16) == "rows"           # fewer than 64 pairs
     monkeypatch.setenv("CORR_XCORR_TC", "0")
     assert k(32, 64, 16, 16) == "tiny"
     monkeypatch.setenv("CORR_XCORR_TC", "1")

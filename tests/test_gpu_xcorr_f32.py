@@ -83,8 +83,17 @@ def test_fixture(path):
     # row kernel with fewer rows than lanes (rows split along x over lanes)
     (1, 1, 5, 400), (2, 2, 3, 700), (1, 6, 4, 520), (1, 1, 16, 1000),
 ])
-def test_shapes(nl, nr, H, W):
-    check(rand(nl, H, W), rand(nr, H, W, "normal"))
+def test_shapes(nl, nr, H, W, monkeypatch):
+    """The scalar kernels (the tensor-core kernels, tested on their own in
+    test_gpu_xcorr_tc.py, switched off so that every block shape above still
+    reaches the kernel it was written for), then the library's own choice."""
+    left, right = rand(nl, H, W), rand(nr, H, W, "normal")
+    monkeypatch.setenv("CORR_XCORR_TC", "0")
+    monkeypatch.setenv("CORR_XCORR_TCL", "0")
+    check(left, right)
+    monkeypatch.delenv("CORR_XCORR_TC")
+    monkeypatch.delenv("CORR_XCORR_TCL")
+    check(left, right)
 
 
 def test_delta_reproduces_shifted_matrix():
