@@ -632,16 +632,18 @@ __global__ void __launch_bounds__(kThreads + 32 * kStreams, 1)
 
 // out[l][r][oy][ox] = the sum, in a fixed order (row-unit group, then unit
 // column), of the partial tiles of its tile's CTAs that hold any of its
-// products.
+// products.  A thread takes 4 consecutive shifts dx (one 16-byte load per
+// partial tile: a tile starts at a multiple of 128 shifts), loads in
+// batches of 8 in flight together.
 __global__ void __launch_bounds__(256) xcorr_tcl_sum_kernel(const TclArgs a) {
-  const int ndy = 2 * a.H - 1, ndx = 2 * a.W - 1;
-  const long long total = (long long)a.nl * a.nr * ndy * ndx;
+  const int ndy = 2 * a.H - 1, ndx = 2 * a.W - 1, nq = (ndx + 3) >> 2;
+  const long long total = (long long)a.nl * a.nr * ndy * nq;
   const int NR = 1 << a.nr_log2;
   for (long long o = (long long)blockIdx.x * blockDim.x + threadIdx.x; o < total;
        o += (long long)gridDim.x * blockDim.x) {
     long long rest = o;
-    const int ox = int(rest % ndx);
-    rest /= ndx;
+    const int ox = 4 * int(rest % nq);
+    rest /= nq;
     const int oy = int(rest % ndy);
     rest /= ndy;
     const int r = int(rest % a.nr);
@@ -655,23 +657,32 @@ __global__ void __launch_bounds__(256) xcorr_tcl_sum_kernel(const TclArgs a) {
     // columns in [xlo / kKX, ceil(xhi / kKX)): every such CTA wrote its tile
     const int kg0 = tl.ylo / kKY / a.ug, kg1 = ((tl.yhi + kKY - 1) / kKY - 1) / a.ug + 1;
     const int kx0 = tl.xlo / kKX, kx1 = (tl.xhi + kKX - 1) / kKX;
-    // loads in batches of 8 so that they are in flight together, the adds
-    // in the same fixed order
-    float s = 0.f;
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
     const float *base = a.partial + size_t(n) * kM + m;
     for (int kg = kg0; kg < kg1; ++kg) {
       const float *row = base + ((b0 + kg) * a.ux) * size_t(kTileFloats);
       for (int kx = kx0; kx < kx1; kx += 8) {
-        float v[8];
+        float4 v[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          v[k] = kx + k < kx1 ? __ldg(row + size_t(kx + k) * kTileFloats) : 0.f;
+          v[k] = kx + k < kx1
+                     ? __ldg(reinterpret_cast<const float4 *>(row + size_t(kx + k) * kTileFloats))
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          if (kx + k < kx1) s += v[k];
+          if (kx + k < kx1) {
+            s.x += v[k].x;
+            s.y += v[k].y;
+            s.z += v[k].z;
+            s.w += v[k].w;
+          }
       }
     }
-    a.out[o] = s;
+    float *dst = a.out + ((size_t(l) * a.nr + r) * ndy + oy) * ndx + ox;
+    dst[0] = s.x;
+    if (ox + 1 < ndx) dst[1] = s.y;
+    if (ox + 2 < ndx) dst[2] = s.z;
+    if (ox + 3 < ndx) dst[3] = s.w;
   }
 }
 
@@ -744,7 +755,7 @@ cudaError_t launch(const float *left, int nl, const float *right, int nr, int H,
   const long long ctas = a.items < device_sm_count() ? a.items : device_sm_count();
   xcorr_tcl_kernel<<<unsigned(ctas), kThreads + 32 * kStreams, kSmemBytes, stream>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const long long outs = (long long)nl * nr * (2LL * H - 1) * (2LL * W - 1);
+  const long long outs = (long long)nl * nr * (2LL * H - 1) * ((2LL * W - 1 + 3) / 4);
   const long long cap = 8LL * device_sm_count() * 8;
   const long long blocks = (outs + 255) / 256 < cap ? (outs + 255) / 256 : cap;
   xcorr_tcl_sum_kernel<<<unsigned(blocks), 256, 0, stream>>>(a);
