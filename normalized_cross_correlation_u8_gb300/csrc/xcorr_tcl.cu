@@ -96,6 +96,28 @@ constexpr size_t kSmemBytes = kClaimOff + 2 * sizeof(int) + 16;
 // the stream
 constexpr uint32_t kRecFirst = 1u << 9, kRecLast = 1u << 10, kRecStop = 1u << 11;
 
+// Division of 0 <= n < 2^31 by an invariant d >= 1 as a multiply-high and
+// a shift (the round-up method for unsigned division by invariant
+// integers): with s = ceil(log2 d) and m = floor(2^32 (2^s - d) / d) + 1,
+// n / d = (umulhi(n, m) + n) >> s.
+struct FastDiv {
+  uint32_t m;
+  int s, d;
+};
+
+inline FastDiv fast_div(int d) {
+  FastDiv f;
+  f.d = d;
+  f.s = 0;
+  while ((1LL << f.s) < d) ++f.s;
+  f.m = uint32_t(((1ULL << 32) * ((1ULL << f.s) - uint64_t(d))) / uint64_t(d) + 1);
+  return f;
+}
+
+__device__ __forceinline__ int div_of(int n, const FastDiv &f) {
+  return int((__umulhi(uint32_t(n), f.m) + uint32_t(n)) >> f.s);
+}
+
 struct TclArgs {
   const float *left;
   const float *right;
@@ -109,6 +131,8 @@ struct TclArgs {
   int ug, ugn;           // row units per item, groups of them along the rows
   long long items;       // work items: tiles x ugn x ux (below 2^31 at launch)
   int *counter;          // items claimed so far (zero at launch)
+  FastDiv fux, fugn, fnrt, fndyt, fndxt;   // the item index's radices
+  float inv_ns;          // 1 / (kKY + ndy - 1), the right row slots of a unit
   int vec4;              // rows readable as float4
 };
 
@@ -125,16 +149,21 @@ struct Tile {
 
 __device__ __forceinline__ Tile tile_of(const TclArgs &a, int b) {
   Tile t;
-  t.kx = b % a.ux;
-  b /= a.ux;
-  t.kg = b % a.ugn;
-  b /= a.ugn;
-  t.rt = b % a.nrt;
-  b /= a.nrt;
-  t.dyt = b % a.ndyt;
-  b /= a.ndyt;
-  t.dxt = b % a.ndxt;
-  t.l = b / a.ndxt;
+  int q = div_of(b, a.fux);
+  t.kx = b - q * a.ux;
+  b = q;
+  q = div_of(b, a.fugn);
+  t.kg = b - q * a.ugn;
+  b = q;
+  q = div_of(b, a.fnrt);
+  t.rt = b - q * a.nrt;
+  b = q;
+  q = div_of(b, a.fndyt);
+  t.dyt = b - q * a.ndyt;
+  b = q;
+  q = div_of(b, a.fndxt);
+  t.dxt = b - q * a.ndxt;
+  t.l = q;
   t.dx0 = t.dxt * kM - (a.W - 1);
   t.dy0 = t.dyt * a.ndy - (a.H - 1);
   t.r0 = t.rt << a.nr_log2;
@@ -224,7 +253,9 @@ __device__ __forceinline__ void copy_b_raw(const TclArgs &a, const Item &it, int
     const int e = t + k * kThreads;
     if (e >= nent) break;
     const int r = e & (NR - 1), qq = e >> a.nr_log2;
-    const int sl = qq % NS, xc = qq / NS;
+    // qq / NS in floating point: exact for qq < 8 NS <= 2^11 (the error of
+    // (qq + 1/2) / NS stays far below the 1/(2 NS) to the next integer)
+    const int xc = int((float(qq) + 0.5f) * a.inv_ns), sl = qq - xc * NS;
     const int yr = yc - sl, rr = it.r0 + r, x = it.xa + 4 * xc;
     const bool row_ok = rr < a.nr && yr >= 0 && yr < H;
     const float *src = row_ok ? a.right + (size_t(rr) * H + yr) * W + x : a.right;
@@ -730,6 +761,12 @@ TclArgs make_args(const float *left, int nl, const float *right, int nr, int H, 
   if (a.ug > a.uy) a.ug = a.uy;
   a.ugn = (a.uy + a.ug - 1) / a.ug;
   a.items = (long long)nl * a.ndxt * a.ndyt * a.nrt * a.ugn * a.ux;
+  a.fux = fast_div(a.ux);
+  a.fugn = fast_div(a.ugn);
+  a.fnrt = fast_div(a.nrt);
+  a.fndyt = fast_div(a.ndyt);
+  a.fndxt = fast_div(a.ndxt);
+  a.inv_ns = 1.0f / float(kKY + a.ndy - 1);
   a.vec4 = (W % 4 == 0 && (reinterpret_cast<uintptr_t>(right) & 15) == 0) ? 1 : 0;
   return a;
 }
