@@ -15,6 +15,8 @@ Checked here, through the C ABI, on two calls in a row:
   * a banded shape run after a different banded / segmented shape has left
     its own partial sums in the array (a slot the second call failed to
     write would then show up as a wrong value, not as a zero);
+  * the larger-matrix tensor-core kernel where its partial tiles fit the
+    array (its item counter lives there too);
   * a shape needing more than the array holds is rejected with
     CORR_EUNSUPPORTED before anything runs.
 This file is collected last so that a failure here stops a -x run only after
@@ -95,6 +97,25 @@ def test_noalloc_default_choice_against_the_oracle():
     for got in (ref, *outs):
         err = np.abs(got.numpy().astype(np.float64) - exact)
         assert (err <= REL_TOL * ab + 1e-30).all()
+
+
+def test_noalloc_runs_the_tensor_core_kernel_where_its_partials_fit():
+    """1 x 32 of 64x64 takes the larger-matrix tensor-core kernel on both
+    entry points (128 partial tiles, 8 MB, and its item counter in the
+    array): bit for bit the same as corr_xcorr_f32, twice in a row (the
+    counter is zeroed per call), and within the bar of the oracle, on
+    non-negative inputs (the tensor cores' accumulation drifts most there)."""
+    assert corr.xcorr_f32_kernel(1, 32, 64, 64) == "tensor_large"
+    rng = np.random.default_rng(31)
+    left = rng.uniform(0, 1, size=(1, 64, 64)).astype(np.float32)
+    right = rng.uniform(0, 1, size=(32, 64, 64)).astype(np.float32)
+    dev = torch.device("cuda", 0)
+    L, R = torch.from_numpy(left).to(dev), torch.from_numpy(right).to(dev)
+    ref, outs = run_both(L, R)
+    exact, ab = oracle.xcorr_f32(left, right, nthreads=NT)
+    for got in outs:
+        assert torch.equal(got, ref)
+        assert (np.abs(got.numpy().astype(np.float64) - exact) <= REL_TOL * ab + 1e-30).all()
 
 
 def test_noalloc_after_another_shape_left_data_in_the_array(monkeypatch):
