@@ -13,12 +13,14 @@
 //   m = (left l, shift dx)   A[m][(y, x')] = L_l[y][x' + dx]    (Toeplitz of L)
 //   n = (shift dy, right r)  B[n][(y, x')] = R_r[y - dy][x']    (rows of R; r fastest)
 //   k = (overlap row y, right column x').
-// A CTA owns 4 lefts x 4 rights and every shift of those 16 pairs: M = 4
-// lefts x 32 shift slots dx, N = 32 shift slots dy x 4 rights, K = every
-// row y and column x'.  All CTAs therefore do the same work, and each
-// left's 4 x (2H-1)(2W-1) outputs -- contiguous in memory -- are written by
-// one CTA as one run in whole 32-byte sectors (a store that ends
-// mid-sector costs a DRAM fill, which dominated earlier layouts).
+// A CTA owns 4 lefts x R rights and every shift of those pairs: M = 4
+// lefts x 32 shift slots dx, N = 32 shift slots dy x R rights, K = every
+// row y and column x' (R = 4; R = 2 for batches too small to fill the GPU
+// with 4 x 4 tiles, so that twice the CTAs run, two per SM).  All CTAs
+// therefore do the same work, and each left's R x (2H-1)(2W-1) outputs --
+// contiguous in memory -- are written by one CTA as one run in whole
+// 32-byte sectors (a store that ends mid-sector costs a DRAM fill, which
+// dominated earlier layouts).
 //
 // Operand placement.  B is read from shared memory in the tensor cores'
 // no-swizzle K-major layout (8 rows x 16 bytes per core matrix, the two
@@ -67,25 +69,35 @@ using namespace tcx;
 constexpr int kThreads = 256;           // builder threads: 2 per A row (one K step each)
 constexpr int kABufs = 4;                // A stages in flight (overlap rows)
 constexpr int kLefts = 4;                 // lefts per tile (M = kLefts x kSlots)
-constexpr int kRights = 4;                // rights per tile (N = kSlots x kRights)
 constexpr int kSlots = 32;                // shifts dx (dy) per left (right): 2W-1 <= 31
 constexpr int kM = kLefts * kSlots;       // 128
-constexpr int kN = kRights * kSlots;      // 128
 constexpr int kPadL = 15;                 // zero columns left of a staged left row
 constexpr int kLRow = 64;                 // floats per staged left row
 constexpr int kSlotsR = 48;               // right row slots (2H + 30 <= 47 used)
-constexpr int kBBytes = 4 * kSlotsR * kRights * 16;   // staged B operand (hi or lo): 12 KB
-constexpr int kRunFloats = kRights * 31 * 31;   // one left's outputs in the epilogue
 constexpr int kStreams = 2;               // row streams: an issuing warp and accumulator each
-constexpr uint32_t kTmemCols = 512;       // 2 accumulators (128 each) + kABufs A stages (32 each)
-constexpr uint32_t kIdesc = tcx::idesc_tf32(kM, kN);
+
+// A tile of kLefts lefts x R rights (R = 4, or 2 for batches too small to
+// fill the GPU with 4 x 4 tiles: half as much work per CTA, and tensor
+// memory for two CTAs per SM).
+template <int R>
+struct TileShape {
+  static constexpr int kRights = R;
+  static constexpr int kN = R * kSlots;                       // 128 or 64
+  static constexpr int kBBytes = 4 * kSlotsR * R * 16;        // staged B (hi or lo): 12 / 6 KB
+  static constexpr int kRunFloats = R * 31 * 31;              // one left's outputs
+  // 2 accumulators + kABufs A stages (32 columns each), a power of two
+  static constexpr uint32_t kTmemCols = R == 4 ? 512 : 256;
+  static constexpr uint32_t kIdesc = tcx::idesc_tf32(kM, kN);
+  static constexpr int kMinBlocks = R == 4 ? 1 : 2;           // CTAs per SM
+  static_assert(kStreams * kN + kABufs * 32 <= int(kTmemCols), "tensor memory plan");
+};
 
 struct TcArgs {
   const float *left;
   const float *right;
   float *out;
   int nl, nr, H, W;
-  int mtiles, rtiles;    // tiles of kLefts lefts x kRights rights
+  int mtiles, rtiles;    // tiles of kLefts lefts x R rights
   int vec4;              // rows readable as float4
   int stall;             // test of the bounded waits: the last commit is left out
 };
@@ -107,9 +119,13 @@ __device__ int g_tc_status;   // bit 0: a bounded wait gave up
 // 2s and 2s + 1; stage b is handed over through two mbarriers: full[b] (one
 // arrival per builder warp once its part is in tensor memory) and empty[b]
 // (a tcgen05.commit: the products that read it have completed).
-template <int KH>
-__global__ void __launch_bounds__(kThreads + 32 * kStreams, 1)
+template <int KH, int R>
+__global__ void __launch_bounds__(kThreads + 32 * kStreams, TileShape<R>::kMinBlocks)
     xcorr_tc_kernel(const TcArgs a) {
+  using TS = TileShape<R>;
+  constexpr int kRights = TS::kRights, kN = TS::kN, kBBytes = TS::kBBytes;
+  constexpr int kRunFloats = TS::kRunFloats;
+  constexpr uint32_t kTmemCols = TS::kTmemCols, kIdesc = TS::kIdesc;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t *b_hi = smem;                                   // [4][kSlotsR][kRights][4] TF32 hi
   uint8_t *b_lo = smem + kBBytes;                         // same, lo parts
@@ -154,7 +170,7 @@ __global__ void __launch_bounds__(kThreads + 32 * kStreams, 1)
 #pragma unroll
     for (int k = 0; k < kBPer; ++k) {
       const int e = t + k * kThreads;
-      const int rq = e & (kRights - 1), q = e >> 2;
+      const int rq = e & (kRights - 1), q = e / kRights;
       const int slot = q % kSlotsR, xc = q / kSlotsR;
       const int yr = 2 * H - 2 - slot;
       bv[k] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -290,16 +306,16 @@ __global__ void __launch_bounds__(kThreads + 32 * kStreams, 1)
 
   if (!failed && !issuer) {
     // epilogue: warp w reads lanes 32 (w % 4) .. + 31 (left l0 + w % 4,
-    // shift slots dx) and columns 64 (w / 4) .. + 63 (shift slots dy 16 (w
-    // / 4) .. + 15 of all 4 rights) into the left's output run, laid out
-    // as in memory: [right][dy][dx]
+    // shift slots dx) and columns kN / 2 (w / 4) .. + kN / 2 - 1 (shift
+    // slots dy 16 (w / 4) .. + 15 of all R rights) of both accumulators
+    // into the left's output run, laid out as in memory: [right][dy][dx]
     const int lt = warp & 3, half = warp >> 2;
     const int ndy = 2 * H - 1, ndx = 2 * W - 1, per_pair = ndy * ndx;
     float *lrun = runs + lt * kRunFloats;
     const uint32_t lane_base = tmem + (uint32_t(32 * lt) << 16);
 #pragma unroll 1
-    for (int j = 0; j < 2; ++j) {
-      const int c0 = 64 * half + 32 * j;
+    for (int j = 0; j < kN / 64; ++j) {
+      const int c0 = (kN / 2) * half + 32 * j;
       uint32_t v[32], w[32];
       tmem_ld32(lane_base + uint32_t(c0), v);           // even rows' accumulator
       tmem_ld32(lane_base + uint32_t(kN + c0), w);      // odd rows' (none when H = 1)
@@ -310,9 +326,9 @@ __global__ void __launch_bounds__(kThreads + 32 * kStreams, 1)
       if (lane < ndx) {
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
-          const int c = c0 + k, dyi = c >> 2;          // c = dyi * 4 + rq
+          const int c = c0 + k, dyi = c / kRights;     // c = dyi * kRights + rq
           if (dyi < ndy)
-            lrun[(c & 3) * per_pair + dyi * ndx + lane] =
+            lrun[(c % kRights) * per_pair + dyi * ndx + lane] =
                 __uint_as_float(v[k]) + __uint_as_float(w[k]);
         }
       }
@@ -364,7 +380,11 @@ cudaError_t launch(const float *left, int nl, const float *right, int nr, int H,
   a.H = H;
   a.W = W;
   a.mtiles = (nl + kLefts - 1) / kLefts;
-  a.rtiles = (nr + kRights - 1) / kRights;
+  // 4 rights per tile once that gives 100+ tiles (measured on GB300: 32 x
+  // 64 of 16^2 9.8 us with 4 against 10.4 with 2), else 2 (16 x 16 of 16^2
+  // 8.1 against 9.5 us; 8 x 8 of 12^2 6.7 against 7.8 us)
+  const int R = (long long)a.mtiles * ((nr + 3) / 4) >= 100 ? 4 : 2;
+  a.rtiles = (nr + R - 1) / R;
   a.vec4 = (W % 4 == 0 && (reinterpret_cast<uintptr_t>(right) & 15) == 0) ? 1 : 0;
   // CORR_XCORR_TC_STALL=1 (read on every call): a test of the failure path
   // -- the kernel's last completion barrier is never signalled, each wait
@@ -376,10 +396,11 @@ cudaError_t launch(const float *left, int nl, const float *right, int nr, int H,
   }
   const long long blocks = (long long)a.mtiles * a.rtiles;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  const size_t smem = 2 * size_t(kBBytes) + size_t(kLefts) * 16 * kLRow * sizeof(float) +
-                      size_t(kLefts) * kRunFloats * sizeof(float) +
-                      (2 * kABufs + 2) * 8;
-  auto kern = W > 8 ? xcorr_tc_kernel<2> : xcorr_tc_kernel<1>;
+  const size_t bbytes = size_t(4) * kSlotsR * R * 16, run = size_t(R) * 31 * 31;
+  const size_t smem = 2 * bbytes + size_t(kLefts) * 16 * kLRow * sizeof(float) +
+                      size_t(kLefts) * run * sizeof(float) + (2 * kABufs + 2) * 8;
+  auto kern = R == 4 ? (W > 8 ? xcorr_tc_kernel<2, 4> : xcorr_tc_kernel<1, 4>)
+                     : (W > 8 ? xcorr_tc_kernel<2, 2> : xcorr_tc_kernel<1, 2>);
   cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void *>(kern));
   if (e != cudaSuccess) return e;
   kern<<<unsigned(blocks), kThreads + 32 * kStreams, smem, stream>>>(a);
