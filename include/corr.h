@@ -175,10 +175,12 @@ int corr_xcorr_f32_kernel(int nl, int nr, int H, int W, int *kind);
  * No counterpart on the pages: this is a deployment variant of
  * corr_xcorr_f32 with the same arguments, layouts and error codes.  It runs
  * the kernel corr_xcorr_f32 would run whenever that kernel's scratch fits
- * the array below, with bit-identical results; otherwise (large one-to-one
- * or one-to-many batches, whose tensor-core kernel keeps partial sums of
- * tens of megabytes) it runs the scalar kernel that fits, whose results
- * meet the same per-element bound but may differ in the last bits.
+ * the array below, with bit-identical results (the larger-matrix
+ * tensor-core kernel's partial tiles and item counter included: 1 x 32 of
+ * 64x64 needs 8 MiB); otherwise (larger one-to-one or one-to-many batches,
+ * e.g. one 256x256 pair, whose tensor-core partial tiles take 16 MiB and
+ * more) it runs the scalar kernel that fits, whose results meet the same
+ * per-element bound but may differ in the last bits.
  * corr_xcorr_f32 takes temporary device memory for the partial sums of large
  * matrices from a stream-ordered pool that may call the driver's allocator.
  * Some callers cannot allow that -- an application that reserves all device
@@ -190,8 +192,9 @@ int corr_xcorr_f32_kernel(int nl, int nr, int H, int W, int *kind);
  * process exits.
  *
  *   * Shapes whose partial sums need more than that return
- *     CORR_EUNSUPPORTED before anything is launched.  Only the large-matrix
- *     kernels use scratch, when they split the overlap rows into bands
+ *     CORR_EUNSUPPORTED before anything is launched.  Of the scalar
+ *     kernels only the large-matrix ones use scratch, when they split the
+ *     overlap rows into bands
  *     (more than 128 rows in a small batch: one 256x256 pair needs 2 MiB)
  *     or the rows into x segments (rows wider than about 770 floats: about
  *     48 bytes per matrix element, so one 1024x1024 pair needs 48 MiB and
