@@ -244,6 +244,18 @@ def test_tcl_row_unit_groups(tcl_on, monkeypatch, group, shape):
     run_check(rand_pos(nl, H, W), rand_pos(nr, H, W))
 
 
+@pytest.mark.parametrize("seed", range(4))
+def test_tcl_random_larger_shapes_in_groups(tcl_on, monkeypatch, seed):
+    """Random shapes with sides 90-160 (up to 5 row units, partial units at
+    both ends), 1-2 lefts, 1-5 rights, a random forced group size, on
+    non-negative inputs: every output against the oracle."""
+    rng = np.random.default_rng(970 + seed)
+    nl, nr = int(rng.integers(1, 3)), int(rng.integers(1, 6))
+    H, W = int(rng.integers(90, 161)), int(rng.integers(90, 161))
+    monkeypatch.setenv("CORR_XCORR_TCL_GROUP", str(int(rng.choice([1, 2, 3, 5]))))
+    run_check(rand_pos(nl, H, W), rand_pos(nr, H, W))
+
+
 def line_sums(v, w):
     """s[o] = sum_i v[i + o - (n - 1)] w[i] (n = len(v) = len(w)), in fp64:
     the sum of the full cross-correlation of two matrices over one output
