@@ -60,6 +60,9 @@ constexpr int kKY = 32;                   // overlap rows per unit
 constexpr int kKX = 32;                   // right columns per unit
 constexpr int kSteps = kKX / 8;           // 8-deep K steps per row
 constexpr int kStreams = 2;               // row streams, one issuer and accumulator each
+constexpr int kStagers = 2;               // warps staging the next units' operands
+constexpr int kStagerThreads = 32 * kStagers;
+constexpr int kAllThreads = kThreads + 32 * kStreams + kStagerThreads;
 constexpr int kBlockRows = 16;            // rows per block: kBlockRows / 2 per stream's chain
 constexpr int kABufs = 4;                 // A stages in tensor memory (2 per stream)
 constexpr int kStageCols = kSteps * 16;   // hi + lo columns of one A stage
@@ -88,9 +91,11 @@ constexpr size_t kRawOff = 2 * size_t(kBBuf);
 constexpr size_t kLpOff = kRawOff + size_t(kBHalf);
 constexpr size_t kInfoOff = kLpOff + 2 * size_t(kLBuf) * sizeof(float);
 constexpr size_t kBarOff = kInfoOff + kABufs * sizeof(uint2);
-constexpr int kBars = 2 * kABufs + 3;    // full, empty, chain done per stream, done
+// full, empty, chain done per stream, done, staging request, staging done
+constexpr int kBars = 2 * kABufs + 5;
 constexpr size_t kClaimOff = kBarOff + kBars * 8;
-constexpr size_t kSmemBytes = kClaimOff + 2 * sizeof(int) + 16;
+// two claimed-item slots, a staging request (B buffer, units u + 1, u + 2)
+constexpr size_t kSmemBytes = kClaimOff + (2 + 5) * sizeof(int) + 16;
 
 // row record flags (second word): first and last row of a chain, end of
 // the stream
@@ -242,15 +247,16 @@ __device__ __forceinline__ void cp_async_wait_all() {
 // <- R[r0 + r][yr][xa + 4 xc .. + 3] with yr = ya + kKY - 1 - dy0 - slot
 // (zero outside the matrix), 16 bytes each.  Thread t takes the entries
 // t + k kThreads, as in convert_b.
+template <int NT = kThreads>
 __device__ __forceinline__ void copy_b_raw(const TclArgs &a, const Item &it, int ky,
                                            uint32_t raw, int t, int NS) {
   const int H = a.H, W = a.W, NR = 1 << a.nr_log2;
   const int nent = 8 * NS * NR;
   const int yc = ky * kKY + kKY - 1 - it.dy0;
-  constexpr int kPer = (kMaxBEntries + kThreads - 1) / kThreads;
+  constexpr int kPer = (kMaxBEntries + NT - 1) / NT;
 #pragma unroll 2
   for (int k = 0; k < kPer; ++k) {
-    const int e = t + k * kThreads;
+    const int e = t + k * NT;
     if (e >= nent) break;
     const int r = e & (NR - 1), qq = e >> a.nr_log2;
     // qq / NS in floating point: exact for qq < 8 NS <= 2^11 (the error of
@@ -275,6 +281,7 @@ __device__ __forceinline__ void copy_b_raw(const TclArgs &a, const Item &it, int
 // Copy the left's rows y0 .. y1 - 1 of unit ky, columns xa + dx0 .. +
 // kLRowF - 1: lpu[y - y0][p] <- L[l][y][xa + dx0 + p] (zero outside the
 // matrix).
+template <int NT = kThreads>
 __device__ __forceinline__ void copy_lp(const TclArgs &a, const Item &it, int ky, uint32_t lpu,
                                         int t) {
   const int H = a.H, W = a.W;
@@ -283,10 +290,10 @@ __device__ __forceinline__ void copy_lp(const TclArgs &a, const Item &it, int ky
   const int nl_ent = (y1 - y0) * kLRowF;
   const float *lrow = a.left + size_t(it.l) * H * W;
   const int xb = it.xa + it.dx0;
-  constexpr int kPer = (kLBuf + kThreads - 1) / kThreads;
+  constexpr int kPer = (kLBuf + NT - 1) / NT;
 #pragma unroll 4
   for (int k = 0; k < kPer; ++k) {
-    const int i = t + k * kThreads;
+    const int i = t + k * NT;
     if (i >= nl_ent) break;
     const int p = i % kLRowF, ry = i / kLRowF;
     const int x = xb + p;
@@ -297,11 +304,12 @@ __device__ __forceinline__ void copy_lp(const TclArgs &a, const Item &it, int ky
 
 // B entries t + k kThreads of this thread's (landed) raw copies, split into
 // TF32 hi (bb) and lo (bb + kBHalf).
+template <int NT = kThreads>
 __device__ __forceinline__ void convert_b(const uint8_t *raw, uint8_t *bb, int t, int nent) {
-  constexpr int kPer = (kMaxBEntries + kThreads - 1) / kThreads;
-#pragma unroll
+  constexpr int kPer = (kMaxBEntries + NT - 1) / NT;
+#pragma unroll 4
   for (int k = 0; k < kPer; ++k) {
-    const int e = t + k * kThreads;
+    const int e = t + k * NT;
     if (e >= nent) break;
     const float4 v = *reinterpret_cast<const float4 *>(raw + e * 16);
     uint4 hi, lo;
@@ -348,8 +356,7 @@ __device__ __forceinline__ int builders_sync_or(int v) {
 // turn the raw rows of unit u + 1 (copied during unit u - 1) into its TF32
 // B and start the asynchronous copies of unit u + 2's raw rows and unit u +
 // 1's left rows, into the buffers unit u - 1 has just released.
-__global__ void __launch_bounds__(kThreads + 32 * kStreams, 1)
-    xcorr_tcl_kernel(const TclArgs a) {
+__global__ void __launch_bounds__(kAllThreads, 1) xcorr_tcl_kernel(const TclArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t *raw = smem + kRawOff;
   float *lp = reinterpret_cast<float *>(smem + kLpOff);                  // [2][kLBuf]
@@ -358,13 +365,17 @@ __global__ void __launch_bounds__(kThreads + 32 * kStreams, 1)
   uint64_t *empty = full + kABufs;                                       // [kABufs]
   uint64_t *chain = empty + kABufs;                                      // [kStreams]
   uint64_t *done = chain + 2;
+  uint64_t *stage_go = done + 1;      // a staging request is in req
+  uint64_t *stage_done = done + 2;    // the stagers finished it
   int *claimed = reinterpret_cast<int *>(smem + kClaimOff);             // [2]
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(claimed + 2);
+  int *req = claimed + 2;             // B buffer, unit u + 1 (b, ky), unit u + 2 (b, ky)
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(req + 5);
 
   const int NR = 1 << a.nr_log2, NS = kKY + a.ndy - 1;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int stream = warp - kThreads / 32;     // issuer warps: 0, 1; builders < 0
-  const bool issuer = stream >= 0;
+  const bool issuer = stream == 0 || stream == 1;
+  const bool stager = stream >= kStreams;
 
   if (stream == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -381,6 +392,8 @@ __global__ void __launch_bounds__(kThreads + 32 * kStreams, 1)
       mbar_init(smem_u32(&chain[0]), 1);
       mbar_init(smem_u32(&chain[1]), 1);
       mbar_init(smem_u32(done), kStreams);
+      mbar_init(smem_u32(stage_go), 1);
+      mbar_init(smem_u32(stage_done), kStagers);
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
   }
@@ -432,6 +445,34 @@ __global__ void __launch_bounds__(kThreads + 32 * kStreams, 1)
         if (!mbar_wait_bounded(smem_u32(&empty[2 * stream + b]), uint32_t(uses - 1) & 1u))
           failed = 1;
       }
+    }
+  } else if (stager) {
+    // Stagers: per request (sent once the last unit's products are done,
+    // so its B and left-row buffers are free), turn unit u + 1's raw rows
+    // into B, copy unit u + 2's raw rows and unit u + 1's left rows, wait
+    // for the copies and report; a request for no unit ends the loop.
+    const int st = t - (kThreads + 32 * kStreams);
+    const int nent = 8 * NS * NR;
+    const uint32_t raw_u32 = smem_u32(raw), lp_u32 = smem_u32(lp);
+    for (int k = 0;; ++k) {
+      if (!mbar_wait_bounded(smem_u32(stage_go), uint32_t(k) & 1u)) {
+        failed = 1;
+        break;
+      }
+      const int nb = req[0], rb1 = req[1], rky1 = req[2], rb2 = req[3], rky2 = req[4];
+      if (rb1 < 0) break;
+      convert_b<kStagerThreads>(raw, smem + nb * kBBuf, st, nent);
+      Item it;
+      if (rb2 >= 0) {
+        item_at(a, rb2, it);
+        copy_b_raw<kStagerThreads>(a, it, rky2, raw_u32, st, NS);
+      }
+      item_at(a, rb1, it);
+      copy_lp<kStagerThreads>(a, it, rky1, lp_u32 + uint32_t(nb * kLBuf) * 4, st);
+      cp_async_commit();
+      cp_async_wait_all();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(stage_done));
     }
   } else {
     // thread: A row m = 32 q + lane (shift dx = dx0 + m) with q = warp % 4,
@@ -514,6 +555,9 @@ __global__ void __launch_bounds__(kThreads + 32 * kStreams, 1)
     }
     failed = builders_sync_or(failed);
 
+    int nreq = 0, nreq_done = 0;   // staging requests sent, and waited for
+    bool stop_sent = false;
+
     // the chains of the last block, still to be taken in
     int pstreams = 0;         // streams that had rows in it (1 or 2; 0: none)
     int pitem = -1;           // its item, if the block ends that item
@@ -554,17 +598,18 @@ __global__ void __launch_bounds__(kThreads + 32 * kStreams, 1)
 #pragma unroll
         for (int k = 0; k < 32; ++k) sum[k] = 0.f;
       }
-      if (punit_end && b1 >= 0 && !failed) {
-        const int nbuf = (u + 1) & 1;
-        convert_b(raw, smem + nbuf * kBBuf, t, nent);
-        Item it;
-        if (b2 >= 0) {
-          item_at(a, b2, it);
-          copy_b_raw(a, it, ky2, raw_u32, t, NS);
+      if (punit_end && !failed && !stop_sent) {
+        // the last unit's products are done: ask the stagers for the next
+        // units (or, with none left, to stop)
+        if (t == 0) {
+          req[0] = (u + 1) & 1;
+          req[1] = b1;
+          req[2] = ky1;
+          req[3] = b2;
+          req[4] = ky2;
+          mbar_arrive(smem_u32(stage_go));
         }
-        item_at(a, b1, it);
-        copy_lp(a, it, ky1, lp_u32 + uint32_t(nbuf * kLBuf) * 4, t);
-        cp_async_commit();
+        if (b1 >= 0) ++nreq; else stop_sent = true;
       }
       pstreams = 0;
     };
@@ -624,6 +669,13 @@ __global__ void __launch_bounds__(kThreads + 32 * kStreams, 1)
       ++u;
       if (t == 0 && b2 >= 0 && is_item_end(b2, ky2)) claimed[u & 1] = claim_item(a);
       cp_async_wait_all();
+      // the next unit's operands from the stagers
+      if (nreq_done < nreq) {
+        if (t == 0 && !failed &&
+            !mbar_wait_bounded(smem_u32(stage_done), uint32_t(nreq_done) & 1u))
+          failed = 1;
+        ++nreq_done;
+      }
       failed = builders_sync_or(failed);
       if (failed) break;
       cb = b1;
@@ -635,6 +687,10 @@ __global__ void __launch_bounds__(kThreads + 32 * kStreams, 1)
     if (pstreams) {
       b1 = -1;
       take_in();
+    }
+    if (!stop_sent && t == 0) {          // the stagers end with a request for no unit
+      req[1] = -1;
+      mbar_arrive(smem_u32(stage_go));
     }
     cp_async_wait_all();                 // no copy in flight when the CTA ends
     // end of both row streams
@@ -790,7 +846,7 @@ cudaError_t launch(const float *left, int nl, const float *right, int nr, int H,
   if ((e = cudaMemsetAsync(a.counter, 0, sizeof(int), stream)) != cudaSuccess) return e;
   // persistent: one CTA per SM (its shared memory and tensor memory fill one)
   const long long ctas = a.items < device_sm_count() ? a.items : device_sm_count();
-  xcorr_tcl_kernel<<<unsigned(ctas), kThreads + 32 * kStreams, kSmemBytes, stream>>>(a);
+  xcorr_tcl_kernel<<<unsigned(ctas), kAllThreads, kSmemBytes, stream>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const long long outs = (long long)nl * nr * (2LL * H - 1) * ((2LL * W - 1 + 3) / 4);
   const long long cap = 8LL * device_sm_count() * 8;
