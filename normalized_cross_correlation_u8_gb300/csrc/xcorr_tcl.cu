@@ -32,7 +32,7 @@
 // no-swizzle K-major layout [x'/4][row slot][right][4 floats], rows in
 // reverse order, so the N rows of consecutive shifts dy are consecutive
 // slots and one descriptor per (y, 8 columns) reads them; two units are
-// staged at a time.  A (the Toeplitz rows of L) is written per overlap row
+// staged at a time, by two staging warps.  A (the Toeplitz rows of L) is written per overlap row
 // by sixteen builder warps straight into tensor memory (tcgen05.st); the
 // rows alternate between two streams, each with two A stages, one
 // accumulator and one warp issuing kind::tf32 tcgen05.mma, which reads per
@@ -352,10 +352,13 @@ __device__ __forceinline__ int builders_sync_or(int v) {
 // row 32 (warp % 4) + lane, columns 32 (warp / 4) .. + 31); at the end of
 // an item the running sum goes to its partial tile.
 //
-// Staging runs two units ahead: at the first block of unit u the builders
-// turn the raw rows of unit u + 1 (copied during unit u - 1) into its TF32
-// B and start the asynchronous copies of unit u + 2's raw rows and unit u +
-// 1's left rows, into the buffers unit u - 1 has just released.
+// Staging runs two units ahead on two staging warps: once the builders
+// have taken in unit u - 1's last chains (so its buffers are free), thread
+// 0 posts a request; the stagers turn the raw rows of unit u + 1 (copied
+// during unit u - 1) into its TF32 B, copy unit u + 2's raw rows and unit
+// u + 1's left rows, and report, which the builders check before unit u +
+// 1 starts.  (Done by the builders themselves, the staging kept both
+// issuers waiting at every unit's start.)
 __global__ void __launch_bounds__(kAllThreads, 1) xcorr_tcl_kernel(const TclArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t *raw = smem + kRawOff;
