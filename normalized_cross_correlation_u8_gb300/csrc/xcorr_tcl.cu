@@ -138,6 +138,7 @@ struct TclArgs {
   int *counter;          // items claimed so far (zero at launch)
   FastDiv fux, fugn, fnrt, fndyt, fndxt;   // the item index's radices
   float inv_ns;          // 1 / (kKY + ndy - 1), the right row slots of a unit
+  int stall;             // test of the bounded waits: the issuers' last commit is left out
   int vec4;              // rows readable as float4
 };
 
@@ -439,7 +440,7 @@ __global__ void __launch_bounds__(kAllThreads, 1) xcorr_tcl_kernel(const TclArgs
         mma_commit(smem_u32(&empty[s]));
         if (rec.y & kRecLast) mma_commit(smem_u32(&chain[stream]));
       }
-      mma_commit(smem_u32(done));
+      if (!a.stall) mma_commit(smem_u32(done));
       if (!mbar_wait_bounded(smem_u32(done), 0)) failed = 1;
       // each of this stream's stages: its last release has landed (no
       // arrival on this CTA's shared memory is left pending when it exits)
@@ -826,6 +827,14 @@ TclArgs make_args(const float *left, int nl, const float *right, int nr, int H, 
   a.fndyt = fast_div(a.ndyt);
   a.fndxt = fast_div(a.ndxt);
   a.inv_ns = 1.0f / float(kKY + a.ndy - 1);
+  // CORR_XCORR_TCL_STALL=1 (read on every call): a test of the failure path
+  // -- the issuers' last completion barrier is never signalled, their waits
+  // on it give up after about a second and corr_device_status() reports
+  // CORR_ETIMEOUT (the products themselves complete)
+  {
+    const char *v = getenv("CORR_XCORR_TCL_STALL");
+    a.stall = (v && v[0] == '1' && v[1] == '\0') ? 1 : 0;
+  }
   a.vec4 = (W % 4 == 0 && (reinterpret_cast<uintptr_t>(right) & 15) == 0) ? 1 : 0;
   return a;
 }

@@ -164,6 +164,24 @@ def test_bounded_wait_gives_up_and_reports(tc_on, monkeypatch):
     run_check(left, right)                     # context still usable, status clear
 
 
+def test_tcl_bounded_wait_gives_up_and_reports(tcl_on, monkeypatch):
+    """The larger-matrix kernel's failure path without a fault:
+    CORR_XCORR_TCL_STALL=1 leaves out the issuers' last completion signal,
+    so their waits on it run out after about a second; corr_device_status
+    reports CORR_ETIMEOUT, and the next call on the same context works."""
+    dev = torch.device("cuda", 0)
+    left, right = rand(1, 64, 64), rand(2, 64, 64)
+    L, R = torch.from_numpy(left).to(dev), torch.from_numpy(right).to(dev)
+    out = torch.empty((1, 2, 127, 127), dtype=torch.float32, device=dev)
+    monkeypatch.setenv("CORR_XCORR_TCL_STALL", "1")
+    corr.xcorr_f32_into(L, R, out)
+    with pytest.raises(corr.CorrError) as e:
+        corr.device_status()
+    assert e.value.code == -4                  # CORR_ETIMEOUT
+    monkeypatch.delenv("CORR_XCORR_TCL_STALL")
+    run_check(left, right)                     # context still usable, status clear
+
+
 @pytest.mark.parametrize("seed", range(6))
 def test_tc_random_shapes(tc_on, seed):
     """Random batch shapes within the small-matrix kernel's range."""
